@@ -1,0 +1,207 @@
+"""Pins of the oracle's number formats and group quantisers (C1, C3).
+
+Each check compares the oracle with something other than itself: the OCP
+anchor values in tests/golden, torch's own fp32->float8_e4m3fn / bfloat16
+conversions (a library routine), closed forms and hand-picked groups.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line.split()
+
+
+def test_e2m1_decode_all_codes(orc):
+    # OCP MX E2M1 grid, magnitude by 3-bit code, sign in bit 3
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        v = orc.e2m1_decode(c)
+        assert abs(v) == grid[c & 7]
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)
+
+
+def test_e2m1_encode_rne_golden(orc):
+    for x, want in _rows("e2m1_rne.txt"):
+        got = orc.e2m1_decode(orc.e2m1_encode(float(x)))
+        assert got == float(want), (x, got, want)
+
+
+def test_e2m1_roundtrip_and_negative_zero(orc):
+    for c in range(16):
+        assert orc.e2m1_encode(orc.e2m1_decode(c)) == c
+    assert orc.e2m1_encode(-0.1) == 0x8  # rounds to zero, keeps the sign bit
+    assert orc.e2m1_encode(0.1) == 0x0
+
+
+def test_e4m3_decode_golden(orc):
+    for code, want in _rows("e4m3_known.txt"):
+        v = orc.e4m3_decode(int(code, 16))
+        assert v == float(want) and math.copysign(1, v) == math.copysign(1, float(want))
+    assert math.isnan(orc.e4m3_decode(0x7F)) and math.isnan(orc.e4m3_decode(0xFF))
+
+
+def test_e4m3_decode_matches_torch_all_codes(orc):
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        v = orc.e4m3_decode(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(v)
+        else:
+            assert v == ref[c], c
+
+
+def test_e4m3_encode_matches_torch(orc):
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * 20,
+        rng.uniform(-448, 448, 2000).astype(np.float32),
+        rng.uniform(-2 ** -6, 2 ** -6, 1000).astype(np.float32),  # subnormal range
+        np.array([0.0, -0.0, 2 ** -10, 3 * 2 ** -11, 448.0, 447.9, 0.0146484375], np.float32),
+    ])
+    # all exact midpoints between neighbouring finite codes
+    vals = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)
+    xs = np.concatenate([xs, mids, -mids])
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(xs, ref):
+        assert orc.e4m3_encode(float(x)) == int(r), (x, r)
+
+
+def test_e4m3_satfinite(orc):
+    assert orc.e4m3_encode(1e6) == 0x7E
+    assert orc.e4m3_encode(-1e6) == 0xFE
+    assert orc.e4m3_encode(460.0) == 0x7E
+
+
+def test_e4m3_roundtrip_all_finite(orc):
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert orc.e4m3_encode(orc.e4m3_decode(c)) == c
+
+
+def test_e8m0(orc):
+    assert orc.e8m0_decode(127) == 1.0
+    assert orc.e8m0_decode(128) == 2.0
+    assert orc.e8m0_decode(0) == 2.0 ** -127
+    assert orc.e8m0_decode(254) == 2.0 ** 127
+    assert math.isnan(orc.e8m0_decode(255))
+
+
+def test_bf16_matches_torch(orc):
+    rng = np.random.default_rng(3)
+    xs = np.concatenate([rng.standard_normal(4000).astype(np.float32) * 10,
+                         np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -0.0, 1e-40], np.float32)])
+    tb = torch.from_numpy(xs).to(torch.bfloat16)
+    ref = tb.view(torch.int16).numpy().astype(np.uint16)
+    back = tb.float().numpy()
+    for x, r, b in zip(xs, ref, back):
+        assert orc.bf16_encode(float(x)) == int(r)
+        assert orc.bf16_decode(int(r)) == float(b)
+
+
+# ---------------------------------------------------------------- groups (C3)
+GRID = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0, 6.0]
+
+
+def test_nvfp4_identity_on_grid(orc):
+    codes, sc = orc.nvfp4_quant16(GRID)
+    assert orc.e4m3_decode(sc) == 1.0  # amax 6 -> scale exactly 1
+    back = orc.dequant_nvfp4(codes[None], np.array([[sc]]))[0]
+    assert list(back) == GRID
+
+
+def test_nvfp4_max_2688(orc):
+    # P4: with a per-16 E4M3 scale the largest representable value is 448 * 6
+    x = np.array(GRID, np.float32) * 448
+    codes, sc = orc.nvfp4_quant16(x)
+    assert orc.e4m3_decode(sc) == 448.0
+    back = orc.dequant_nvfp4(codes[None], np.array([[sc]]))[0]
+    assert back.max() == 2688.0
+    assert list(back) == list(x.astype(np.float64))
+
+
+def test_nvfp4_post_rope_bound_does_not_saturate_scale(orc):
+    # P4: post-RoPE KV stays within ~22.6, far below the 2688 range: the scale never saturates
+    x = np.linspace(-22.6, 22.6, 16).astype(np.float32)
+    codes, sc = orc.nvfp4_quant16(x)
+    assert orc.e4m3_decode(sc) < 448
+    back = orc.dequant_nvfp4(codes[None], np.array([[sc]]))[0]
+    assert np.max(np.abs(back - x)) <= 0.5 * orc.e4m3_decode(sc) * 2 + 1e-6
+
+
+def test_nvfp4_midpoints_even(orc):
+    # unit scale (amax 6), midpoints between grid points go to the even code
+    x = np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5,
+                  -3.5, -5.0, 0.0], np.float32)
+    codes, sc = orc.nvfp4_quant16(x)
+    back = orc.dequant_nvfp4(codes[None], np.array([[sc]]))[0]
+    assert list(back) == [6.0, 0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0, -0.0, -1.0, -1.0, -2.0, -2.0,
+                          -4.0, -4.0, 0.0]
+
+
+def test_nvfp4_zero_and_tiny_group(orc):
+    codes, sc = orc.nvfp4_quant16(np.zeros(16))
+    assert sc == 0 and not codes.any()
+    # amax/6 below half the smallest E4M3 subnormal -> scale 0 -> all codes 0
+    codes, sc = orc.nvfp4_quant16(np.full(16, 1e-3, np.float32))
+    assert sc == 0 and not codes.any()
+
+
+def test_nvfp4_error_bound_random(orc):
+    # every value is within half a grid step (times the decoded scale) of its code,
+    # unless it saturated at 6 * s
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        x = rng.standard_normal(16).astype(np.float32) * rng.uniform(0.01, 50)
+        codes, sc = orc.nvfp4_quant16(x)
+        s = orc.e4m3_decode(sc)
+        back = orc.dequant_nvfp4(codes[None], np.array([[sc]]))[0]
+        y = x.astype(np.float64) / s
+        step = np.where(np.abs(y) < 2, 0.5, np.where(np.abs(y) < 4, 1.0, 2.0))
+        sat = np.abs(y) > 6
+        assert np.all(sat | (np.abs(back / s - y) <= step / 2 + 1e-9))
+
+
+def test_mxfp4_identity_on_scaled_grids(orc):
+    for k in (-5, -2, 0, 1, 3, 7):
+        x = np.array(GRID + GRID, np.float32) * np.float32(2.0 ** k)
+        codes, sc = orc.mxfp4_quant32(x)
+        assert sc == 127 + k
+        back = orc.dequant_mxfp4(codes[None], np.array([[sc]]))[0]
+        assert list(back) == list(x.astype(np.float64))
+
+
+def test_mxfp4_scale_rule(orc):
+    # e = floor(log2 amax) - 2, exactly at powers of two and just below them
+    for amax, e in ((4.0, 0), (3.9999998, -1), (1.0, -2), (0.75, -3), (1024.0, 8)):
+        x = np.zeros(32, np.float32)
+        x[5] = amax
+        _, sc = orc.mxfp4_quant32(x)
+        assert sc - 127 == e, (amax, sc)
+    codes, sc = orc.mxfp4_quant32(np.zeros(32))
+    assert sc == 0 and not codes.any()
+
+
+def test_mxfp8_identity_and_scale(orc):
+    vals = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    x = np.concatenate([vals[-16:], -vals[-16:]]).astype(np.float32)  # amax 448 -> e = 0
+    codes, sc = orc.mxfp8_quant32(x)
+    assert sc == 127
+    back = np.array([orc.e4m3_decode(c) for c in codes])
+    assert list(back) == list(x.astype(np.float64))
+    x2 = x * np.float32(2.0 ** -6)
+    codes2, sc2 = orc.mxfp8_quant32(x2)
+    assert sc2 == 121 and list(codes2) == list(codes)
