@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Throughput of the CSA2 decode step on one GB300 (one process per GPU).
+
+Default workload (N=1): Full-layer decode, batch 32, context 65,536 per
+sequence, 64 query heads, 64 indexer heads x 128, top-512, 8-bit window.
+One step = the whole hot path for that layer on one batch: append the step's
+token (RoPE + quantise into the FP4 cache and the window), score every visible
+position, select the top 512 and build the 2,048-block candidate pool, attend
+over the selected entries plus the window.  Inputs are seeded synthetic data
+(N(0,1) KV and queries, U(0,1) head weights) resident in HBM before timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "decode tokens/s and KV HBM GB/s (% of roofline) at 64K-1M context, 1 GB300"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+def decode_step_bytes(B, T, H, H_I, k, swa_dtype):
+    """Algorithmic HBM bytes of one Full-layer decode step (what the method must move)."""
+    keys = B * T * 68                                  # indexer keys of every visible position
+    qidx = B * (H_I * 128 * 2 + 4 * H_I)               # indexer query (bf16) + head weights
+    sel = B * k * (324 + 4)                            # selected entries (288 + 36 sidecar) + index
+    swa = B * 128 * (594 if swa_dtype == 1 else 1152)  # window entries
+    q = B * H * 576 * 2                                # absorbed query
+    out = B * H * 512 * 4 + B * H * 4                  # output + lse
+    append = B * ((576 + 128) * 4 + 324 + 68 + (594 if swa_dtype == 1 else 1152))
+    return {"keys": keys, "qidx": qidx, "attn": sel + swa + q + out, "append": append,
+            "total": keys + qidx + sel + swa + q + out + append}
+
+
+class FullDecode:
+    """Full-layer decode on a batch: caches built through csa2_kv_append."""
+
+    def __init__(self, W, n_steps, device):
+        from fp4_compressed_sparse_gb300 import csa2
+        self.csa2 = csa2
+        self.W = W
+        B, ctx = W.batch, W.context
+        self.cap = ctx + n_steps + 8
+        self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
+        self.rope = csa2.rope_table(W.theta, self.cap + 8)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        chunk = 8192
+        for t0 in range(0, ctx, chunk):
+            n = min(chunk, ctx - t0)
+            kv = torch.stack([W.kv(b, t0, n, device=device) for b in range(B)])
+            ik = torch.stack([W.ik(b, t0, n, device=device) for b in range(B)])
+            csa2.kv_append(self.cache, kv, ik, self.rope, err=self.err)
+            del kv, ik
+        torch.cuda.synchronize()
+        # per-step inputs (resident in HBM)
+        self.kv_new = [torch.stack([W.kv(b, ctx + s, 1, device=device) for b in range(B)])
+                       for s in range(n_steps)]
+        self.ik_new = [torch.stack([W.ik(b, ctx + s, 1, device=device) for b in range(B)])
+                       for s in range(n_steps)]
+        self.q_idx = [W.q_idx(s, 0, device=device) for s in range(n_steps)]
+        self.w = [W.w(s, 0, device=device) for s in range(n_steps)]
+        self.q = [W.q(s, 0, device=device) for s in range(n_steps)]
+        self.q_pos = [torch.full((B,), ctx + s, dtype=torch.int64, device=device) for s in range(n_steps)]
+        self.scores = torch.empty((B, self.cap), device=device)
+        self.idx = torch.empty((B, W.topk), dtype=torch.int32, device=device)
+        self.pool = torch.empty((B, W.pool_blocks), dtype=torch.int32, device=device)
+        self.pool_cnt = torch.empty((B,), dtype=torch.int32, device=device)
+        self.out = torch.empty((B, W.heads, 512), device=device)
+        self.lse = torch.empty((B, W.heads), device=device)
+        self.ws_topk = csa2.topk_workspace(B, self.cap, W.topk, W.pool_blocks)
+        self.ws_attn = csa2.attn_workspace(B, W.heads, W.topk)
+        self.launches_per_step = None
+
+    def step(self, s, ev=None):
+        c, W = self.csa2, self.W
+        if ev is not None:
+            ev[0].record()
+        c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+        if ev is not None:
+            ev[1].record()
+        c.index_score(self.cache, self.q_idx[s], self.w[s], self.q_pos[s], self.scores, err=self.err)
+        if ev is not None:
+            ev[2].record()
+        c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
+               pool_count=self.pool_cnt, err=self.err)
+        if ev is not None:
+            ev[3].record()
+        c.sparse_attn_decode(self.cache, self.q[s], self.q_pos[s], self.idx, self.out, self.lse,
+                             self.ws_attn, W.sm_scale, err=self.err)
+        if ev is not None:
+            ev[4].record()
+
+    @staticmethod
+    def kernel_launches(n_splits_gt1=False):
+        # kv_append ratio 1: append + advance; index_score: 1; topk: 3 x (hist, resolve) + count
+        # + write, twice (top-k, then the pool); attention: 1 (+ combine when split)
+        return 2 + 1 + 16 + 1 + (1 if n_splits_gt1 else 0)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    from fp4_compressed_sparse_gb300 import build_lib, csa2
+    from fp4_compressed_sparse_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build_lib.build()
+    csa2.load()
+    W = getattr(wl, args.workload)(device="cuda")
+    # weak scaling: every rank runs its own batch (independent sequences), seeds offset by rank
+    W.seed = W.seed + 1000 * rank
+    n_steps = args.warmup + args.steps + args.e2e_steps
+    bench = FullDecode(W, n_steps, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+
+    for s in range(args.warmup):
+        flush.zero_()
+        bench.step(s)
+    torch.cuda.synchronize()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flushed between timed steps (outside the events)
+        bench.step(args.warmup + i, evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    score_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    parts = {"append": [e[0].elapsed_time(e[1]) for e in evs], "score": score_ms,
+             "topk_pool": [e[2].elapsed_time(e[3]) for e in evs],
+             "attention": [e[3].elapsed_time(e[4]) for e in evs]}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = W.batch * world * args.steps
+    value = tokens / (total_ms / 1e3)
+
+    hbm, hbm_kind = peaks()
+    T = W.context + args.warmup + args.steps // 2
+    nbytes = decode_step_bytes(W.batch, T, W.heads, W.index_heads, W.topk, W.swa_dtype)
+    kv_gbs = nbytes["total"] / (ms_per_step / 1e3) / 1e9
+    score_avg = statistics.mean(score_ms)
+    score_bytes = nbytes["keys"] + nbytes["qidx"]
+    achieved = score_bytes / (score_avg / 1e3) / 1e9
+
+    # end to end through the public API: host inputs (pinned) -> device, step, result -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e(bench, W, args, dev, flush)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4/bf16/fp32",
+        "data": "synthetic (seeded N(0,1) KV/queries, U(0,1) head weights)",
+        "config": {"workload": W.name, "batch": W.batch, "context": W.context, "heads": W.heads,
+                   "index_heads": W.index_heads, "topk": W.topk, "window": 128,
+                   "window_dtype": "mxfp8" if W.swa_dtype == 1 else "bf16",
+                   "pool_blocks": W.pool_blocks, "l2": "flushed between timed steps (256 MB write)",
+                   "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
+        "kv_hbm": {"algorithmic_bytes_per_step": nbytes["total"], "gbs": round(kv_gbs, 1),
+                   "frac": round(kv_gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind},
+        "roofline": {"kernel": "index_score (Full scan)", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": round(score_avg, 5),
+                     "peak_kind": hbm_kind},
+        "step_breakdown_ms": {k: round(statistics.mean(v), 5) for k, v in parts.items()},
+        "gpu_launches": FullDecode.kernel_launches(
+            csa2.load().csa2_attn_workspace_size(W.batch, W.heads, W.topk) > 256) * args.steps,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(W, args, sample_steps=1)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(bench, W, args, dev, flush):
+    """Same metric through the public calls with host buffers: every step copies its
+    inputs (new token, indexer query, head weights, query, positions) from pinned host
+    memory and reads the step's result (attention output + lse) back to the host."""
+    first = args.warmup + args.steps
+    names = ("kv_new", "ik_new", "q_idx", "w", "q", "q_pos")
+    host_in = [[getattr(bench, n)[first + s].cpu().pin_memory() for n in names]
+               for s in range(args.e2e_steps)]
+    dev_in = [torch.empty_like(getattr(bench, n)[first]) for n in names]
+    out_h = torch.empty(bench.out.shape, dtype=bench.out.dtype).pin_memory()
+    lse_h = torch.empty(bench.lse.shape, dtype=bench.lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in[0])
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    for n, d in zip(names, dev_in):  # the step reads slot `first` of each input list
+        getattr(bench, n)[first] = d
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for s in range(args.e2e_steps):
+        flush.zero_()
+        start.record()
+        for d, h in zip(dev_in, host_in[s]):
+            d.copy_(h, non_blocking=True)
+        bench.step(first)
+        out_h.copy_(bench.out, non_blocking=True)
+        lse_h.copy_(bench.lse, non_blocking=True)
+        end.record()
+        torch.cuda.synchronize()
+        total += start.elapsed_time(end)
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} in the e2e steps")
+    value = W.batch * args.e2e_steps / (total / 1e3)
+    return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "ms_per_step": round(total / args.e2e_steps, 4)}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def cpu_baseline(W, args, sample_steps=1):
+    """The CPU oracle (as it stands) on a bounded sample of the workload: sequence 0,
+    `sample_steps` decode steps (append the token, Full-layer score over every visible
+    position, top-k, pool, attention), on the host cores."""
+    import numpy as np
+    from oracle import oracle as orc
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    orc.build()
+    cache = orc.Cache(W.context + sample_steps + 8, swa_dtype=W.swa_dtype)
+    chunk = 8192
+    for t0 in range(0, W.context, chunk):
+        n = min(chunk, W.context - t0)
+        orc.append_r1(cache, W.kv(0, t0, n, device=dev).cpu().numpy(),
+                      W.ik(0, t0, n, device=dev).cpu().numpy(), W.theta)
+    u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    t_total = 0.0
+    for s in range(sample_steps):
+        kv = W.kv(0, W.context + s, 1, device=dev).cpu().numpy()
+        ik = W.ik(0, W.context + s, 1, device=dev).cpu().numpy()
+        q_idx = u16(W.q_idx(s, 0, device=dev)[0])
+        w = W.w(s, 0, device=dev)[0].cpu().numpy()
+        q = u16(W.q(s, 0, device=dev)[0])
+        t0 = time.perf_counter()
+        orc.append_r1(cache, kv, ik, W.theta)
+        orc.full_layer(cache, q_idx, w, q, W.context + s, W.topk, W.sm_scale)
+        t_total += time.perf_counter() - t0
+    return {"value": round(sample_steps / t_total, 4), "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(t_total, 3),
+            "sample": f"sequence 0 x {sample_steps} decode step(s) of {W.name}: append + Full-layer "
+                      f"score over {W.context} positions x {W.index_heads} heads + top-{W.topk} + "
+                      f"pool + attention ({W.heads} heads)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from fp4_compressed_sparse_gb300 import workloads as wl
+    W = getattr(wl, args.workload)(device="cuda" if torch.cuda.is_available() else "cpu")
+    steps = max(1, args.steps)
+    cb = cpu_baseline(W, args, sample_steps=steps)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * cb["seconds"] / steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
+            "data": "synthetic (seeded)", "config": {"workload": W.name, "batch": W.batch,
+                                                      "context": W.context, "heads": W.heads,
+                                                      "index_heads": W.index_heads, "topk": W.topk},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="full_decode", choices=["full_decode", "tiny_decode"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

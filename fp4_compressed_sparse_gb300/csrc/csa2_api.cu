@@ -1,0 +1,540 @@
+// csa2_api.cu -- the libcsa2 C ABI: host-side validation, workspace sizing and
+// launches.  See include/csa2.h for the contract of every entry point.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "csa2_encode.cuh"
+#include "csa2_internal.cuh"
+
+namespace {
+
+thread_local std::string g_detail;
+
+csa2_status fail(csa2_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+csa2_status fail(csa2_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return st;
+}
+
+csa2_status cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return CSA2_OK;
+  return fail(CSA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, status, ...) \
+  do {                             \
+    if (!(cond)) return fail(status, __VA_ARGS__); \
+  } while (0)
+
+#define REQUIRE_PTR(p)                                                   \
+  do {                                                                   \
+    if ((p) == nullptr) return fail(CSA2_ERR_NULL, "%s is NULL", #p);    \
+    if (!aligned16(p)) return fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+#define REQUIRE_OPT_PTR(p)                                               \
+  do {                                                                   \
+    if ((p) != nullptr && !aligned16(p)) return fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+csa2_status check_cache(const csa2_cache *c) {
+  REQUIRE(c != nullptr, CSA2_ERR_NULL, "cache is NULL");
+  REQUIRE(c->batch >= 1 && c->batch <= 65535, CSA2_ERR_SHAPE, "cache batch %d outside 1..65535", c->batch);
+  REQUIRE(c->capacity >= 1 && c->capacity <= (1 << 30), CSA2_ERR_SHAPE, "cache capacity %d outside 1..2^30",
+          c->capacity);
+  REQUIRE(c->ratio == 1 || c->ratio == 2, CSA2_ERR_RANGE, "cache ratio %d (must be 1 or 2)", c->ratio);
+  REQUIRE(c->swa_dtype == CSA2_SWA_BF16 || c->swa_dtype == CSA2_SWA_MXFP8, CSA2_ERR_RANGE, "swa_dtype %d",
+          c->swa_dtype);
+  REQUIRE_PTR(c->lat_codes);
+  REQUIRE_PTR(c->lat_scales);
+  REQUIRE_PTR(c->rope_codes);
+  REQUIRE_PTR(c->rope_scales);
+  REQUIRE_PTR(c->idx_codes);
+  REQUIRE_PTR(c->idx_scales);
+  REQUIRE_PTR(c->swa_codes);
+  if (c->swa_dtype == CSA2_SWA_MXFP8) REQUIRE_PTR(c->swa_scales);
+  REQUIRE_PTR(c->n_tokens);
+  if (c->ratio == 2) REQUIRE_PTR(c->cmp_buf);
+  return CSA2_OK;
+}
+
+// A view of one sequence of a cache (batch 1).
+csa2_cache seq_view(const csa2_cache &c, int seq) {
+  csa2_cache v = c;
+  const size_t e = static_cast<size_t>(seq) * c.capacity;
+  v.batch = 1;
+  v.lat_codes += e * 256;
+  v.lat_scales += e * 32;
+  v.rope_codes += e * 32;
+  v.rope_scales += e * 4;
+  v.idx_codes += e * 64;
+  v.idx_scales += e * 4;
+  v.swa_codes += static_cast<size_t>(seq) * csa2::kWin * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
+  if (v.swa_scales) v.swa_scales += static_cast<size_t>(seq) * csa2::kWin * csa2::kSwaScaleStride;
+  if (v.cmp_buf) v.cmp_buf += static_cast<size_t>(seq) * 4 * 4 * csa2::kDcmp;
+  v.n_tokens += seq;
+  return v;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+}  // namespace
+
+// ===================================================================== prefill kernels
+namespace csa2 {
+namespace {
+
+// P = n_tokens (before the append), q_pos[i] = P + i, and a copy of the window ring.
+__global__ void k_prefill_snapshot(csa2_cache v, int Q, int64_t *P, int64_t *q_pos, uint8_t *ring_codes,
+                                   uint8_t *ring_scales) {
+  const int64_t p0 = v.n_tokens[0];
+  const int tid = blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid == 0) *P = p0;
+  for (int i = tid; i < Q; i += gridDim.x * blockDim.x) q_pos[i] = p0 + i;
+  const int cb = v.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+  const int n16 = kWin * cb / 16;
+  for (int i = tid; i < n16; i += gridDim.x * blockDim.x)
+    reinterpret_cast<uint4 *>(ring_codes)[i] = reinterpret_cast<const uint4 *>(v.swa_codes)[i];
+  if (v.swa_scales)
+    for (int i = tid; i < kWin * kSwaScaleStride / 16; i += gridDim.x * blockDim.x)
+      reinterpret_cast<uint4 *>(ring_scales)[i] = reinterpret_cast<const uint4 *>(v.swa_scales)[i];
+}
+
+// Window rows of every chunk token: its own C^a[0:576], rotated at P+i.
+__global__ void __launch_bounds__(256) k_prefill_window(const float *ca, int Q, const int64_t *P, const float *rope_cs,
+                                                        int64_t rope_len, int swa_dtype, uint8_t *lin_codes,
+                                                        uint8_t *lin_scales) {
+  __shared__ float srow[8][kDqk];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * 8 + warp;
+  if (i >= Q) return;
+  const int64_t t = *P + i;
+  if (t >= rope_len) return;  // the append reports the ROPE error
+  for (int d = lane; d < kDqk; d += 32) srow[warp][d] = ca[static_cast<size_t>(i) * kDcmp + d];
+  __syncwarp();
+  const int cb = swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+  warp_encode_swa(lin_codes + static_cast<size_t>(i) * cb,
+                  lin_scales ? lin_scales + static_cast<size_t>(i) * kSwaScaleStride : nullptr, swa_dtype,
+                  srow[warp], rope_cs + t * 64, lane);
+}
+
+}  // namespace
+}  // namespace csa2
+
+// ===================================================================== C ABI
+extern "C" {
+
+int32_t csa2_version(void) { return 100; }
+
+const char *csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_NULL: return "a required pointer is NULL";
+    case CSA2_ERR_SHAPE: return "a size is outside its documented range";
+    case CSA2_ERR_ALIGN: return "a device pointer is not 16-byte aligned";
+    case CSA2_ERR_RANGE: return "an argument is out of range";
+    case CSA2_ERR_UNSUPPORTED: return "not supported";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+const char *csa2_last_error_detail(void) { return g_detail.c_str(); }
+
+size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane, int32_t swa_dtype) {
+  const size_t e = static_cast<size_t>(batch) * capacity;
+  switch (plane) {
+    case 0: return e * 256;
+    case 1: return e * 32;
+    case 2: return e * 32;
+    case 3: return e * 4;
+    case 4: return e * 64;
+    case 5: return e * 4;
+    case 6: return static_cast<size_t>(batch) * csa2::kWin * (swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
+    case 7: return static_cast<size_t>(batch) * csa2::kWin * csa2::kSwaScaleStride;
+    case 8: return static_cast<size_t>(batch) * 4 * 4 * csa2::kDcmp * sizeof(float);
+    case 9: return static_cast<size_t>(batch) * sizeof(int64_t);
+  }
+  return 0;
+}
+
+csa2_status csa2_rope_table(double theta, int64_t n_pos, float *out_host) {
+  REQUIRE(out_host != nullptr, CSA2_ERR_NULL, "out_host is NULL");
+  REQUIRE(n_pos >= 0, CSA2_ERR_SHAPE, "n_pos %lld < 0", static_cast<long long>(n_pos));
+  REQUIRE(theta > 0.0, CSA2_ERR_RANGE, "theta must be > 0");
+  double inv_freq[csa2::kRope / 2];
+  for (int i = 0; i < csa2::kRope / 2; ++i) inv_freq[i] = std::pow(theta, -static_cast<double>(2 * i) / csa2::kRope);
+  for (int64_t p = 0; p < n_pos; ++p)
+    for (int i = 0; i < csa2::kRope / 2; ++i) {
+      const double ang = static_cast<double>(p) * inv_freq[i];
+      out_host[p * 64 + 2 * i] = static_cast<float>(std::cos(ang));
+      out_host[p * 64 + 2 * i + 1] = static_cast<float>(std::sin(ang));
+    }
+  return CSA2_OK;
+}
+
+csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *idx_key, int32_t in_dtype,
+                           const csa2_compress_in *cmp, const float *rope_cs, int64_t rope_len, int32_t n_new,
+                           float *cmp_dbg, int32_t *err_word, csa2_stream_t stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  REQUIRE(n_new >= 0, CSA2_ERR_SHAPE, "n_new %d < 0", n_new);
+  REQUIRE_PTR(rope_cs);
+  REQUIRE(rope_len >= 1, CSA2_ERR_SHAPE, "rope_len %lld < 1", static_cast<long long>(rope_len));
+  REQUIRE_OPT_PTR(cmp_dbg);
+  if (cache->ratio == 1) {
+    REQUIRE(cmp == nullptr, CSA2_ERR_RANGE, "cmp must be NULL for a ratio-1 cache");
+    REQUIRE(in_dtype == CSA2_IN_F32 || in_dtype == CSA2_IN_BF16, CSA2_ERR_RANGE, "in_dtype %d", in_dtype);
+    REQUIRE_PTR(kv);
+    REQUIRE_PTR(idx_key);
+  } else {
+    REQUIRE(cmp != nullptr, CSA2_ERR_NULL, "cmp is NULL for a ratio-2 cache");
+    REQUIRE_PTR(cmp->ca);
+    REQUIRE_PTR(cmp->cb);
+    REQUIRE_PTR(cmp->za);
+    REQUIRE_PTR(cmp->zb);
+    REQUIRE_PTR(cmp->ba);
+    REQUIRE_PTR(cmp->bb);
+  }
+  if (n_new == 0) return CSA2_OK;
+  return cuda_status(csa2::launch_kv_append(*cache, kv, idx_key, in_dtype, cmp, rope_cs, rope_len, n_new, cmp_dbg,
+                                            err_word, reinterpret_cast<cudaStream_t>(stream)),
+                     "csa2_kv_append launch");
+}
+
+csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w, int32_t n_heads_idx,
+                             const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
+                             int32_t pool_block_size, float *scores, int64_t score_stride, int32_t *err_word,
+                             csa2_stream_t stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  REQUIRE_PTR(q_idx);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(q_pos);
+  REQUIRE_PTR(scores);
+  REQUIRE(n_heads_idx >= 1 && n_heads_idx <= CSA2_MAX_HEADS, CSA2_ERR_SHAPE, "n_heads_idx %d outside 1..128",
+          n_heads_idx);
+  if (pool) {
+    REQUIRE_PTR(pool);
+    REQUIRE(pool_blocks >= 1 && pool_block_size >= 1 && pool_block_size <= 64, CSA2_ERR_SHAPE,
+            "pool_blocks %d / pool_block_size %d", pool_blocks, pool_block_size);
+    REQUIRE(score_stride >= static_cast<int64_t>(pool_blocks) * pool_block_size, CSA2_ERR_SHAPE,
+            "score_stride %lld < pool_blocks*pool_block_size", static_cast<long long>(score_stride));
+  } else {
+    REQUIRE(score_stride >= cache->capacity, CSA2_ERR_SHAPE, "score_stride %lld < capacity %d",
+            static_cast<long long>(score_stride), cache->capacity);
+  }
+  csa2::ScoreArgs a{};
+  a.idx_codes = cache->idx_codes;
+  a.idx_scales = cache->idx_scales;
+  a.cap = cache->capacity;
+  a.ratio = cache->ratio;
+  a.rows = cache->batch;
+  a.heads = n_heads_idx;
+  a.q_idx = q_idx;
+  a.w = w;
+  a.q_pos = q_pos;
+  a.cache_seq = -1;
+  a.pool = pool;
+  a.pool_blocks = pool_blocks;
+  a.pool_bs = pool_block_size;
+  a.scores = scores;
+  a.stride = score_stride;  // row stride of scores in both modes
+  a.err = err_word;
+  return cuda_status(csa2::launch_index_score(a, reinterpret_cast<cudaStream_t>(stream)), "csa2_index_score launch");
+}
+
+size_t csa2_topk_workspace_size(int32_t batch, int64_t score_stride, int32_t k, int32_t out_pool_blocks) {
+  (void)k;
+  (void)out_pool_blocks;
+  if (batch <= 0 || score_stride <= 0) return 256;
+  return csa2::select_workspace_bytes(batch, score_stride);
+}
+
+csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio, const int64_t *q_pos,
+                      const int32_t *pool, int32_t pool_blocks, int32_t pool_block_size, int32_t k, int32_t *idx_out,
+                      int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count, void *ws, size_t ws_bytes,
+                      int32_t *err_word, csa2_stream_t stream) {
+  REQUIRE_PTR(scores);
+  REQUIRE_PTR(q_pos);
+  REQUIRE_PTR(idx_out);
+  REQUIRE(batch >= 1 && batch <= 65535, CSA2_ERR_SHAPE, "batch %d", batch);
+  REQUIRE(ratio == 1 || ratio == 2, CSA2_ERR_RANGE, "ratio %d", ratio);
+  REQUIRE(k >= 1 && k <= CSA2_MAX_TOPK, CSA2_ERR_RANGE, "k %d outside 1..2048", k);
+  REQUIRE(score_stride >= 1, CSA2_ERR_SHAPE, "score_stride %lld", static_cast<long long>(score_stride));
+  REQUIRE(pool_block_size >= 1 && pool_block_size <= 64, CSA2_ERR_SHAPE, "pool_block_size %d", pool_block_size);
+  if (pool) {
+    REQUIRE_PTR(pool);
+    REQUIRE(pool_blocks >= 1, CSA2_ERR_SHAPE, "pool_blocks %d", pool_blocks);
+    REQUIRE(pool_out == nullptr, CSA2_ERR_RANGE, "a pool can only be built in FULL mode");
+    REQUIRE(score_stride >= static_cast<int64_t>(pool_blocks) * pool_block_size, CSA2_ERR_SHAPE,
+            "score_stride too small for the pool");
+  }
+  if (pool_out) {
+    REQUIRE_PTR(pool_out);
+    REQUIRE_PTR(pool_count);
+    REQUIRE(out_pool_blocks >= 1 && out_pool_blocks <= 65536, CSA2_ERR_RANGE, "out_pool_blocks %d",
+            out_pool_blocks);
+  }
+  const size_t need = csa2_topk_workspace_size(batch, score_stride, k, out_pool_blocks);
+  REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "topk workspace %zu < %zu bytes", ws_bytes, need);
+  REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  csa2::SelArgs a{};
+  a.rows = batch;
+  a.scores = scores;
+  a.stride = score_stride;
+  a.ratio = ratio;
+  a.q_pos = q_pos;
+  a.pool = pool;
+  a.pool_blocks = pool_blocks;
+  a.bs = pool_block_size;
+  a.mode = pool ? csa2::kSelPool : csa2::kSelFull;
+  a.k = k;
+  a.out = idx_out;
+  a.out_stride = k;
+  a.count_out = nullptr;
+  a.err = err_word;
+  const int64_t slots = pool ? static_cast<int64_t>(pool_blocks) * pool_block_size : score_stride;
+  csa2_status st = cuda_status(csa2::launch_select(a, slots, ws, s), "csa2_topk launch");
+  if (st != CSA2_OK || !pool_out) return st;
+  csa2::SelArgs b = a;
+  b.mode = csa2::kSelBlockMax;
+  b.k = out_pool_blocks;
+  b.out = pool_out;
+  b.out_stride = out_pool_blocks;
+  b.count_out = pool_count;
+  return cuda_status(csa2::launch_select(b, (score_stride + pool_block_size - 1) / pool_block_size, ws, s),
+                     "csa2_topk pool launch");
+}
+
+size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k) {
+  if (batch <= 0 || n_heads <= 0 || k <= 0) return 256;
+  return csa2::attn_workspace_bytes(batch, n_heads, k);
+}
+
+csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t n_heads, const int64_t *q_pos,
+                                    const int32_t *idx, int32_t k, const float *sink, float sm_scale, float *out,
+                                    float *lse, void *ws, size_t ws_bytes, int32_t *err_word, csa2_stream_t stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(q_pos);
+  REQUIRE_PTR(idx);
+  REQUIRE_PTR(out);
+  REQUIRE_PTR(lse);
+  REQUIRE_OPT_PTR(sink);
+  REQUIRE(n_heads >= 16 && n_heads <= CSA2_MAX_HEADS && n_heads % 16 == 0, CSA2_ERR_SHAPE,
+          "n_heads %d must be a multiple of 16 in 16..128", n_heads);
+  REQUIRE(k >= 1 && k <= CSA2_MAX_TOPK, CSA2_ERR_RANGE, "k %d outside 1..2048", k);
+  REQUIRE(std::isfinite(sm_scale), CSA2_ERR_RANGE, "sm_scale is not finite");
+  const size_t need = csa2_attn_workspace_size(cache->batch, n_heads, k);
+  REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "attention workspace %zu < %zu bytes", ws_bytes,
+          need);
+  REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
+  csa2::AttnArgs a{};
+  a.rows = cache->batch;
+  a.heads = n_heads;
+  a.k = k;
+  a.q = q;
+  a.idx = idx;
+  a.q_pos = q_pos;
+  a.cache_seq = -1;
+  a.lat_codes = cache->lat_codes;
+  a.lat_scales = cache->lat_scales;
+  a.rope_codes = cache->rope_codes;
+  a.rope_scales = cache->rope_scales;
+  a.cap = cache->capacity;
+  a.ratio = cache->ratio;
+  a.n_tokens = cache->n_tokens;
+  a.ring_codes = cache->swa_codes;
+  a.ring_scales = cache->swa_scales;
+  a.ring_single = 0;
+  a.swa_dtype = cache->swa_dtype;
+  a.lin_codes = nullptr;
+  a.lin_scales = nullptr;
+  a.lin_base = nullptr;
+  a.sink = sink;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.lse = lse;
+  a.err = err_word;
+  return cuda_status(csa2::launch_attn(a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)),
+                     "csa2_sparse_attn_decode launch");
+}
+
+// -------------------------------------------------------------------- prefill
+namespace {
+struct PrefillLayout {
+  int qb;  // queries per block
+  size_t off_P, off_qpos, off_ring_c, off_ring_s, off_lin_c, off_lin_s, off_scores, off_sel, off_attn, total;
+};
+
+PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dtype) {
+  PrefillLayout L{};
+  const int cb = swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+  // bound the score block to ~256 MB
+  int qb = static_cast<int>((size_t(256) << 20) / (static_cast<size_t>(capacity) * 4));
+  if (qb < 1) qb = 1;
+  if (qb > Q) qb = Q;
+  if (qb > 4096) qb = 4096;
+  L.qb = qb;
+  size_t o = 0;
+  L.off_P = o;
+  o = align256(o + 16);
+  L.off_qpos = o;
+  o = align256(o + static_cast<size_t>(Q) * 8);
+  L.off_ring_c = o;
+  o = align256(o + static_cast<size_t>(csa2::kWin) * cb);
+  L.off_ring_s = o;
+  o = align256(o + static_cast<size_t>(csa2::kWin) * csa2::kSwaScaleStride);
+  L.off_lin_c = o;
+  o = align256(o + static_cast<size_t>(Q) * cb);
+  L.off_lin_s = o;
+  o = align256(o + static_cast<size_t>(Q) * csa2::kSwaScaleStride);
+  L.off_scores = o;
+  o = align256(o + static_cast<size_t>(qb) * capacity * 4);
+  L.off_sel = o;
+  o = align256(o + csa2::select_workspace_bytes(qb, capacity));
+  L.off_attn = o;
+  o = align256(o + csa2::attn_workspace_bytes(qb, n_heads, k));
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+size_t csa2_prefill_workspace_size(int32_t Q, int32_t capacity, int32_t n_heads_idx, int32_t n_heads, int32_t k) {
+  (void)n_heads_idx;
+  if (Q <= 0 || capacity <= 0 || n_heads <= 0 || k <= 0) return 256;
+  // the window layout is sized for bf16 (the larger format)
+  return prefill_layout(Q, capacity, n_heads, k, CSA2_SWA_BF16).total;
+}
+
+csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_compress_in *cmp, const float *rope_cs,
+                               int64_t rope_len, int32_t Q, const uint16_t *q_idx, const float *w,
+                               int32_t n_heads_idx, const uint16_t *q, int32_t n_heads, int32_t k, const float *sink,
+                               float sm_scale, int32_t *idx_out, float *out, float *lse, void *ws, size_t ws_bytes,
+                               int32_t *err_word, csa2_stream_t stream) {
+  csa2_status st = check_cache(cache);
+  if (st != CSA2_OK) return st;
+  REQUIRE(cache->ratio == 2, CSA2_ERR_UNSUPPORTED, "csa2_prefill_chunk needs a ratio-2 cache");
+  REQUIRE(seq >= 0 && seq < cache->batch, CSA2_ERR_RANGE, "seq %d outside the cache batch", seq);
+  REQUIRE(cmp != nullptr, CSA2_ERR_NULL, "cmp is NULL");
+  REQUIRE_PTR(cmp->ca);
+  REQUIRE_PTR(cmp->cb);
+  REQUIRE_PTR(cmp->za);
+  REQUIRE_PTR(cmp->zb);
+  REQUIRE_PTR(cmp->ba);
+  REQUIRE_PTR(cmp->bb);
+  REQUIRE_PTR(rope_cs);
+  REQUIRE(Q >= 1 && Q <= (1 << 20), CSA2_ERR_SHAPE, "Q %d outside 1..2^20", Q);
+  REQUIRE_PTR(q_idx);
+  REQUIRE_PTR(w);
+  REQUIRE_PTR(q);
+  REQUIRE_PTR(idx_out);
+  REQUIRE_PTR(out);
+  REQUIRE_PTR(lse);
+  REQUIRE_OPT_PTR(sink);
+  REQUIRE(n_heads_idx >= 1 && n_heads_idx <= CSA2_MAX_HEADS, CSA2_ERR_SHAPE, "n_heads_idx %d", n_heads_idx);
+  REQUIRE(n_heads >= 16 && n_heads <= CSA2_MAX_HEADS && n_heads % 16 == 0, CSA2_ERR_SHAPE, "n_heads %d", n_heads);
+  REQUIRE(k >= 1 && k <= CSA2_MAX_TOPK, CSA2_ERR_RANGE, "k %d", k);
+  const PrefillLayout L = prefill_layout(Q, cache->capacity, n_heads, k, cache->swa_dtype);
+  const size_t need = csa2_prefill_workspace_size(Q, cache->capacity, n_heads_idx, n_heads, k);
+  REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "prefill workspace %zu < %zu bytes", ws_bytes,
+          need);
+  REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *wb = static_cast<uint8_t *>(ws);
+  int64_t *P = reinterpret_cast<int64_t *>(wb + L.off_P);
+  int64_t *qpos = reinterpret_cast<int64_t *>(wb + L.off_qpos);
+  uint8_t *ring_c = wb + L.off_ring_c, *ring_s = wb + L.off_ring_s;
+  uint8_t *lin_c = wb + L.off_lin_c, *lin_s = wb + L.off_lin_s;
+  float *scores = reinterpret_cast<float *>(wb + L.off_scores);
+  const csa2_cache v = seq_view(*cache, seq);
+
+  csa2::k_prefill_snapshot<<<64, 256, 0, s>>>(v, Q, P, qpos, ring_c, ring_s);
+  cudaError_t e = csa2::launch_kv_append(v, nullptr, nullptr, CSA2_IN_F32, cmp, rope_cs, rope_len, Q, nullptr,
+                                         err_word, s);
+  if (e != cudaSuccess) return cuda_status(e, "prefill append");
+  csa2::k_prefill_window<<<(Q + 7) / 8, 256, 0, s>>>(cmp->ca, Q, P, rope_cs, rope_len, cache->swa_dtype, lin_c,
+                                                      cache->swa_dtype == CSA2_SWA_MXFP8 ? lin_s : nullptr);
+  for (int q0 = 0; q0 < Q; q0 += L.qb) {
+    const int nq = Q - q0 < L.qb ? Q - q0 : L.qb;
+    csa2::ScoreArgs sa{};
+    sa.idx_codes = v.idx_codes;
+    sa.idx_scales = v.idx_scales;
+    sa.cap = cache->capacity;
+    sa.ratio = 2;
+    sa.rows = nq;
+    sa.heads = n_heads_idx;
+    sa.q_idx = q_idx + static_cast<size_t>(q0) * n_heads_idx * csa2::kDi;
+    sa.w = w + static_cast<size_t>(q0) * n_heads_idx;
+    sa.q_pos = qpos + q0;
+    sa.cache_seq = 0;
+    sa.pool = nullptr;
+    sa.scores = scores;
+    sa.stride = cache->capacity;
+    sa.err = err_word;
+    e = csa2::launch_index_score(sa, s);
+    if (e != cudaSuccess) return cuda_status(e, "prefill score");
+    csa2::SelArgs se{};
+    se.rows = nq;
+    se.scores = scores;
+    se.stride = cache->capacity;
+    se.ratio = 2;
+    se.q_pos = qpos + q0;
+    se.pool = nullptr;
+    se.bs = 8;
+    se.mode = csa2::kSelFull;
+    se.k = k;
+    se.out = idx_out + static_cast<size_t>(q0) * k;
+    se.out_stride = k;
+    se.count_out = nullptr;
+    se.err = err_word;
+    e = csa2::launch_select(se, cache->capacity, wb + L.off_sel, s);
+    if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    csa2::AttnArgs aa{};
+    aa.rows = nq;
+    aa.heads = n_heads;
+    aa.k = k;
+    aa.q = q + static_cast<size_t>(q0) * n_heads * csa2::kDqk;
+    aa.idx = idx_out + static_cast<size_t>(q0) * k;
+    aa.q_pos = qpos + q0;
+    aa.cache_seq = 0;
+    aa.lat_codes = v.lat_codes;
+    aa.lat_scales = v.lat_scales;
+    aa.rope_codes = v.rope_codes;
+    aa.rope_scales = v.rope_scales;
+    aa.cap = cache->capacity;
+    aa.ratio = 2;
+    aa.n_tokens = v.n_tokens;
+    aa.ring_codes = ring_c;
+    aa.ring_scales = cache->swa_dtype == CSA2_SWA_MXFP8 ? ring_s : nullptr;
+    aa.ring_single = 1;
+    aa.swa_dtype = cache->swa_dtype;
+    aa.lin_codes = lin_c;
+    aa.lin_scales = cache->swa_dtype == CSA2_SWA_MXFP8 ? lin_s : nullptr;
+    aa.lin_base = P;
+    aa.sink = sink;
+    aa.sm_scale = sm_scale;
+    aa.out = out + static_cast<size_t>(q0) * n_heads * csa2::kLat;
+    aa.lse = lse + static_cast<size_t>(q0) * n_heads;
+    aa.err = err_word;
+    e = csa2::launch_attn(aa, wb + L.off_attn, L.total - L.off_attn, s);
+    if (e != cudaSuccess) return cuda_status(e, "prefill attention");
+  }
+  return cuda_status(cudaGetLastError(), "csa2_prefill_chunk");
+}
+
+}  // extern "C"

@@ -1,0 +1,260 @@
+/*
+ * csa2.h -- C ABI of libcsa2, the CSA2 long-context attention step
+ * (FP4 global KV cache, lightning indexer, top-k, sparse absorbed-query
+ * attention with a sliding window) on one GB300 (sm_103a).
+ *
+ * Source pages cited below:
+ *   [P1] "DeepSeek V4.1 Flash 아키텍처 분석" (plaidlabs.ai blog)
+ *   [P2] "DeepSeek Multi-Head Latent Attention(MLA) 해부" (huny.dev blog)
+ *   [P3] "DeepSeek V4.1 Flash 해부, KV 캐시는 줄고 사후학습 레시피는 그대로" (traillabs.ai)
+ *   [P4] "매개변수는 커졌는데 메모리는 4분의 1, DeepSeek V4.1 Flash의 KV 캐시 다이어트" (ithotfix.com)
+ *   [P5] "DeepSeek-V4: Towards Highly Efficient Million-Token Context Intelligence" (issue #58 translation)
+ *
+ * Conventions (all calls):
+ *   - The caller owns every buffer.  Device pointers are CUDA device memory of
+ *     the current device; host pointers are marked (host).  The library never
+ *     allocates on these calls; scratch comes from a caller workspace whose
+ *     size the matching *_workspace_size() returns.
+ *   - Every device pointer must be 16-byte aligned (CSA2_ERR_ALIGN otherwise).
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL = the
+ *     legacy default stream).  They validate their arguments on the host first
+ *     and return a status; they never abort and never throw.
+ *   - Errors that only the device can see (an append beyond the capacity, an
+ *     index outside the cache, a NaN score) set bits of the caller's int32
+ *     *err_word (device memory, may be NULL to ignore) with atomicOr; the
+ *     affected outputs are then unspecified.  Clear it before the calls and
+ *     read it after synchronising.
+ *   - csa2_last_error_detail() returns a thread-local text for the last
+ *     non-OK status of this thread.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *csa2_stream_t;
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_NULL = 1,        /* a required pointer is NULL                       */
+  CSA2_ERR_SHAPE = 2,       /* a size is outside its documented range           */
+  CSA2_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned          */
+  CSA2_ERR_RANGE = 4,       /* an enum / k / ratio argument is out of range      */
+  CSA2_ERR_UNSUPPORTED = 5, /* valid but not implemented (e.g. ratio-1 prefill) */
+  CSA2_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed      */
+  CSA2_ERR_WORKSPACE = 7    /* the workspace is NULL or smaller than required   */
+} csa2_status;
+
+/* bits of the device error word */
+#define CSA2_DEVERR_CAPACITY 1u /* append past the cache capacity (nothing written) */
+#define CSA2_DEVERR_INDEX 2u    /* an index / pool id outside the visible cache (skipped) */
+#define CSA2_DEVERR_NAN 4u      /* a NaN index score (it ranks lowest)                */
+#define CSA2_DEVERR_ROPE 8u     /* a position outside the RoPE table (nothing written) */
+
+/* sliding-window storage */
+#define CSA2_SWA_BF16 0  /* 576 bf16 values, 1,152 B per token                         */
+#define CSA2_SWA_MXFP8 1 /* 576 E4M3 codes + 18 E8M0 scales (one per 32), 594 B/token */
+
+/* input element types for csa2_kv_append */
+#define CSA2_IN_F32 0
+#define CSA2_IN_BF16 1
+
+/* Fixed dimensions of the path (see the citations on csa2_cache). */
+#define CSA2_D_LATENT 512 /* latent dims of a main-KV entry ([P1] "890 bytes/token")       */
+#define CSA2_D_ROPE 64    /* decoupled RoPE dims ([P2] §3; [P5] §2.3.3 "last 64 dims")     */
+#define CSA2_D_QK 576     /* score dims of an absorbed query: latent + RoPE ([P2] §4)      */
+#define CSA2_D_INDEX 128  /* indexer head dim c_I ([P5] §4.2.1)                            */
+#define CSA2_D_CMP 704    /* one compression row: 576 main dims then 128 indexer dims      */
+#define CSA2_WINDOW 128   /* sliding window n_win ([P5] §4.2.1)                            */
+#define CSA2_MAX_TOPK 2048
+#define CSA2_MAX_HEADS 128
+
+/*
+ * One global-KV cache (the output of one Full layer; Reindex and Reuse layers
+ * read it).  Every plane is [batch][capacity][bytes], sequence-major, so one
+ * sequence's entries are contiguous.  Per entry ([P1] "890 bytes/token";
+ * [P4] "890이 맞아떨어지는 계산"):
+ *   lat_codes   256 B  E2M1 codes of the 512 latent dims, byte j = code(2j) | code(2j+1) << 4
+ *   lat_scales   32 B  one E4M3 scale per 16 dims                 -> 288 B main entry
+ *   rope_codes   32 B  E2M1 codes of the 64 rotated RoPE dims (sidecar of the MLA split, [P2] §3)
+ *   rope_scales   4 B  one E4M3 scale per 16                       -> 36 B sidecar
+ *   idx_codes    64 B  E2M1 codes of the 128-dim indexer key
+ *   idx_scales    4 B  one E8M0 scale per 32 (MXFP4)               -> 68 B indexer entry
+ * swa_codes / swa_scales: the sliding-window ring, [batch][128][576] codes
+ *   (E4M3 bytes, or bf16 when swa_dtype == CSA2_SWA_BF16) and [batch][128][32]
+ *   scale bytes (18 used, MXFP8 only); token t lives in slot t % 128 ([P5]
+ *   §3.5.1: the window is a fixed-size per-sequence state).
+ * cmp_buf: ratio 2 only, float [batch][4][4][704]: the last tokens' compression
+ *   rows (C^a, C^b, Z^a, Z^b) at slot t % 4, carried between appends ([P5] §3.5.1
+ *   "Compression Buffer").
+ * n_tokens: int64 [batch] tokens appended so far (device; csa2_kv_append and
+ *   csa2_prefill_chunk advance it).  A ratio-r cache holds floor(n_tokens/r) entries.
+ * ratio: 1 (one token per entry, decoder) or 2 (two tokens per entry, encoder;
+ *   [P1] "Global KV는 네 곳에서 만든다", [P4] 178 B per token).
+ */
+typedef struct csa2_cache {
+  int32_t batch;
+  int32_t capacity; /* entries per sequence */
+  int32_t ratio;
+  int32_t swa_dtype;
+  uint8_t *lat_codes, *lat_scales;
+  uint8_t *rope_codes, *rope_scales;
+  uint8_t *idx_codes, *idx_scales;
+  uint8_t *swa_codes, *swa_scales;
+  float *cmp_buf;
+  int64_t *n_tokens;
+} csa2_cache;
+
+/* Ratio-2 compression inputs ([P5] §2.3.1 "압축된 Key-Value Entry"): per token
+ * rows of C^a, C^b, Z^a, Z^b ([batch][n_new][704], device fp32) and the
+ * positional biases B^a, B^b ([2][704], device fp32). */
+typedef struct csa2_compress_in {
+  const float *ca, *cb, *za, *zb;
+  const float *ba, *bb;
+} csa2_compress_in;
+
+/* Bytes each plane of a cache needs (host helper; no device work). */
+size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane /* 0..9 as listed */,
+                              int32_t swa_dtype);
+
+/*
+ * csa2_rope_table (host): cos/sin table for the 64 RoPE dims, rope_cs[pos][i][2]
+ * = (cos, sin)(pos * theta^(-2i/64)) for i < 32, evaluated in double and rounded
+ * to fp32, positions 0..n_pos-1 ([P5] §2.3.3 "Partial Rotary Positional
+ * Embedding"; pairs (2i, 2i+1) interleaved).  out_host holds n_pos*64 floats.
+ */
+csa2_status csa2_rope_table(double theta, int64_t n_pos, float *out_host);
+
+/*
+ * csa2_kv_append: quantise n_new new tokens of every sequence into the cache,
+ * at positions n_tokens[b] .. n_tokens[b]+n_new-1, then advance n_tokens.
+ *   ratio 1: kv [batch][n_new][576] (512 latent, 64 RoPE dims not yet rotated),
+ *            idx_key [batch][n_new][128], element type in_dtype; cmp = NULL.
+ *            Entry t = token t: RoPE at position t, then quantise ([P4]
+ *            "890이 맞아떨어지는 계산": quantisation after RoPE).
+ *   ratio 2: cmp != NULL, kv = idx_key = NULL.  Entry i is emitted when tokens
+ *            2i, 2i+1 are present: per channel a softmax over the 4 rows
+ *            [Z^a_2i + B^a_0, Z^a_2i+1 + B^a_1, Z^b_2i-2 + B^b_0, Z^b_2i-1 + B^b_1]
+ *            and the gated sum of the matching C rows ([P5] §2.3.1), computed in
+ *            fp64 and rounded to fp32, then RoPE at position 2i, then quantised.
+ *            Rows of earlier appends come from cmp_buf.
+ *   Window: each of the last min(n_new, 128) tokens fills slot t % 128 with its
+ *            own vector (ratio 1: kv; ratio 2: C^a[0:576]) rotated at t, in 8 bits
+ *            or bf16 ([P1] "890 bytes/token": the window KV stays in FP8).
+ * rope_cs: device table from csa2_rope_table with rope_len positions.
+ * cmp_dbg: NULL, or device fp32 [batch][n_new/2+1][704] receiving each emitted
+ *   ratio-2 entry before RoPE (row e = the e-th entry emitted by this call).
+ * Device errors: CAPACITY (a sequence would exceed capacity; nothing written
+ *   for it), ROPE (a position >= rope_len).
+ */
+csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *idx_key,
+                           int32_t in_dtype, const csa2_compress_in *cmp, const float *rope_cs,
+                           int64_t rope_len, int32_t n_new, float *cmp_dbg, int32_t *err_word,
+                           csa2_stream_t stream);
+
+/*
+ * csa2_index_score: lightning-indexer scores ([P5] §2.3.1, "I_{t,s} = sum_h
+ * w_{t,h} ReLU(q_{t,h} . K_s)"), with the query quantised to MXFP4 like the
+ * keys (the indexer QK product runs in FP4, [P5] §2.3.4).
+ *   q_idx: bf16 [batch][n_heads_idx][128]; w: fp32 [batch][n_heads_idx];
+ *   q_pos: int64 [batch] query positions; entry s is visible iff
+ *          s < floor(q_pos / ratio) ([P5] §2.3.1).
+ *   d_h is the dot of the dequantised vectors (exact when the block exponents of
+ *   a (query, key) pair span at most 9 binades, as for N(0,1) data);
+ *   score = fma chain over heads in order: acc = fma(w_h, max(d_h, +0), acc).
+ * FULL (pool == NULL): scores[b][s] for every visible s (others untouched).
+ * POOL (Reindex, [P1] "512개를 고르기 위해 ..."): pool [batch][pool_blocks] int32
+ *   ascending block ids (-1 = empty); scores[b][j*pool_block_size + i] is the
+ *   score of position pool[b][j]*pool_block_size + i when it is visible.
+ * score_stride: floats per sequence in scores (>= capacity for FULL,
+ *   >= pool_blocks*pool_block_size for POOL).  n_heads_idx in 1..128.
+ */
+csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
+                             int32_t n_heads_idx, const int64_t *q_pos, const int32_t *pool,
+                             int32_t pool_blocks, int32_t pool_block_size, float *scores,
+                             int64_t score_stride, int32_t *err_word, csa2_stream_t stream);
+
+/*
+ * csa2_topk: top-k selector ([P5] §2.3.1 "Top-k(I_{t,:})") over the candidates
+ * csa2_index_score scored (same ratio / q_pos / pool arguments), ordered by
+ * score descending then position ascending (ties go to the lower position;
+ * -0 == +0).  idx_out [batch][k] receives the chosen positions in ascending
+ * order, padded with -1.  k in 1..2048.
+ * FULL mode only: when pool_out != NULL also builds the candidate pool of the
+ * Hierarchical Sparse Indexer ([P1], [P4]): positions are grouped in
+ * pool_block_size-aligned blocks, a block's score is the max over its visible
+ * positions, and the top out_pool_blocks blocks by (max desc, block asc) are
+ * written ascending to pool_out [batch][out_pool_blocks] (padded with -1),
+ * with their number in pool_count [batch].
+ * ws: device workspace of csa2_topk_workspace_size() bytes.
+ */
+size_t csa2_topk_workspace_size(int32_t batch, int64_t score_stride, int32_t k,
+                                int32_t out_pool_blocks);
+csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
+                      const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
+                      int32_t pool_block_size, int32_t k, int32_t *idx_out,
+                      int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count, void *ws,
+                      size_t ws_bytes, int32_t *err_word, csa2_stream_t stream);
+
+/*
+ * csa2_sparse_attn_decode: core attention of one decode step over the k
+ * selected entries and the window ([P5] §2.3.1 "Shared Key-Value MQA": each
+ * entry is key and value; [P2] §4 absorbed query: logits over 576 dims, values
+ * the 512 latent dims; [P5] §2.3.3 window branch and attention sink).
+ *   q: bf16 [batch][n_heads][576] (latent 512 then rotated RoPE 64);
+ *   idx: int32 [batch][k] positions (-1 = empty) -- a Reuse layer passes its
+ *        leader's list and cache ([P3] "CSA2의 세 가지 모드");
+ *   window: tokens max(0, q_pos-127) .. q_pos that are < n_tokens[b];
+ *   sink: fp32 [n_heads] or NULL; sm_scale: logit scale.
+ *   z_j = sm_scale * q . e_j; p_j = exp(z_j - M) / (sum_j exp(z_j - M) + exp(sink_h - M));
+ *   out: fp32 [batch][n_heads][512] = sum_j p_j c_j; lse: fp32 [batch][n_heads]
+ *   = M + log(denominator) (-inf when there is nothing to attend to).
+ * n_heads: a multiple of 16, 16..128.  k: 1..2048.
+ * ws: device workspace of csa2_attn_workspace_size() bytes (split partials).
+ * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
+ */
+size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k);
+csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t n_heads,
+                                    const int64_t *q_pos, const int32_t *idx, int32_t k,
+                                    const float *sink, float sm_scale, float *out, float *lse,
+                                    void *ws, size_t ws_bytes, int32_t *err_word,
+                                    csa2_stream_t stream);
+
+/*
+ * csa2_prefill_chunk: encoder-style chunked prefill of sequence `seq` of a
+ * ratio-2 cache.  Appends the Q tokens (as csa2_kv_append, ratio 2), then for
+ * every query i (position P+i, P = n_tokens[seq] before the call): scores all
+ * visible entries s < floor((P+i)/2) with its own indexer query (a dense FP4
+ * contraction), keeps its top k, and attends over them plus its window tokens
+ * max(0, P+i-127) .. P+i ([P5] §2.3.1, §2.3.3).
+ *   cmp: rows [Q][704] for this sequence; q_idx bf16 [Q][n_heads_idx][128];
+ *   w fp32 [Q][n_heads_idx]; q bf16 [Q][n_heads][576];
+ *   idx_out int32 [Q][k]; out fp32 [Q][n_heads][512]; lse fp32 [Q][n_heads].
+ * ws: device workspace of csa2_prefill_workspace_size() bytes.
+ * Ratio-1 caches return CSA2_ERR_UNSUPPORTED.
+ */
+size_t csa2_prefill_workspace_size(int32_t Q, int32_t capacity, int32_t n_heads_idx,
+                                   int32_t n_heads, int32_t k);
+csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_compress_in *cmp,
+                               const float *rope_cs, int64_t rope_len, int32_t Q,
+                               const uint16_t *q_idx, const float *w, int32_t n_heads_idx,
+                               const uint16_t *q, int32_t n_heads, int32_t k, const float *sink,
+                               float sm_scale, int32_t *idx_out, float *out, float *lse, void *ws,
+                               size_t ws_bytes, int32_t *err_word, csa2_stream_t stream);
+
+/* Status text, and the thread-local detail of this thread's last failure. */
+const char *csa2_status_string(csa2_status status);
+const char *csa2_last_error_detail(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

@@ -1,0 +1,92 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads and exports
+every function include/csa2.h declares; host validation returns the documented
+status codes before any device work; the host RoPE table matches the oracle's."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp4_compressed_sparse_gb300 import build_lib, csa2
+    build_lib.build()
+    return csa2.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from fp4_compressed_sparse_gb300 import csa2
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(csa2.EXPORTS) == names
+
+
+def test_status_strings_and_version(lib):
+    assert lib.csa2_version() >= 100
+    for s in range(8):
+        assert lib.csa2_status_string(s)
+    assert lib.csa2_status_string(99) == b"unknown status"
+
+
+def test_host_validation_codes(lib):
+    from fp4_compressed_sparse_gb300 import csa2
+    # NULL cache
+    assert lib.csa2_kv_append(None, None, None, 0, None, None, 1, 1, None, None, None) == 1
+    assert b"cache" in lib.csa2_last_error_detail()
+    # bad shapes / ranges before any device work (pointers are 16-aligned fakes, never touched)
+    fake = 1 << 20
+    st = csa2.CacheStruct(1, 16, 3, 1, *([fake] * 10))
+    assert lib.csa2_kv_append(ctypes.byref(st), None, None, 0, None, None, 1, 1, None, None, None) == 4
+    st = csa2.CacheStruct(0, 16, 1, 1, *([fake] * 10))
+    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None,
+                                None) == 2
+    st = csa2.CacheStruct(1, 16, 1, 1, *([fake] * 10))
+    st.lat_codes = fake + 8  # misaligned
+    assert lib.csa2_sparse_attn_decode(ctypes.byref(st), None, 64, None, None, 512, None, 0.1, None,
+                                       None, None, 0, None, None) == 3
+    st.lat_codes = fake
+    p = ctypes.c_void_p(fake)
+    # heads not a multiple of 16
+    assert lib.csa2_sparse_attn_decode(ctypes.byref(st), p, 24, p, p, 512, None, 0.1, p, p, p, 1 << 20,
+                                       None, None) == 2
+    # k out of range
+    assert lib.csa2_topk(p, 100, 1, 1, p, None, 0, 8, 0, p, 0, None, None, p, 1 << 20, None, None) == 4
+    # workspace too small
+    assert lib.csa2_topk(p, 100, 1, 1, p, None, 0, 8, 8, p, 0, None, None, p, 16, None, None) == 7
+    # prefill needs a ratio-2 cache
+    assert lib.csa2_prefill_chunk(ctypes.byref(st), 0, None, p, 10, 4, p, p, 4, p, 16, 8, None, 0.1,
+                                  p, p, p, p, 1 << 30, None, None) == 5
+
+
+def test_rope_table_matches_oracle(lib, orc):
+    n = 300
+    host = np.zeros((n, 64), np.float32)
+    assert lib.csa2_rope_table(10000.0, n, host.ctypes.data_as(ctypes.c_void_p)) == 0
+    for pos in (0, 1, 17, 255, 299):
+        assert np.array_equal(host[pos], orc.rope_cs(10000.0, pos))
+    big = np.zeros((1, 64), np.float32)
+    # a far position through the table formula (pos * theta^(-2i/64) in double)
+    far = np.zeros((1048577, 64), np.float32)
+    assert lib.csa2_rope_table(10000.0, far.shape[0], far.ctypes.data_as(ctypes.c_void_p)) == 0
+    assert np.array_equal(far[1048576], orc.rope_cs(10000.0, 1048576))
+    del big
+
+
+def test_cache_plane_bytes_match_record(lib):
+    # 288 B main + 36 B sidecar + 68 B indexer per entry; MXFP8 window 576 + scales
+    per = [lib.csa2_cache_plane_bytes(1, 1, p, 1) for p in range(6)]
+    assert per[0] + per[1] == 288 and per[2] + per[3] == 36 and per[4] + per[5] == 68
+    assert lib.csa2_cache_plane_bytes(1, 1, 6, 1) == 128 * 576
+    assert lib.csa2_cache_plane_bytes(1, 1, 6, 0) == 128 * 1152
