@@ -23,7 +23,7 @@ D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128
 
 EXPORTS = [
     "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score",
-    "csa2_topk_workspace_size", "csa2_topk", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
+    "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_status_string",
     "csa2_last_error_detail", "csa2_version",
 ]
@@ -77,6 +77,7 @@ def load() -> ctypes.CDLL:
         "csa2_index_score": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_topk": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, sz, vp, vp]),
+        "csa2_topk_noalloc": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
         "csa2_attn_workspace_size": (sz, [i32, i32, i32]),
         "csa2_sparse_attn_decode": (i32, [vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, sz, vp, vp]),
         "csa2_prefill_workspace_size": (sz, [i32, i32, i32, i32, i32]),
@@ -197,6 +198,18 @@ def topk(scores, ratio, q_pos, k, idx_out, ws, pool=None, pool_block_size=8, poo
                      pool_out.shape[1] if pool_out is not None else 0, _ptr(pool_out), _ptr(pool_count),
                      _ptr(ws), ws.numel(), _ptr(err), _stream(stream))
     _check("csa2_topk", st)
+
+
+def topk_noalloc(scores, ratio, q_pos, k, idx_out, pool=None, pool_block_size=8, pool_out=None,
+                 pool_count=None, err=None, stream=None):
+    """csa2_topk_noalloc: csa2_topk with the library's built-in 4 MiB scratch instead of a
+    caller workspace (for callers that cannot allocate device memory while running)."""
+    L = load()
+    st = L.csa2_topk_noalloc(_ptr(scores), scores.shape[1], scores.shape[0], ratio, _ptr(q_pos),
+                             _ptr(pool), pool.shape[1] if pool is not None else 0, pool_block_size, k,
+                             _ptr(idx_out), pool_out.shape[1] if pool_out is not None else 0,
+                             _ptr(pool_out), _ptr(pool_count), _ptr(err), _stream(stream))
+    _check("csa2_topk_noalloc", st)
 
 
 def attn_workspace(batch, heads, k, device="cuda"):

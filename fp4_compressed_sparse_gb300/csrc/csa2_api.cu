@@ -90,6 +90,10 @@ size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
 
+namespace csa2 {
+void set_error_detail(const char *msg) { g_detail = msg ? msg : ""; }
+}  // namespace csa2
+
 // ===================================================================== prefill kernels
 namespace csa2 {
 namespace {

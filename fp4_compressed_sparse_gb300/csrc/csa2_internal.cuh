@@ -5,6 +5,9 @@
 
 namespace csa2 {
 
+// thread-local text returned by csa2_last_error_detail()
+void set_error_detail(const char *msg);
+
 cudaError_t launch_kv_append(const csa2_cache &c, const void *kv, const void *ik, int in_dtype,
                              const csa2_compress_in *cmp, const float *rope_cs, int64_t rope_len, int n_new,
                              float *cmp_dbg, int32_t *err, cudaStream_t s);

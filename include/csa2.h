@@ -219,6 +219,28 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, 
  * ws: device workspace of csa2_attn_workspace_size() bytes (split partials).
  * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
  */
+/*
+ * csa2_topk_noalloc: csa2_topk without a caller workspace, for callers that
+ * may not allocate device memory while they run (a host framework that owns all
+ * device allocations, a service whose memory budget is fixed at start-up, code
+ * that must not hit the allocator's implicit synchronisation).  The source pages
+ * have no counterpart: this is a library convenience, not a step of the method.
+ * Same arguments and results as csa2_topk minus ws / ws_bytes.  Its scratch is
+ * a 4 MiB array compiled into the library, resident on every GPU that loads it
+ * until the process exits; calls needing more (csa2_topk_workspace_size() >
+ * 4 MiB, i.e. large batch x score_stride) return CSA2_ERR_WORKSPACE with the
+ * sizes in csa2_last_error_detail().  The first call on each device looks up the
+ * array's device address (a runtime query), so make that first call before any
+ * stream capture.  Every call shares the array and leaves its contents behind
+ * (the histograms are cleared at the start of each call): calls whose kernels
+ * may overlap on the GPU -- different streams without ordering -- race.
+ */
+csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
+                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
+                              int32_t pool_block_size, int32_t k, int32_t *idx_out,
+                              int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count,
+                              int32_t *err_word, csa2_stream_t stream);
+
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k);
 csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t n_heads,
                                     const int64_t *q_pos, const int32_t *idx, int32_t k,
