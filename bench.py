@@ -160,32 +160,38 @@ class FullDecode:
         self.lse = torch.empty((B, W.heads), device=device)
         self.ws_topk = csa2.topk_workspace(B, self.cap, W.topk, W.pool_blocks)
         self.ws_attn = csa2.attn_workspace(B, W.heads, W.topk)
+        self.ws_score = csa2.index_score_workspace(B, W.index_heads)
         self.launches_per_step = None
 
-    def step(self, s, ev=None):
+    PARTS = ("append", "score", "topk_pool", "attention")
+
+    def part(self, s, name):
         c, W = self.csa2, self.W
+        if name == "append":
+            c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+        elif name == "score":
+            c.index_score(self.cache, self.q_idx[s], self.w[s], self.q_pos[s], self.scores, err=self.err,
+                          ws=self.ws_score)
+        elif name == "topk_pool":
+            c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
+                   pool_count=self.pool_cnt, err=self.err)
+        else:
+            c.sparse_attn_decode(self.cache, self.q[s], self.q_pos[s], self.idx, self.out, self.lse,
+                                 self.ws_attn, W.sm_scale, err=self.err)
+
+    def step(self, s, ev=None):
+        for k, name in enumerate(self.PARTS):
+            if ev is not None:
+                ev[k].record()
+            self.part(s, name)
         if ev is not None:
-            ev[0].record()
-        c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
-        if ev is not None:
-            ev[1].record()
-        c.index_score(self.cache, self.q_idx[s], self.w[s], self.q_pos[s], self.scores, err=self.err)
-        if ev is not None:
-            ev[2].record()
-        c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
-               pool_count=self.pool_cnt, err=self.err)
-        if ev is not None:
-            ev[3].record()
-        c.sparse_attn_decode(self.cache, self.q[s], self.q_pos[s], self.idx, self.out, self.lse,
-                             self.ws_attn, W.sm_scale, err=self.err)
-        if ev is not None:
-            ev[4].record()
+            ev[len(self.PARTS)].record()
 
     @staticmethod
     def kernel_launches(n_splits_gt1=False):
-        # kv_append ratio 1: append + advance; index_score: 1; topk: 3 x (hist, resolve) + count
+        # kv_append ratio 1: append + advance; index_score: q prep + score; topk: 3 x (hist, resolve) + count
         # + write, twice (top-k, then the pool); attention: 1 (+ combine when split)
-        return 2 + 1 + 16 + 1 + (1 if n_splits_gt1 else 0)
+        return 2 + 2 + 16 + 1 + (1 if n_splits_gt1 else 0)
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -208,14 +214,28 @@ def run_ours(args):
     bench = FullDecode(W, n_steps, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
 
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    # warm-up steps run eagerly (first calls set kernel attributes); every timed
+    # step is one CUDA graph (its launches and the event records between them)
     for s in range(args.warmup):
         flush.zero_()
         bench.step(s)
     torch.cuda.synchronize()
     if bench.err.item() != 0:
         raise RuntimeError(f"device error word {bench.err.item()} during warm-up")
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    graphs = None
+    if not args.no_graph:
+        # one graph per part of every timed step; the events sit between replays
+        graphs = []
+        for i in range(args.steps):
+            row = []
+            for name in FullDecode.PARTS:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    bench.part(args.warmup + i, name)
+                row.append(g)
+            graphs.append(row)
+        torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -223,7 +243,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()  # L2 flushed between timed steps (outside the events)
-        bench.step(args.warmup + i, evs[i])
+        if graphs is not None:
+            for k, g in enumerate(graphs[i]):
+                evs[i][k].record()
+                g.replay()
+            evs[i][len(graphs[i])].record()
+        else:
+            bench.step(args.warmup + i, evs[i])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -264,6 +290,7 @@ def run_ours(args):
                    "index_heads": W.index_heads, "topk": W.topk, "window": 128,
                    "window_dtype": "mxfp8" if W.swa_dtype == 1 else "bf16",
                    "pool_blocks": W.pool_blocks, "l2": "flushed between timed steps (256 MB write)",
+                   "launch": "eager" if args.no_graph else "one CUDA graph per part of each step",
                    "parallelism": f"replicas x{world} (sequences sharded, no collective)"},
         "kv_hbm": {"algorithmic_bytes_per_step": nbytes["total"], "gbs": round(kv_gbs, 1),
                    "frac": round(kv_gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind},
@@ -384,6 +411,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch every kernel eagerly instead of one "
+                    "CUDA graph per step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

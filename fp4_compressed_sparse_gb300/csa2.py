@@ -16,13 +16,14 @@ from . import build_lib
 OK = 0
 ERR_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RANGE",
              5: "ERR_UNSUPPORTED", 6: "ERR_CUDA", 7: "ERR_WORKSPACE"}
-DEVERR_CAPACITY, DEVERR_INDEX, DEVERR_NAN, DEVERR_ROPE = 1, 2, 4, 8
+DEVERR_CAPACITY, DEVERR_INDEX, DEVERR_NAN, DEVERR_ROPE, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 SWA_BF16, SWA_MXFP8 = 0, 1
 IN_F32, IN_BF16 = 0, 1
 D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128
 
 EXPORTS = [
-    "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score",
+    "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
+    "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_status_string",
     "csa2_last_error_detail", "csa2_version",
@@ -74,7 +75,8 @@ def load() -> ctypes.CDLL:
         "csa2_cache_plane_bytes": (sz, [i32, i32, i32, i32]),
         "csa2_rope_table": (i32, [f64, i64, vp]),
         "csa2_kv_append": (i32, [vp, vp, vp, i32, vp, vp, i64, i32, vp, vp, vp]),
-        "csa2_index_score": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, vp]),
+        "csa2_index_score_workspace_size": (sz, [i32, i32]),
+        "csa2_index_score": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, sz, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_topk": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, sz, vp, vp]),
         "csa2_topk_noalloc": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
@@ -123,8 +125,10 @@ class Cache:
         self.lat_scales = u8(nb[1]).view(batch, capacity, 32)
         self.rope_codes = u8(nb[2]).view(batch, capacity, 32)
         self.rope_scales = u8(nb[3]).view(batch, capacity, 4)
-        self.idx_codes = u8(nb[4]).view(batch, capacity, 64)
-        self.idx_scales = u8(nb[5]).view(batch, capacity, 4)
+        # tile-major indexer planes (see csa2_cache in csa2.h)
+        self.idx_tiles = (capacity + 127) // 128
+        self.idx_codes = u8(nb[4]).view(batch, self.idx_tiles, 8192)
+        self.idx_scales = u8(nb[5]).view(batch, self.idx_tiles, 512)
         sw = 576 if swa_dtype == SWA_MXFP8 else 1152
         self.swa_codes = u8(nb[6]).view(batch, WINDOW, sw)
         self.swa_scales = u8(nb[7]).view(batch, WINDOW, 32)
@@ -140,6 +144,13 @@ class Cache:
 
     def ref(self):
         return ctypes.byref(self.struct)
+
+    def idx_entries(self):
+        """The indexer planes re-read per entry: (codes [B,cap,64], scales [B,cap,4])."""
+        B, nt = self.batch, self.idx_tiles
+        codes = self.idx_codes.view(B, nt, 4, 128, 16).permute(0, 1, 3, 2, 4).reshape(B, nt * 128, 64)
+        scales = self.idx_scales.view(B, nt, 32, 4, 4).permute(0, 1, 3, 2, 4).reshape(B, nt * 128, 4)
+        return codes[:, :self.capacity], scales[:, :self.capacity]
 
     def entry_bytes(self):
         """Bytes of one stored entry (main 288 + sidecar 36 + indexer 68)."""
@@ -173,14 +184,28 @@ def kv_append(cache: Cache, kv=None, idx_key=None, rope_cs=None, cmp=None, cmp_d
     _check("csa2_kv_append", st)
 
 
+def index_score_workspace(batch, heads_idx, device="cuda"):
+    n = load().csa2_index_score_workspace_size(batch, heads_idx)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+_ws_cache = {}
+
+
 def index_score(cache: Cache, q_idx, w, q_pos, scores, pool=None, pool_block_size=8, err=None,
-                stream=None):
+                stream=None, ws=None):
     """csa2_index_score: q_idx bf16 [B,H_I,128], w fp32 [B,H_I], q_pos int64 [B],
     scores fp32 [B, stride]; pool int32 [B, pool_blocks] for a Reindex layer."""
     L = load()
+    if ws is None:
+        key = (q_idx.shape[0], q_idx.shape[1], q_idx.device)
+        ws = _ws_cache.get(key)
+        if ws is None:
+            ws = _ws_cache[key] = index_score_workspace(q_idx.shape[0], q_idx.shape[1], q_idx.device)
     st = L.csa2_index_score(cache.ref(), _ptr(q_idx), _ptr(w), q_idx.shape[1], _ptr(q_pos),
                             _ptr(pool), pool.shape[1] if pool is not None else 0, pool_block_size,
-                            _ptr(scores), scores.shape[1], _ptr(err), _stream(stream))
+                            _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(), _ptr(err),
+                            _stream(stream))
     _check("csa2_index_score", st)
 
 

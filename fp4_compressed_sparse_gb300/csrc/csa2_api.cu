@@ -77,8 +77,8 @@ csa2_cache seq_view(const csa2_cache &c, int seq) {
   v.lat_scales += e * 32;
   v.rope_codes += e * 32;
   v.rope_scales += e * 4;
-  v.idx_codes += e * 64;
-  v.idx_scales += e * 4;
+  v.idx_codes += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileCodeBytes;
+  v.idx_scales += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileScaleBytes;
   v.swa_codes += static_cast<size_t>(seq) * csa2::kWin * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
   if (v.swa_scales) v.swa_scales += static_cast<size_t>(seq) * csa2::kWin * csa2::kSwaScaleStride;
   if (v.cmp_buf) v.cmp_buf += static_cast<size_t>(seq) * 4 * 4 * csa2::kDcmp;
@@ -163,8 +163,8 @@ size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane, in
     case 1: return e * 32;
     case 2: return e * 32;
     case 3: return e * 4;
-    case 4: return e * 64;
-    case 5: return e * 4;
+    case 4: return static_cast<size_t>(batch) * csa2::idx_tiles(capacity) * csa2::kIdxTileCodeBytes;
+    case 5: return static_cast<size_t>(batch) * csa2::idx_tiles(capacity) * csa2::kIdxTileScaleBytes;
     case 6: return static_cast<size_t>(batch) * csa2::kWin * (swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
     case 7: return static_cast<size_t>(batch) * csa2::kWin * csa2::kSwaScaleStride;
     case 8: return static_cast<size_t>(batch) * 4 * 4 * csa2::kDcmp * sizeof(float);
@@ -217,10 +217,15 @@ csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *
                      "csa2_kv_append launch");
 }
 
+size_t csa2_index_score_workspace_size(int32_t batch, int32_t n_heads_idx) {
+  if (batch <= 0 || n_heads_idx <= 0) return 256;
+  return csa2::score_tc_workspace_bytes(batch, n_heads_idx);
+}
+
 csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w, int32_t n_heads_idx,
                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
-                             int32_t pool_block_size, float *scores, int64_t score_stride, int32_t *err_word,
-                             csa2_stream_t stream) {
+                             int32_t pool_block_size, float *scores, int64_t score_stride, void *ws,
+                             size_t ws_bytes, int32_t *err_word, csa2_stream_t stream) {
   csa2_status st = check_cache(cache);
   if (st != CSA2_OK) return st;
   REQUIRE_PTR(q_idx);
@@ -256,7 +261,14 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, con
   a.scores = scores;
   a.stride = score_stride;  // row stride of scores in both modes
   a.err = err_word;
-  return cuda_status(csa2::launch_index_score(a, reinterpret_cast<cudaStream_t>(stream)), "csa2_index_score launch");
+  const size_t need = csa2_index_score_workspace_size(cache->batch, n_heads_idx);
+  REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "index-score workspace %zu < %zu bytes", ws_bytes,
+          need);
+  REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pool && pool_block_size != 8)
+    return cuda_status(csa2::launch_index_score(a, s), "csa2_index_score launch");
+  return cuda_status(csa2::launch_index_score_tc(a, ws, s), "csa2_index_score launch");
 }
 
 size_t csa2_topk_workspace_size(int32_t batch, int64_t score_stride, int32_t k, int32_t out_pool_blocks) {
@@ -382,7 +394,8 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
 namespace {
 struct PrefillLayout {
   int qb;  // queries per block
-  size_t off_P, off_qpos, off_ring_c, off_ring_s, off_lin_c, off_lin_s, off_scores, off_sel, off_attn, total;
+  size_t off_P, off_qpos, off_ring_c, off_ring_s, off_lin_c, off_lin_s, off_scores, off_qrec, off_sel, off_attn,
+      total;
 };
 
 PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dtype) {
@@ -409,6 +422,8 @@ PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dt
   o = align256(o + static_cast<size_t>(Q) * csa2::kSwaScaleStride);
   L.off_scores = o;
   o = align256(o + static_cast<size_t>(qb) * capacity * 4);
+  L.off_qrec = o;
+  o = align256(o + csa2::score_tc_workspace_bytes(qb, 128));
   L.off_sel = o;
   o = align256(o + csa2::select_workspace_bytes(qb, capacity));
   L.off_attn = o;
@@ -490,7 +505,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     sa.scores = scores;
     sa.stride = cache->capacity;
     sa.err = err_word;
-    e = csa2::launch_index_score(sa, s);
+    e = csa2::launch_index_score_tc(sa, wb + L.off_qrec, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill score");
     csa2::SelArgs se{};
     se.rows = nq;

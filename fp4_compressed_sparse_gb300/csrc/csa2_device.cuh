@@ -24,6 +24,24 @@ constexpr int kDcmp = CSA2_D_CMP;    // 704
 constexpr int kWin = CSA2_WINDOW;    // 128
 constexpr int kSwaScaleStride = 32;  // bytes per window slot in swa_scales (18 used)
 
+// Indexer-key planes are stored tile-major, in the operand layout the
+// block-scaled tensor-core MMA reads, so that a 128-entry tile is one
+// contiguous 8 KB code block plus one 512 B scale block:
+//   codes: tile*8192 + chunk*2048 + m*16 + byte   (m = entry % 128, chunk = 16-byte
+//          piece = one 32-value MXFP4 block of the 128-dim key)
+//   scales: tile*512 + 16*(m % 32) + 4*(m / 32) + block
+constexpr int kIdxTile = 128;
+constexpr int kIdxTileCodeBytes = 8192;
+constexpr int kIdxTileScaleBytes = 512;
+__host__ __device__ __forceinline__ int64_t idx_tiles(int64_t capacity) { return (capacity + kIdxTile - 1) / kIdxTile; }
+__host__ __device__ __forceinline__ size_t idx_code_off(int64_t seq_tiles_base, int64_t e, int chunk) {
+  return static_cast<size_t>(seq_tiles_base + e / kIdxTile) * kIdxTileCodeBytes + chunk * 2048 + (e % kIdxTile) * 16;
+}
+__host__ __device__ __forceinline__ size_t idx_scale_off(int64_t seq_tiles_base, int64_t e) {
+  const int m = static_cast<int>(e % kIdxTile);
+  return static_cast<size_t>(seq_tiles_base + e / kIdxTile) * kIdxTileScaleBytes + 16 * (m % 32) + 4 * (m / 32);
+}
+
 // ---------------------------------------------------------------- error word
 __device__ __forceinline__ void raise_err(int32_t *err, uint32_t bit) {
   if (err) atomicOr(reinterpret_cast<unsigned int *>(err), bit);

@@ -40,8 +40,9 @@ __device__ __forceinline__ void warp_encode_entry(const csa2_cache &c, int b, in
     for (int i = 0; i < 32; ++i) x[i] = row[kDqk + 32 * blk + i];
     uint32_t w[4];
     quant_mxfp4_32(x, w, &sc);
-    reinterpret_cast<uint4 *>(c.idx_codes + ent * 64)[blk] = make_uint4(w[0], w[1], w[2], w[3]);
-    c.idx_scales[ent * 4 + blk] = static_cast<uint8_t>(sc);
+    const int64_t tbase = static_cast<int64_t>(b) * idx_tiles(c.capacity);
+    *reinterpret_cast<uint4 *>(c.idx_codes + idx_code_off(tbase, e, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
+    c.idx_scales[idx_scale_off(tbase, e) + blk] = static_cast<uint8_t>(sc);
   }
 }
 

@@ -30,7 +30,10 @@ struct ScoreArgs {
   int64_t stride;
   int32_t *err;
 };
-cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);
+cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);  // CUDA cores (dp4a)
+// tensor cores (tcgen05 kind::mxf4); needs pool == nullptr or pool_bs == 8, heads <= 128
+size_t score_tc_workspace_bytes(int rows, int heads);
+cudaError_t launch_index_score_tc(const ScoreArgs &a, void *ws, cudaStream_t s);
 
 // ------------------------------------------------------------------ top-k
 enum SelMode { kSelFull = 0, kSelPool = 1, kSelBlockMax = 2 };

@@ -68,13 +68,12 @@ __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
     }
     if (s >= T) return;
   }
-  const size_t ent = static_cast<size_t>(seq) * a.cap + s;
-  const uint4 *kc = reinterpret_cast<const uint4 *>(a.idx_codes + ent * 64);
-  const uint32_t ksc = *reinterpret_cast<const uint32_t *>(a.idx_scales + ent * 4);
+  const int64_t tbase = static_cast<int64_t>(seq) * idx_tiles(a.cap);
+  const uint32_t ksc = *reinterpret_cast<const uint32_t *>(a.idx_scales + idx_scale_off(tbase, s));
   uint32_t kw[32];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const uint4 u = kc[v];
+    const uint4 u = *reinterpret_cast<const uint4 *>(a.idx_codes + idx_code_off(tbase, s, v));
     const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

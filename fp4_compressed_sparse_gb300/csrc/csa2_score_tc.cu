@@ -1,0 +1,422 @@
+// csa2_score_tc.cu -- lightning-indexer scores on the 5th-generation tensor cores.
+//
+// [P5] "DeepSeek-V4: Towards Highly Efficient Million-Token Context
+// Intelligence" §2.3.1: I_{t,s} = sum_h w_{t,h} * ReLU(q_{t,h} . K_s); §2.3.4:
+// the indexer QK product runs in FP4.  Keys and queries are MXFP4 (E2M1 with an
+// E8M0 scale per 32), which is exactly the operand format of
+// tcgen05.mma kind::mxf4 block_scale: the tensor core applies both scales and
+// accumulates in fp32.  Each 32-wide block sum of E2M1 products is an exact
+// small integer, so every accumulator holds the fp32 value of the exact dot
+// whenever that value is representable (block exponents of a pair within 9
+// binades) -- the same number the CUDA-core path and the oracle produce.
+//
+// One 128-key tile = one MMA pair: M = 128 keys (TMEM lanes), N = padded
+// indexer heads (TMEM columns), K = 128 (two K=64 instructions).  The epilogue
+// thread of a key reads its N accumulators and runs the fixed-order chain
+// acc = fma(w_h, max(d_h, +0), acc).
+//
+// Persistent CTA per SM, warp-specialised:
+//   warp 0      producer: bulk copies of the key tiles (8 KB codes + 512 B
+//               scales, already stored in the MMA operand layout) into an
+//               8-stage ring; Reindex (POOL) tiles are gathered by the warp;
+//               the per-row query operand goes to one of two B slots
+//   warp 1      MMA issuer: scale factors to TMEM (tcgen05.cp), two MMAs,
+//               commits that free the stage and hand the accumulator over
+//   warps 2..9  epilogue: warps 2-5 own accumulator 0 (even tiles), 6-9
+//               accumulator 1 (odd tiles); each warp reads its 32-lane quarter
+// Every mbarrier wait is bounded; a wait that runs out raises
+// CSA2_DEVERR_TIMEOUT, sets a CTA abort flag and the CTA drains and exits.
+#include "csa2_internal.cuh"
+#include "csa2_tc.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kStages = 8;
+constexpr int kAcc = 3;                 // TMEM accumulator buffers (tiles in flight in the epilogue)
+constexpr int kEpiWarps = 4 * kAcc;     // four warps (one per TMEM lane quarter) per accumulator
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
+constexpr int kMaxRowsPerCta = 256;
+constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
+
+// Per-row query record built by k_qprep: B codes (NP x 64 B, K-major no-swizzle:
+// chunk c of head h at c*NP*16 + h*16), SFB atom (512 B), w (NP floats).
+__host__ __device__ __forceinline__ int qrec_bytes(int np) { return np * 64 + 512 + np * 4; }
+
+__global__ void __launch_bounds__(128) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out) {
+  const int r = blockIdx.x;
+  uint8_t *rec = out + static_cast<size_t>(r) * qrec_bytes(np);
+  uint8_t *sfb = rec + np * 64;
+  float *wr = reinterpret_cast<float *>(sfb + 512);
+  for (int i = threadIdx.x; i < 512 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(sfb)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  for (int task = threadIdx.x; task < np * 4; task += blockDim.x) {
+    const int h = task >> 2, blk = task & 3;
+    uint32_t w4[4] = {0, 0, 0, 0}, sc = 0;
+    if (h < H) {
+      const uint16_t *src = q_idx + (static_cast<size_t>(r) * H + h) * kDi + 32 * blk;
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(static_cast<uint32_t>(src[i]) << 16);
+      quant_mxfp4_32(x, w4, &sc);
+    }
+    *reinterpret_cast<uint4 *>(rec + blk * np * 16 + h * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    sfb[16 * (h % 32) + 4 * (h / 32) + blk] = static_cast<uint8_t>(sc);
+  }
+  for (int h = threadIdx.x; h < np; h += blockDim.x) wr[h] = h < H ? w[static_cast<size_t>(r) * H + h] : 0.0f;
+}
+
+struct TcArgs {
+  ScoreArgs s;
+  const uint8_t *qrec;  // [rows][qrec_bytes(np)]
+  int np;               // heads padded to a multiple of 16
+  int ncols;            // TMEM columns allocated
+};
+
+__device__ __forceinline__ int64_t row_slots(const TcArgs &a, int r) {
+  if (a.s.pool) return static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs;
+  int64_t T = a.s.q_pos[r] / a.s.ratio;
+  if (T < 0) T = 0;
+  return min(T, min(a.s.cap, a.s.stride));
+}
+__device__ __forceinline__ int row_tiles(const TcArgs &a, int r) {
+  return static_cast<int>((row_slots(a, r) + kIdxTile - 1) / kIdxTile);
+}
+
+struct __align__(1024) Smem {
+  uint8_t stage[kStages][kStageBytes];
+  uint8_t bslot[2][128 * 64 + 512 + 128 * 4];
+  // mbarriers in their own 128-byte lines: generic loads/stores that share a
+  // line with them slow every barrier operation down
+  __align__(128) uint64_t full[kStages];
+  __align__(128) uint64_t empty[kStages];
+  __align__(128) uint64_t tfull[kAcc];
+  __align__(128) uint64_t tempty[kAcc];
+  __align__(128) uint64_t bfull[2];
+  __align__(128) uint64_t bempty[2];
+  __align__(128) uint32_t tmem;
+  int abort;   // written only when a wait gives up
+  int issued;  // items whose copies the producer started (written once, at exit)
+  __align__(128) int nt[kMaxRowsPerCta];  // visible tiles of the rows this CTA touches (row - row0)
+};
+
+// Bounded wait for one thread; a wait that runs out raises the timeout bit.
+__device__ __forceinline__ bool wait1(Smem &sm, uint64_t *bar, uint32_t phase, int32_t *err) {
+  if (tc::mbar_wait_bounded(bar, phase, kWaitIters)) return true;
+  *reinterpret_cast<volatile int *>(&sm.abort) = 1;
+  raise_err(err, CSA2_DEVERR_TIMEOUT);
+  return false;
+}
+
+// Warp-uniform bounded wait: lane 0 waits, the whole warp gets the same answer.
+__device__ __forceinline__ bool wait_warp(Smem &sm, uint64_t *bar, uint32_t phase, int32_t *err) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait1(sm, bar, phase, err) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(tc::smem_addr(bar))
+               : "memory");
+}
+
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int max_tiles, int64_t total_items,
+                                                                int64_t per_cta) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * per_cta;
+  const int64_t i1 = min(total_items, i0 + per_cta);
+  // items are (row, tile < max_tiles), row-major; a tile past the row's visible
+  // length is empty and every role skips it the same way
+  constexpr int np = NP;
+  const int brec = qrec_bytes(np);
+  const bool pool_mode = a.s.pool != nullptr;
+  const int64_t seq_tiles = idx_tiles(a.s.cap);
+
+  if (warp == 0) {
+    tc::tmem_alloc(&sm.tmem, a.ncols);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sm.full[s], 1);
+      tc::mbar_init(&sm.empty[s], 1);
+    }
+    for (int i = 0; i < kAcc; ++i) {
+      tc::mbar_init(&sm.tfull[i], 1);
+      tc::mbar_init(&sm.tempty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm.bfull[i], 1);
+      tc::mbar_init(&sm.bempty[i], 1 + kEpiWarps);
+    }
+    sm.abort = 0;
+    sm.issued = 0;
+    tc::fence_mbar_init();
+  }
+  // visible tile count of every row in this CTA's item range, computed once
+  const int row0 = static_cast<int>(i0 / max_tiles);
+  const int row_last = i1 > i0 ? static_cast<int>((i1 - 1) / max_tiles) : row0;
+  const int nrows = row_last - row0 + 1;
+  for (int r = threadIdx.x; r < nrows && r < kMaxRowsPerCta; r += blockDim.x) sm.nt[r] = row_tiles(a, row0 + r);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  auto tiles_of = [&](int row) -> int {
+    const int k = row - row0;
+    return k < kMaxRowsPerCta ? sm.nt[k] : row_tiles(a, row);
+  };
+  // TMEM columns: accumulators [0, kAcc*np), SFA per accumulator at kAcc*np + 8*i,
+  // SFB per B slot at kAcc*np + 8*kAcc + 8*i
+  const uint32_t col_sfa = kAcc * np, col_sfb = kAcc * np + 8 * kAcc;
+
+  // Every role walks the same (row, tile) sequence and skips the same empty
+  // tiles; a row's visible tile count is read once, when the walk enters it.
+  const int tile_begin = static_cast<int>(i0 - static_cast<int64_t>(row0) * max_tiles);
+
+  if (warp == 0 && (lane == 0 || pool_mode)) {
+    // ------------------------------------------------------------ producer
+    // FULL: lane 0 alone issues two bulk copies per tile; POOL: the warp gathers.
+    int prev_row = -1, bchanges = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
+    for (int64_t it = i0; it < i1; ++it) {
+      if (tile < nt) {
+        const int s = j % kStages;
+        bool ok = true;
+        if (j >= kStages) ok = pool_mode ? wait_warp(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err)
+                                         : wait1(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err);
+        if (!ok) break;
+        if (row != prev_row) {
+          const int bs = bchanges & 1;
+          if (bchanges >= 2) {
+            ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
+                           : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            tc::mbar_expect_tx(&sm.bfull[bs], brec);
+            bulk_g2s(tc::smem_addr(sm.bslot[bs]), a.qrec + static_cast<size_t>(row) * brec, brec, &sm.bfull[bs]);
+          }
+          prev_row = row;
+          ++bchanges;
+        }
+        const int seq = a.s.cache_seq < 0 ? row : a.s.cache_seq;
+        uint8_t *dst = sm.stage[s];
+        if (!pool_mode) {
+          const size_t t = static_cast<size_t>(seq * seq_tiles + tile);
+          tc::mbar_expect_tx(&sm.full[s], kStageBytes);
+          bulk_g2s(tc::smem_addr(dst), a.s.idx_codes + t * kIdxTileCodeBytes, kIdxTileCodeBytes, &sm.full[s]);
+          bulk_g2s(tc::smem_addr(dst + kIdxTileCodeBytes), a.s.idx_scales + t * kIdxTileScaleBytes,
+                   kIdxTileScaleBytes, &sm.full[s]);
+        } else {
+          // 16 pool blocks of 8 keys: lane l handles block l/2, chunks 2*(l%2)..+1
+          const int jb = lane >> 1;
+          const int pidx = tile * 16 + jb;
+          const int32_t pid =
+              pidx < a.s.pool_blocks ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + pidx] : -1;
+          const int64_t p0 = static_cast<int64_t>(pid) * a.s.pool_bs;
+          const bool okb = pid >= 0 && p0 + a.s.pool_bs <= seq_tiles * kIdxTile;
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * (lane & 1) + cc;
+            for (int i = 0; i < 8; ++i) {
+              uint4 v = make_uint4(0, 0, 0, 0);
+              if (okb) v = *reinterpret_cast<const uint4 *>(a.s.idx_codes + idx_code_off(seq * seq_tiles, p0 + i, c));
+              *reinterpret_cast<uint4 *>(dst + c * 2048 + (jb * 8 + i) * 16) = v;
+            }
+          }
+          for (int i = (lane & 1) * 4; i < (lane & 1) * 4 + 4; ++i) {
+            const int m = jb * 8 + i;
+            uint32_t v = 0;
+            if (okb) v = *reinterpret_cast<const uint32_t *>(a.s.idx_scales + idx_scale_off(seq * seq_tiles, p0 + i));
+            *reinterpret_cast<uint32_t *>(dst + kIdxTileCodeBytes + 16 * (m % 32) + 4 * (m / 32)) = v;
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sm.full[s]);
+        }
+        ++j;
+      }
+      if (++tile == max_tiles) {
+        tile = 0;
+        ++row;
+        if (it + 1 < i1) nt = tiles_of(row);
+      }
+    }
+    if (lane == 0) sm.issued = j;
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
+    const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
+    for (int64_t it = i0; it < i1; ++it) {
+      if (tile < nt) {
+        const int s = j % kStages, acc = j % kAcc;
+        if (row != prev_row) {
+          bs = bchanges & 1;
+          if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) break;
+          prev_row = row;
+          ++bchanges;
+          tc::tc_fence_after();
+          tc::tmem_cp_32x128b_x4(tmem + col_sfb + 8 * bs,
+                                 tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
+        }
+        if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) break;
+        if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) break;
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
+        tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
+        const uint32_t d = tmem + acc * np;
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
+                     tmem + col_sfa + 8 * acc, tmem + col_sfb + 8 * bs, 0);
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
+                     tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc,
+                     tmem + col_sfb + 8 * bs, 1);
+        tc::mma_commit(&sm.empty[s]);
+        tc::mma_commit(&sm.tfull[acc]);
+        if (tile + 1 >= nt || it + 1 >= i1) tc::mma_commit(&sm.bempty[bs]);
+        ++j;
+      }
+      if (++tile == max_tiles) {
+        tile = 0;
+        ++row;
+        if (it + 1 < i1) nt = tiles_of(row);
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;           // 0 .. kEpiWarps-1
+    const int parity = e >> 2;        // accumulator buffer this warp drains (tiles j % kAcc == parity)
+    const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+    const int m = 32 * quarter + lane;
+    int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
+    int64_t row_nslots = row_slots(a, row0);
+    for (int64_t it = i0; it < i1; ++it) {
+      if (tile < nt) {
+        if (row != prev_row) {
+          bs = bchanges & 1;
+          prev_row = row;
+          ++bchanges;
+        }
+        const bool last_of_row = tile + 1 >= nt || it + 1 >= i1;
+        if (j % kAcc == parity) {
+          if (!wait_warp(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err)) break;
+          if (!wait_warp(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err)) break;
+          tc::tc_fence_after();
+          const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
+          uint32_t r[np];
+#pragma unroll
+          for (int h0 = 0; h0 < np; h0 += 16) tc::tmem_ld_32x32b_x16(base + h0, r + h0);
+          tc::tmem_ld_wait();
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
+          const float *wv = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
+          float acc = 0.0f;
+#pragma unroll
+          for (int h = 0; h < np; ++h) {
+            const float d = __uint_as_float(r[h]);
+            acc = __fmaf_rn(wv[h], d > 0.0f ? d : 0.0f, acc);
+          }
+          const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
+          bool valid;
+          if (!pool_mode) {
+            valid = slot < row_nslots;
+          } else {
+            const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
+                                    ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
+                                    : -1;
+            const int64_t T = a.s.q_pos[row] / a.s.ratio;
+            const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
+            valid = pid >= 0 && p < T && p < a.s.cap;
+            if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
+          }
+          if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
+        }
+        if (last_of_row && lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
+        ++j;
+      }
+      if (++tile == max_tiles) {
+        tile = 0;
+        ++row;
+        if (it + 1 < i1) {
+          nt = tiles_of(row);
+          row_nslots = row_slots(a, row);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    // copies still in flight (only after an abort): bounded wait on the last items issued
+    if (*reinterpret_cast<volatile int *>(&sm.abort) && lane == 0) {  // after a timeout only
+      const int n = sm.issued;
+      for (int jj = n > kStages ? n - kStages : 0; jj < n; ++jj)
+        tc::mbar_wait_bounded(&sm.full[jj % kStages], (jj / kStages) & 1, kWaitIters);
+    }
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, a.ncols);
+  }
+}
+
+}  // namespace
+
+size_t score_tc_workspace_bytes(int rows, int heads) {
+  const int np = ((heads + 15) / 16) * 16;
+  return static_cast<size_t>(rows) * qrec_bytes(np) + 256;
+}
+
+cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st) {
+  if (s.rows <= 0) return cudaSuccess;
+  TcArgs a{};
+  a.s = s;
+  a.np = ((s.heads + 15) / 16) * 16;
+  a.qrec = static_cast<const uint8_t *>(ws);
+  const int cols = kAcc * a.np + 8 * kAcc + 16;
+  a.ncols = cols <= 128 ? 128 : (cols <= 256 ? 256 : 512);
+  k_qprep<<<s.rows, 128, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
+  const int max_tiles = static_cast<int>(
+      s.pool ? (static_cast<int64_t>(s.pool_blocks) * s.pool_bs + kIdxTile - 1) / kIdxTile
+             : idx_tiles(s.cap < s.stride ? s.cap : s.stride));
+  const int64_t total = static_cast<int64_t>(s.rows) * max_tiles;
+  if (total <= 0) return cudaGetLastError();
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (num_sms <= 0) num_sms = 148;
+  }
+  const size_t smem = sizeof(Smem) + 1024;
+  using KernelFn = void (*)(TcArgs, int, int64_t, int64_t);
+  KernelFn fn = nullptr;
+  switch (a.np) {
+    case 16: fn = k_index_score_tc<16>; break;
+    case 32: fn = k_index_score_tc<32>; break;
+    case 48: fn = k_index_score_tc<48>; break;
+    case 64: fn = k_index_score_tc<64>; break;
+    case 80: fn = k_index_score_tc<80>; break;
+    case 96: fn = k_index_score_tc<96>; break;
+    case 112: fn = k_index_score_tc<112>; break;
+    default: fn = k_index_score_tc<128>; break;
+  }
+  static bool attr[9] = {};
+  const int slot = a.np / 16;
+  if (!attr[slot]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr[slot] = true;
+  }
+  const int64_t grid = total < num_sms ? total : num_sms;
+  const int64_t per = (total + grid - 1) / grid;
+  fn<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, max_tiles, total, per);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

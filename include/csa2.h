@@ -56,6 +56,7 @@ typedef enum csa2_status {
 #define CSA2_DEVERR_INDEX 2u    /* an index / pool id outside the visible cache (skipped) */
 #define CSA2_DEVERR_NAN 4u      /* a NaN index score (it ranks lowest)                */
 #define CSA2_DEVERR_ROPE 8u     /* a position outside the RoPE table (nothing written) */
+#define CSA2_DEVERR_TIMEOUT 16u /* a bounded device wait gave up (outputs unspecified)  */
 
 /* sliding-window storage */
 #define CSA2_SWA_BF16 0  /* 576 bf16 values, 1,152 B per token                         */
@@ -86,6 +87,12 @@ typedef enum csa2_status {
  *   rope_scales   4 B  one E4M3 scale per 16                       -> 36 B sidecar
  *   idx_codes    64 B  E2M1 codes of the 128-dim indexer key
  *   idx_scales    4 B  one E8M0 scale per 32 (MXFP4)               -> 68 B indexer entry
+ *   The two indexer planes are tile-major: [batch][ceil(capacity/128)][8192 B]
+ *   and [batch][ceil(capacity/128)][512 B], in the operand layout of the
+ *   block-scaled tensor-core MMA.  For entry e (tile = e/128, m = e%128) the
+ *   16 code bytes of 32-value block j sit at tile*8192 + j*2048 + m*16 and its
+ *   scale byte at tile*512 + 16*(m%32) + 4*(m/32) + j.  csa2_cache_plane_bytes()
+ *   gives every plane's size.
  * swa_codes / swa_scales: the sliding-window ring, [batch][128][576] codes
  *   (E4M3 bytes, or bf16 when swa_dtype == CSA2_SWA_BF16) and [batch][128][32]
  *   scale bytes (18 used, MXFP8 only); token t lives in slot t % 128 ([P5]
@@ -174,11 +181,17 @@ csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *
  *   score of position pool[b][j]*pool_block_size + i when it is visible.
  * score_stride: floats per sequence in scores (>= capacity for FULL,
  *   >= pool_blocks*pool_block_size for POOL).  n_heads_idx in 1..128.
+ * ws: device workspace of csa2_index_score_workspace_size() bytes (the
+ *   quantised queries in the tensor-core operand layout).
+ * The contraction runs on the tensor cores (block-scaled MXFP4 MMA) for FULL
+ * and for POOL with pool_block_size 8; other block sizes use CUDA cores.
  */
+size_t csa2_index_score_workspace_size(int32_t batch, int32_t n_heads_idx);
 csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
                              int32_t n_heads_idx, const int64_t *q_pos, const int32_t *pool,
                              int32_t pool_blocks, int32_t pool_block_size, float *scores,
-                             int64_t score_stride, int32_t *err_word, csa2_stream_t stream);
+                             int64_t score_stride, void *ws, size_t ws_bytes, int32_t *err_word,
+                             csa2_stream_t stream);
 
 /*
  * csa2_topk: top-k selector ([P5] §2.3.1 "Top-k(I_{t,:})") over the candidates

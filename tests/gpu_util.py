@@ -72,9 +72,11 @@ def build_r2(orc, batch, n_tokens, swa_dtype, seed, chunks=None, cap=None, theta
 
 
 def assert_cache_equal(c, oc, n_entries, check_swa=True):
+    ic, isc = c.idx_entries()
+    planes = {"idx_codes": ic, "idx_scales": isc}
     for b, o in enumerate(oc):
         for name in ("lat_codes", "lat_scales", "rope_codes", "rope_scales", "idx_codes", "idx_scales"):
-            g = getattr(c, name)[b, :n_entries].cpu().numpy()
+            g = planes.get(name, getattr(c, name, None))[b, :n_entries].cpu().numpy()
             ref = getattr(o, name)[:n_entries]
             bad = np.argwhere(g != ref)
             assert bad.size == 0, f"seq {b} {name}: {len(bad)} bytes differ, first {bad[:3].tolist()}"

@@ -50,8 +50,8 @@ def test_host_validation_codes(lib):
     st = csa2.CacheStruct(1, 16, 3, 1, *([fake] * 10))
     assert lib.csa2_kv_append(ctypes.byref(st), None, None, 0, None, None, 1, 1, None, None, None) == 4
     st = csa2.CacheStruct(0, 16, 1, 1, *([fake] * 10))
-    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None,
-                                None) == 2
+    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None, 0,
+                                None, None) == 2
     st = csa2.CacheStruct(1, 16, 1, 1, *([fake] * 10))
     st.lat_codes = fake + 8  # misaligned
     assert lib.csa2_sparse_attn_decode(ctypes.byref(st), None, 64, None, None, 512, None, 0.1, None,
@@ -86,7 +86,10 @@ def test_rope_table_matches_oracle(lib, orc):
 
 def test_cache_plane_bytes_match_record(lib):
     # 288 B main + 36 B sidecar + 68 B indexer per entry; MXFP8 window 576 + scales
-    per = [lib.csa2_cache_plane_bytes(1, 1, p, 1) for p in range(6)]
+    per = [lib.csa2_cache_plane_bytes(1, 128, p, 1) / 128 for p in range(6)]
     assert per[0] + per[1] == 288 and per[2] + per[3] == 36 and per[4] + per[5] == 68
+    # indexer planes are stored in whole 128-entry tiles
+    assert lib.csa2_cache_plane_bytes(2, 129, 4, 1) == 2 * 2 * 8192
+    assert lib.csa2_cache_plane_bytes(2, 129, 5, 1) == 2 * 2 * 512
     assert lib.csa2_cache_plane_bytes(1, 1, 6, 1) == 128 * 576
     assert lib.csa2_cache_plane_bytes(1, 1, 6, 0) == 128 * 1152

@@ -73,7 +73,7 @@ def _decode_inputs(B, H_I, H, seed, step=0):
     return q_idx, w, q
 
 
-@pytest.mark.parametrize("H_I", [4, 64])
+@pytest.mark.parametrize("H_I", [4, 20, 64, 128])
 def test_index_score_full_and_topk_bitexact(orc, H_I):
     B, T = 2, 1500
     c, oc, _, err = build_r1(orc, B, T, csa2.SWA_MXFP8, seed=21)
@@ -99,6 +99,35 @@ def test_index_score_full_and_topk_bitexact(orc, H_I):
         assert idx[b].tolist() == orc.topk(ref, k).tolist()
         pids, cnt = orc.pool(ref, Tv, 8, 32)
         assert pcount[b].item() == cnt and pool[b].tolist() == pids.tolist()
+
+
+def test_index_score_block_scale_spread(orc):
+    """Keys whose four 32-dim blocks differ in magnitude by up to 2^6 (and queries by
+    up to 2^2): the block-scaled tensor-core dot must still equal the exact dot."""
+    from gpu_util import build_r1  # noqa: F401
+    B, T, H_I = 1, 700, 16
+    cap = T + 8
+    c = csa2.Cache(B, cap, ratio=1)
+    rope = csa2.rope_table(1e4, cap + 8)
+    oc = orc.Cache(cap)
+    g = torch.Generator().manual_seed(71)
+    kv = torch.randn((T, 576), generator=g)
+    ik = torch.randn((T, 128), generator=g)
+    fac = torch.tensor([2.0 ** -3, 1.0, 2.0 ** 3, 0.5]).repeat_interleave(32)
+    ik = ik * fac
+    csa2.kv_append(c, kv[None].cuda(), ik[None].cuda(), rope)
+    orc.append_r1(oc, kv.numpy(), ik.numpy(), 1e4)
+    q_idx = (torch.randn((B, H_I, 128), generator=g) *
+             torch.tensor([1.0, 2.0, 0.5, 4.0]).repeat_interleave(32)).to(torch.bfloat16)
+    w = torch.rand((B, H_I), generator=g)
+    q_pos = torch.full((B,), T - 1, dtype=torch.int64, device="cuda")
+    scores = torch.empty((B, cap), device="cuda")
+    csa2.index_score(c, q_idx.cuda(), w.cuda(), q_pos, scores)
+    torch.cuda.synchronize()
+    ref, flags = orc.index_scores(oc, u16(q_idx[0]), w[0].numpy(), n_vis=T - 1)
+    assert flags == 0
+    got = scores[0, :T - 1].cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
 def test_topk_ties_zero_weight_and_short_context(orc):
@@ -263,9 +292,10 @@ def test_prefill_chunk_small(orc):
                   for t in range(max(0, prior - 128), prior)}
     orc.append_r2(o, *[r.numpy() for r in rows], ba.numpy(), bb.numpy(), 1e4)
     # the appended chunk: cache bytes of this sequence match
-    for name in ("lat_codes", "idx_codes", "rope_codes"):
-        n_e = (prior + Q) // 2
+    n_e = (prior + Q) // 2
+    for name in ("lat_codes", "rope_codes"):
         assert np.array_equal(getattr(c, name)[seq, :n_e].cpu().numpy(), getattr(o, name)[:n_e])
+    assert np.array_equal(c.idx_entries()[0][seq, :n_e].cpu().numpy(), o.idx_codes[:n_e])
     chunk_win = {}
     for i in range(Q):
         t = prior + i
