@@ -161,6 +161,7 @@ class FullDecode:
         self.ws_topk = csa2.topk_workspace(B, self.cap, W.topk, W.pool_blocks)
         self.ws_attn = csa2.attn_workspace(B, W.heads, W.topk)
         self.ws_score = csa2.index_score_workspace(B, W.index_heads)
+        self.aux = csa2.score_aux(B, self.cap)
         self.launches_per_step = None
 
     PARTS = ("append", "score", "topk_pool", "attention")
@@ -171,10 +172,10 @@ class FullDecode:
             c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
         elif name == "score":
             c.index_score(self.cache, self.q_idx[s], self.w[s], self.q_pos[s], self.scores, err=self.err,
-                          ws=self.ws_score)
+                          ws=self.ws_score, aux=self.aux)
         elif name == "topk_pool":
             c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
-                   pool_count=self.pool_cnt, err=self.err)
+                   pool_count=self.pool_cnt, err=self.err, aux=self.aux)
         else:
             c.sparse_attn_decode(self.cache, self.q[s], self.q_pos[s], self.idx, self.out, self.lse,
                                  self.ws_attn, W.sm_scale, err=self.err)
@@ -189,9 +190,10 @@ class FullDecode:
 
     @staticmethod
     def kernel_launches(n_splits_gt1=False):
-        # kv_append ratio 1: append + advance; index_score: q prep + score; topk: 3 x (hist, resolve) + count
-        # + write, twice (top-k, then the pool); attention: 1 (+ combine when split)
-        return 2 + 2 + 16 + 1 + (1 if n_splits_gt1 else 0)
+        # kv_append ratio 1: append + advance; index_score: q prep + score (the sideband clear is a
+        # memset); topk from the sideband: resolve, collect, final (top-k and pool in the same
+        # launches); attention: 1 (+ combine when split)
+        return 2 + 2 + 3 + 1 + (1 if n_splits_gt1 else 0)
 
 
 # ----------------------------------------------------------------------------- our arm

@@ -23,7 +23,7 @@ D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128
 
 EXPORTS = [
     "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
-    "csa2_index_score",
+    "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_status_string",
     "csa2_last_error_detail", "csa2_version",
@@ -76,9 +76,10 @@ def load() -> ctypes.CDLL:
         "csa2_rope_table": (i32, [f64, i64, vp]),
         "csa2_kv_append": (i32, [vp, vp, vp, i32, vp, vp, i64, i32, vp, vp, vp]),
         "csa2_index_score_workspace_size": (sz, [i32, i32]),
-        "csa2_index_score": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, sz, vp, vp]),
+        "csa2_score_aux_size": (sz, [i32, i64]),
+        "csa2_index_score": (i32, [vp, vp, vp, i32, vp, vp, i32, i32, vp, i64, vp, vp, sz, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32, i32]),
-        "csa2_topk": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, sz, vp, vp]),
+        "csa2_topk": (i32, [vp, i64, vp, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, sz, vp, vp]),
         "csa2_topk_noalloc": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, i32, vp, i32, vp, vp, vp, vp]),
         "csa2_attn_workspace_size": (sz, [i32, i32, i32]),
         "csa2_sparse_attn_decode": (i32, [vp, vp, i32, vp, vp, i32, vp, f32, vp, vp, vp, sz, vp, vp]),
@@ -189,13 +190,20 @@ def index_score_workspace(batch, heads_idx, device="cuda"):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
+def score_aux(batch, stride, device="cuda"):
+    """A buffer for the score sideband csa2_index_score can leave for csa2_topk."""
+    n = load().csa2_score_aux_size(batch, stride)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
 _ws_cache = {}
 
 
 def index_score(cache: Cache, q_idx, w, q_pos, scores, pool=None, pool_block_size=8, err=None,
-                stream=None, ws=None):
+                stream=None, ws=None, aux=None):
     """csa2_index_score: q_idx bf16 [B,H_I,128], w fp32 [B,H_I], q_pos int64 [B],
-    scores fp32 [B, stride]; pool int32 [B, pool_blocks] for a Reindex layer."""
+    scores fp32 [B, stride]; pool int32 [B, pool_blocks] for a Reindex layer;
+    aux (optional, from score_aux()) receives the sideband for topk()."""
     L = load()
     if ws is None:
         key = (q_idx.shape[0], q_idx.shape[1], q_idx.device)
@@ -204,7 +212,7 @@ def index_score(cache: Cache, q_idx, w, q_pos, scores, pool=None, pool_block_siz
             ws = _ws_cache[key] = index_score_workspace(q_idx.shape[0], q_idx.shape[1], q_idx.device)
     st = L.csa2_index_score(cache.ref(), _ptr(q_idx), _ptr(w), q_idx.shape[1], _ptr(q_pos),
                             _ptr(pool), pool.shape[1] if pool is not None else 0, pool_block_size,
-                            _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(), _ptr(err),
+                            _ptr(scores), scores.shape[1], _ptr(aux), _ptr(ws), ws.numel(), _ptr(err),
                             _stream(stream))
     _check("csa2_index_score", st)
 
@@ -215,10 +223,10 @@ def topk_workspace(batch, stride, k, out_pool_blocks=0, device="cuda"):
 
 
 def topk(scores, ratio, q_pos, k, idx_out, ws, pool=None, pool_block_size=8, pool_out=None,
-         pool_count=None, err=None, stream=None):
-    """csa2_topk over the candidates csa2_index_score scored."""
+         pool_count=None, err=None, stream=None, aux=None):
+    """csa2_topk over the candidates csa2_index_score scored (aux: its sideband, or None)."""
     L = load()
-    st = L.csa2_topk(_ptr(scores), scores.shape[1], scores.shape[0], ratio, _ptr(q_pos), _ptr(pool),
+    st = L.csa2_topk(_ptr(scores), scores.shape[1], _ptr(aux), scores.shape[0], ratio, _ptr(q_pos), _ptr(pool),
                      pool.shape[1] if pool is not None else 0, pool_block_size, k, _ptr(idx_out),
                      pool_out.shape[1] if pool_out is not None else 0, _ptr(pool_out), _ptr(pool_count),
                      _ptr(ws), ws.numel(), _ptr(err), _stream(stream))

@@ -222,9 +222,14 @@ size_t csa2_index_score_workspace_size(int32_t batch, int32_t n_heads_idx) {
   return csa2::score_tc_workspace_bytes(batch, n_heads_idx);
 }
 
+size_t csa2_score_aux_size(int32_t batch, int64_t score_stride) {
+  if (batch <= 0 || score_stride <= 0) return 256;
+  return static_cast<size_t>(batch) * csa2::aux_row_bytes(score_stride);
+}
+
 csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w, int32_t n_heads_idx,
                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
-                             int32_t pool_block_size, float *scores, int64_t score_stride, void *ws,
+                             int32_t pool_block_size, float *scores, int64_t score_stride, void *score_aux, void *ws,
                              size_t ws_bytes, int32_t *err_word, csa2_stream_t stream) {
   csa2_status st = check_cache(cache);
   if (st != CSA2_OK) return st;
@@ -232,6 +237,7 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, con
   REQUIRE_PTR(w);
   REQUIRE_PTR(q_pos);
   REQUIRE_PTR(scores);
+  REQUIRE_OPT_PTR(score_aux);
   REQUIRE(n_heads_idx >= 1 && n_heads_idx <= CSA2_MAX_HEADS, CSA2_ERR_SHAPE, "n_heads_idx %d outside 1..128",
           n_heads_idx);
   if (pool) {
@@ -260,14 +266,36 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, con
   a.pool_bs = pool_block_size;
   a.scores = scores;
   a.stride = score_stride;  // row stride of scores in both modes
+  a.aux = static_cast<uint8_t *>(score_aux);
   a.err = err_word;
   const size_t need = csa2_index_score_workspace_size(cache->batch, n_heads_idx);
   REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "index-score workspace %zu < %zu bytes", ws_bytes,
           need);
   REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (pool && pool_block_size != 8)
-    return cuda_status(csa2::launch_index_score(a, s), "csa2_index_score launch");
+  if (pool && pool_block_size != 8) {
+    // CUDA-core path; the sideband is then built from the scores
+    a.aux = nullptr;
+    cudaError_t e = csa2::launch_index_score(a, s);
+    if (e != cudaSuccess || !score_aux) return cuda_status(e, "csa2_index_score launch");
+    csa2::TopkArgs t{};
+    t.rows = cache->batch;
+    t.scores = scores;
+    t.stride = score_stride;
+    t.ratio = cache->ratio;
+    t.q_pos = q_pos;
+    t.pool = pool;
+    t.pool_blocks = pool_blocks;
+    t.bs = pool_block_size;
+    t.err = err_word;
+    return cuda_status(csa2::launch_fill_aux(t, static_cast<uint8_t *>(score_aux), s), "csa2_index_score sideband");
+  }
+  if (score_aux) {
+    // the histograms are accumulated by the kernel: start from zero
+    cudaError_t e = cudaMemset2DAsync(score_aux, csa2::aux_row_bytes(score_stride), 0, 2 * csa2::kSelBins * 4,
+                                      cache->batch, s);
+    if (e != cudaSuccess) return cuda_status(e, "csa2_index_score sideband clear");
+  }
   return cuda_status(csa2::launch_index_score_tc(a, ws, s), "csa2_index_score launch");
 }
 
@@ -275,14 +303,15 @@ size_t csa2_topk_workspace_size(int32_t batch, int64_t score_stride, int32_t k, 
   (void)k;
   (void)out_pool_blocks;
   if (batch <= 0 || score_stride <= 0) return 256;
-  return csa2::select_workspace_bytes(batch, score_stride);
+  return csa2::topk_workspace_bytes(batch, score_stride, false);
 }
 
-csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio, const int64_t *q_pos,
-                      const int32_t *pool, int32_t pool_blocks, int32_t pool_block_size, int32_t k, int32_t *idx_out,
-                      int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count, void *ws, size_t ws_bytes,
-                      int32_t *err_word, csa2_stream_t stream) {
+csa2_status csa2_topk(const float *scores, int64_t score_stride, const void *score_aux, int32_t batch, int32_t ratio,
+                      const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks, int32_t pool_block_size,
+                      int32_t k, int32_t *idx_out, int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count,
+                      void *ws, size_t ws_bytes, int32_t *err_word, csa2_stream_t stream) {
   REQUIRE_PTR(scores);
+  REQUIRE_OPT_PTR(score_aux);
   REQUIRE_PTR(q_pos);
   REQUIRE_PTR(idx_out);
   REQUIRE(batch >= 1 && batch <= 65535, CSA2_ERR_SHAPE, "batch %d", batch);
@@ -300,39 +329,30 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, 
   if (pool_out) {
     REQUIRE_PTR(pool_out);
     REQUIRE_PTR(pool_count);
-    REQUIRE(out_pool_blocks >= 1 && out_pool_blocks <= 65536, CSA2_ERR_RANGE, "out_pool_blocks %d",
-            out_pool_blocks);
+    REQUIRE(out_pool_blocks >= 1 && out_pool_blocks <= CSA2_MAX_TOPK, CSA2_ERR_RANGE,
+            "out_pool_blocks %d outside 1..2048", out_pool_blocks);
+    REQUIRE(pool_block_size == 8, CSA2_ERR_UNSUPPORTED, "the candidate pool is built from 8-position blocks");
   }
-  const size_t need = csa2_topk_workspace_size(batch, score_stride, k, out_pool_blocks);
+  const size_t need = csa2::topk_workspace_bytes(batch, score_stride, score_aux != nullptr);
   REQUIRE(ws != nullptr && ws_bytes >= need, CSA2_ERR_WORKSPACE, "topk workspace %zu < %zu bytes", ws_bytes, need);
   REQUIRE(aligned16(ws), CSA2_ERR_ALIGN, "ws is not 16-byte aligned");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  csa2::SelArgs a{};
+  csa2::TopkArgs a{};
   a.rows = batch;
   a.scores = scores;
   a.stride = score_stride;
+  a.aux = static_cast<const uint8_t *>(score_aux);
   a.ratio = ratio;
   a.q_pos = q_pos;
   a.pool = pool;
   a.pool_blocks = pool_blocks;
   a.bs = pool_block_size;
-  a.mode = pool ? csa2::kSelPool : csa2::kSelFull;
   a.k = k;
-  a.out = idx_out;
-  a.out_stride = k;
-  a.count_out = nullptr;
+  a.idx_out = idx_out;
+  a.out_pool_blocks = pool_out ? out_pool_blocks : 0;
+  a.pool_out = pool_out;
+  a.pool_count = pool_count;
   a.err = err_word;
-  const int64_t slots = pool ? static_cast<int64_t>(pool_blocks) * pool_block_size : score_stride;
-  csa2_status st = cuda_status(csa2::launch_select(a, slots, ws, s), "csa2_topk launch");
-  if (st != CSA2_OK || !pool_out) return st;
-  csa2::SelArgs b = a;
-  b.mode = csa2::kSelBlockMax;
-  b.k = out_pool_blocks;
-  b.out = pool_out;
-  b.out_stride = out_pool_blocks;
-  b.count_out = pool_count;
-  return cuda_status(csa2::launch_select(b, (score_stride + pool_block_size - 1) / pool_block_size, ws, s),
-                     "csa2_topk pool launch");
+  return cuda_status(csa2::launch_topk(a, ws, reinterpret_cast<cudaStream_t>(stream)), "csa2_topk launch");
 }
 
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k) {
@@ -394,8 +414,8 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
 namespace {
 struct PrefillLayout {
   int qb;  // queries per block
-  size_t off_P, off_qpos, off_ring_c, off_ring_s, off_lin_c, off_lin_s, off_scores, off_qrec, off_sel, off_attn,
-      total;
+  size_t off_P, off_qpos, off_ring_c, off_ring_s, off_lin_c, off_lin_s, off_scores, off_aux, off_qrec, off_sel,
+      off_attn, total;
 };
 
 PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dtype) {
@@ -422,10 +442,12 @@ PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dt
   o = align256(o + static_cast<size_t>(Q) * csa2::kSwaScaleStride);
   L.off_scores = o;
   o = align256(o + static_cast<size_t>(qb) * capacity * 4);
+  L.off_aux = o;
+  o = align256(o + static_cast<size_t>(qb) * csa2::aux_row_bytes(capacity));
   L.off_qrec = o;
   o = align256(o + csa2::score_tc_workspace_bytes(qb, 128));
   L.off_sel = o;
-  o = align256(o + csa2::select_workspace_bytes(qb, capacity));
+  o = align256(o + csa2::topk_workspace_bytes(qb, capacity, true));
   L.off_attn = o;
   o = align256(o + csa2::attn_workspace_bytes(qb, n_heads, k));
   L.total = o;
@@ -504,24 +526,26 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     sa.pool = nullptr;
     sa.scores = scores;
     sa.stride = cache->capacity;
+    sa.aux = wb + L.off_aux;
     sa.err = err_word;
+    e = cudaMemset2DAsync(sa.aux, csa2::aux_row_bytes(cache->capacity), 0, 2 * csa2::kSelBins * 4, nq, s);
+    if (e != cudaSuccess) return cuda_status(e, "prefill sideband clear");
     e = csa2::launch_index_score_tc(sa, wb + L.off_qrec, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill score");
-    csa2::SelArgs se{};
+    csa2::TopkArgs se{};
     se.rows = nq;
     se.scores = scores;
     se.stride = cache->capacity;
+    se.aux = wb + L.off_aux;
     se.ratio = 2;
     se.q_pos = qpos + q0;
     se.pool = nullptr;
     se.bs = 8;
-    se.mode = csa2::kSelFull;
     se.k = k;
-    se.out = idx_out + static_cast<size_t>(q0) * k;
-    se.out_stride = k;
-    se.count_out = nullptr;
+    se.idx_out = idx_out + static_cast<size_t>(q0) * k;
+    se.out_pool_blocks = 0;
     se.err = err_word;
-    e = csa2::launch_select(se, cache->capacity, wb + L.off_sel, s);
+    e = csa2::launch_topk(se, wb + L.off_sel, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
     csa2::AttnArgs aa{};
     aa.rows = nq;

@@ -12,6 +12,19 @@ cudaError_t launch_kv_append(const csa2_cache &c, const void *kv, const void *ik
                              const csa2_compress_in *cmp, const float *rope_cs, int64_t rope_len, int n_new,
                              float *cmp_dbg, int32_t *err, cudaStream_t s);
 
+// ------------------------------------------------------------------ score sideband
+// Per score row, the index-score kernel also leaves a 13-bit histogram of the
+// order-preserving score keys and (FULL rows) the maxima of 8-position blocks
+// with their histogram; the selector reads these instead of re-scanning.
+// Row layout: hist[0][kSelBins] (scores) | hist[1][kSelBins] (block maxima) |
+// bmax[ceil(stride/8)] floats, padded to 16 bytes.
+constexpr int kSelBins = 8192;
+constexpr int kSelBinShift = 19;  // key >> 19 = top 13 bits
+constexpr int kSelCap = 4096;     // candidates kept per (row, problem)
+__host__ __device__ __forceinline__ int64_t aux_row_bytes(int64_t stride) {
+  return 2 * kSelBins * 4 + ((((stride + 7) / 8) * 4 + 15) / 16) * 16;
+}
+
 // ------------------------------------------------------------------ index score
 struct ScoreArgs {
   const uint8_t *idx_codes;   // cache plane base
@@ -28,32 +41,35 @@ struct ScoreArgs {
   int pool_blocks, pool_bs;
   float *scores;              // [rows][stride]
   int64_t stride;
+  uint8_t *aux;               // [rows][aux_row_bytes(stride)] zeroed histograms, or nullptr
   int32_t *err;
 };
-cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);  // CUDA cores (dp4a)
-// tensor cores (tcgen05 kind::mxf4); needs pool == nullptr or pool_bs == 8, heads <= 128
+cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);  // CUDA cores (dp4a), no sideband
+// tensor cores (tcgen05 kind::mxf4); needs pool == nullptr or pool_bs == 8, heads <= 128; fills aux
 size_t score_tc_workspace_bytes(int rows, int heads);
 cudaError_t launch_index_score_tc(const ScoreArgs &a, void *ws, cudaStream_t s);
 
 // ------------------------------------------------------------------ top-k
-enum SelMode { kSelFull = 0, kSelPool = 1, kSelBlockMax = 2 };
-struct SelArgs {
+struct TopkArgs {
   int rows;
-  const float *scores;
+  const float *scores;        // [rows][stride]
   int64_t stride;
+  const uint8_t *aux;         // sideband from the score kernel, or nullptr (built here)
   int ratio;
-  const int64_t *q_pos;
-  const int32_t *pool;  // kSelPool
+  const int64_t *q_pos;       // [rows]
+  const int32_t *pool;        // POOL rows: [rows][pool_blocks] ascending block ids; nullptr = FULL
   int pool_blocks, bs;
-  int mode;
   int k;
-  int32_t *out;         // [rows][out_stride]
-  int out_stride;
-  int32_t *count_out;   // [rows] or nullptr
+  int32_t *idx_out;           // [rows][k]
+  int out_pool_blocks;        // FULL only: candidate-pool size (0 = no pool)
+  int32_t *pool_out;          // [rows][out_pool_blocks]
+  int32_t *pool_count;        // [rows]
   int32_t *err;
 };
-size_t select_workspace_bytes(int rows, int64_t max_slots);
-cudaError_t launch_select(const SelArgs &a, int64_t max_slots, void *ws, cudaStream_t s);
+size_t topk_workspace_bytes(int rows, int64_t stride, bool have_aux);
+// fills the sideband of `rows` score rows from the scores themselves
+cudaError_t launch_fill_aux(const TopkArgs &a, uint8_t *aux, cudaStream_t s);
+cudaError_t launch_topk(const TopkArgs &a, void *ws, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 struct AttnArgs {

@@ -22,8 +22,12 @@
 //               the per-row query operand goes to one of two B slots
 //   warp 1      MMA issuer: scale factors to TMEM (tcgen05.cp), two MMAs,
 //               commits that free the stage and hand the accumulator over
-//   warps 2..9  epilogue: warps 2-5 own accumulator 0 (even tiles), 6-9
-//               accumulator 1 (odd tiles); each warp reads its 32-lane quarter
+//   warps 2..13 epilogue: three TMEM accumulators, four warps each (one per
+//               32-lane quarter); tile j of the CTA goes to accumulator j % 3.
+//               With a sideband buffer the epilogue also histograms the score
+//               keys (and, in FULL mode, the 8-position block maxima) in shared
+//               memory and adds them to the row's global histogram once the
+//               CTA is done with the row, so top-k needs no pass of its own.
 // Every mbarrier wait is bounded; a wait that runs out raises
 // CSA2_DEVERR_TIMEOUT, sets a CTA abort flag and the CTA drains and exits.
 #include "csa2_internal.cuh"
@@ -99,7 +103,9 @@ struct __align__(1024) Smem {
   int abort;   // written only when a wait gives up
   int issued;  // items whose copies the producer started (written once, at exit)
   __align__(128) int nt[kMaxRowsPerCta];  // visible tiles of the rows this CTA touches (row - row0)
+  uint32_t hist[2][kSelBins];  // this CTA's share of the current row's sideband histograms
 };
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "score kernel shared memory above the per-CTA limit");
 
 // Bounded wait for one thread; a wait that runs out raises the timeout bit.
 __device__ __forceinline__ bool wait1(Smem &sm, uint64_t *bar, uint32_t phase, int32_t *err) {
@@ -115,6 +121,8 @@ __device__ __forceinline__ bool wait_warp(Smem &sm, uint64_t *bar, uint32_t phas
   if ((threadIdx.x & 31) == 0) ok = wait1(sm, bar, phase, err) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
+
+__device__ __forceinline__ uint32_t sel_key(float f) { return isnan(f) ? 0u : orderable(f); }
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
@@ -163,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
   const int row_last = i1 > i0 ? static_cast<int>((i1 - 1) / max_tiles) : row0;
   const int nrows = row_last - row0 + 1;
   for (int r = threadIdx.x; r < nrows && r < kMaxRowsPerCta; r += blockDim.x) sm.nt[r] = row_tiles(a, row0 + r);
+  for (int i = threadIdx.x; i < 2 * kSelBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -293,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
     const int m = 32 * quarter + lane;
     int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
     int64_t row_nslots = row_slots(a, row0);
+    const int64_t aux_row = aux_row_bytes(a.s.stride);
+    bool dead = false;
     for (int64_t it = i0; it < i1; ++it) {
       if (tile < nt) {
         if (row != prev_row) {
@@ -301,41 +312,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
           ++bchanges;
         }
         const bool last_of_row = tile + 1 >= nt || it + 1 >= i1;
-        if (j % kAcc == parity) {
-          if (!wait_warp(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err)) break;
-          if (!wait_warp(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err)) break;
-          tc::tc_fence_after();
-          const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
-          uint32_t r[np];
-#pragma unroll
-          for (int h0 = 0; h0 < np; h0 += 16) tc::tmem_ld_32x32b_x16(base + h0, r + h0);
-          tc::tmem_ld_wait();
-          tc::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
-          const float *wv = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
-          float acc = 0.0f;
-#pragma unroll
-          for (int h = 0; h < np; ++h) {
-            const float d = __uint_as_float(r[h]);
-            acc = __fmaf_rn(wv[h], d > 0.0f ? d : 0.0f, acc);
-          }
-          const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
-          bool valid;
-          if (!pool_mode) {
-            valid = slot < row_nslots;
+        if (j % kAcc == parity && !dead) {
+          if (!wait_warp(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) ||
+              !wait_warp(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err)) {
+            dead = true;  // keep walking (the named barriers below), but do no more work
           } else {
-            const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
-                                    ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
-                                    : -1;
-            const int64_t T = a.s.q_pos[row] / a.s.ratio;
-            const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
-            valid = pid >= 0 && p < T && p < a.s.cap;
-            if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
+            tc::tc_fence_after();
+            const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
+            // heads in chunks of at most 64 columns (bounded register use), the
+            // fma chain still runs over the heads in order
+            constexpr int kCh = np < 64 ? np : 64;
+            const float *wv = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
+            float acc = 0.0f;
+#pragma unroll
+            for (int c0 = 0; c0 < np; c0 += kCh) {
+              uint32_t r[kCh];
+#pragma unroll
+              for (int h0 = 0; h0 < kCh; h0 += 16) tc::tmem_ld_32x32b_x16(base + c0 + h0, r + h0);
+              tc::tmem_ld_wait();
+              if (c0 + kCh >= np) {
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
+              }
+#pragma unroll
+              for (int h = 0; h < kCh; ++h) {
+                const float d = __uint_as_float(r[h]);
+                acc = __fmaf_rn(wv[c0 + h], d > 0.0f ? d : 0.0f, acc);
+              }
+            }
+            const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
+            bool valid;
+            if (!pool_mode) {
+              valid = slot < row_nslots;
+            } else {
+              const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
+                                      ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
+                                      : -1;
+              const int64_t T = a.s.q_pos[row] / a.s.ratio;
+              const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
+              valid = pid >= 0 && p < T && p < a.s.cap;
+              if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
+            }
+            if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
+            if (a.s.aux) {
+              // sideband: score-key histogram; FULL rows also the max of each
+              // 8-position block (8 consecutive lanes) and its histogram
+              if (valid) atomicAdd(&sm.hist[0][sel_key(acc) >> kSelBinShift], 1u);
+              if (!pool_mode) {
+                float v = valid ? acc : -INFINITY;
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+                if ((lane & 7) == 0 && valid) {
+                  float *bm = reinterpret_cast<float *>(a.s.aux + static_cast<size_t>(row) * aux_row + 2 * kSelBins * 4);
+                  bm[slot / 8] = v;
+                  atomicAdd(&sm.hist[1][sel_key(v) >> kSelBinShift], 1u);
+                }
+              }
+            }
           }
-          if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
         }
         if (last_of_row && lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
+        if (last_of_row && a.s.aux) {
+          // every epilogue warp is done with this row: add the CTA's histograms
+          // to the row's sideband and clear them
+          asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+          uint32_t *gh = reinterpret_cast<uint32_t *>(a.s.aux + static_cast<size_t>(row) * aux_row);
+          for (int i = threadIdx.x - 64; i < 2 * kSelBins; i += kEpiWarps * 32) {
+            const uint32_t c = (&sm.hist[0][0])[i];
+            if (c) {
+              atomicAdd(&gh[i], c);
+              (&sm.hist[0][0])[i] = 0;
+            }
+          }
+          asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+        }
         ++j;
       }
       if (++tile == max_tiles) {

@@ -5,15 +5,17 @@
 // hands plugins only the tensors it created, a real-time service whose memory
 // budget is fixed at start-up, or code that must not trigger the allocator's
 // implicit device synchronisation.  csa2_topk needs a caller workspace for its
-// radix histograms and per-CTA counts; this variant keeps that scratch in a
-// fixed array compiled into the library instead, so the caller passes only its
-// inputs and outputs.
+// score histograms, selection state and candidate lists; this variant keeps
+// that scratch in a fixed array compiled into the library instead, so the
+// caller passes only its inputs and outputs (and no score sideband: it is
+// always rebuilt from the scores, inside the array).
 //
 // The array (kNoAllocScratchBytes, 4 MiB) lives in every GPU that loads the
 // library until the process exits.  All calls share it: two calls whose kernels
 // overlap on the GPU (different streams, no ordering between them) race on it.
-// The histograms are cleared at the start of every call; nothing else in the
-// array needs a known value.
+// The histograms are cleared at the start of every call and the selection
+// state is written before it is read; nothing in the array needs a known value
+// on entry.
 #include <cstdio>
 #include <mutex>
 
@@ -71,10 +73,11 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stri
   if (pool_out) {
     if (!pool_count) return CSA2_ERR_NULL;
     if (!aligned16(pool_out) || !aligned16(pool_count)) return CSA2_ERR_ALIGN;
-    if (out_pool_blocks < 1 || out_pool_blocks > 65536) return CSA2_ERR_RANGE;
+    if (out_pool_blocks < 1 || out_pool_blocks > CSA2_MAX_TOPK) return CSA2_ERR_RANGE;
+    if (pool_block_size != 8) return CSA2_ERR_UNSUPPORTED;
   }
   // the same scratch layout csa2_topk uses for its caller workspace
-  const size_t need = csa2::select_workspace_bytes(batch, score_stride);
+  const size_t need = csa2::topk_workspace_bytes(batch, score_stride, false);
   if (need > kNoAllocScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
@@ -91,31 +94,22 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stri
     return CSA2_ERR_CUDA;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  csa2::SelArgs a{};
+  csa2::TopkArgs a{};
   a.rows = batch;
   a.scores = scores;
   a.stride = score_stride;
+  a.aux = nullptr;
   a.ratio = ratio;
   a.q_pos = q_pos;
   a.pool = pool;
   a.pool_blocks = pool_blocks;
   a.bs = pool_block_size;
-  a.mode = pool ? csa2::kSelPool : csa2::kSelFull;
   a.k = k;
-  a.out = idx_out;
-  a.out_stride = k;
-  a.count_out = nullptr;
+  a.idx_out = idx_out;
+  a.out_pool_blocks = pool_out ? out_pool_blocks : 0;
+  a.pool_out = pool_out;
+  a.pool_count = pool_count;
   a.err = err_word;
-  const int64_t slots = pool ? static_cast<int64_t>(pool_blocks) * pool_block_size : score_stride;
-  if (csa2::launch_select(a, slots, ws, s) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (!pool_out) return CSA2_OK;
-  csa2::SelArgs b = a;
-  b.mode = csa2::kSelBlockMax;
-  b.k = out_pool_blocks;
-  b.out = pool_out;
-  b.out_stride = out_pool_blocks;
-  b.count_out = pool_count;
-  if (csa2::launch_select(b, (score_stride + pool_block_size - 1) / pool_block_size, ws, s) != cudaSuccess)
-    return CSA2_ERR_CUDA;
+  if (csa2::launch_topk(a, ws, s) != cudaSuccess) return CSA2_ERR_CUDA;
   return CSA2_OK;
 }

@@ -181,39 +181,75 @@ csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *
  *   score of position pool[b][j]*pool_block_size + i when it is visible.
  * score_stride: floats per sequence in scores (>= capacity for FULL,
  *   >= pool_blocks*pool_block_size for POOL).  n_heads_idx in 1..128.
+ * score_aux: NULL, or a device buffer of csa2_score_aux_size(batch,
+ *   score_stride) bytes that receives a sideband for csa2_topk: per row a
+ *   histogram of the scores' top 13 order bits and, in FULL mode, the max of
+ *   every 8-position block with its histogram.  Owned by the caller; valid
+ *   until the scores change.  Building it here costs no extra pass over them.
  * ws: device workspace of csa2_index_score_workspace_size() bytes (the
  *   quantised queries in the tensor-core operand layout).
  * The contraction runs on the tensor cores (block-scaled MXFP4 MMA) for FULL
- * and for POOL with pool_block_size 8; other block sizes use CUDA cores.
+ * and for POOL with pool_block_size 8; other block sizes use CUDA cores (the
+ * sideband is then built by a second kernel over the scores).
  */
 size_t csa2_index_score_workspace_size(int32_t batch, int32_t n_heads_idx);
+size_t csa2_score_aux_size(int32_t batch, int64_t score_stride);
 csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
                              int32_t n_heads_idx, const int64_t *q_pos, const int32_t *pool,
                              int32_t pool_blocks, int32_t pool_block_size, float *scores,
-                             int64_t score_stride, void *ws, size_t ws_bytes, int32_t *err_word,
-                             csa2_stream_t stream);
+                             int64_t score_stride, void *score_aux, void *ws, size_t ws_bytes,
+                             int32_t *err_word, csa2_stream_t stream);
 
 /*
  * csa2_topk: top-k selector ([P5] §2.3.1 "Top-k(I_{t,:})") over the candidates
  * csa2_index_score scored (same ratio / q_pos / pool arguments), ordered by
  * score descending then position ascending (ties go to the lower position;
- * -0 == +0).  idx_out [batch][k] receives the chosen positions in ascending
- * order, padded with -1.  k in 1..2048.
+ * -0 == +0; NaN ranks lowest and raises the NAN bit).  idx_out [batch][k]
+ * receives the chosen positions in ascending order, padded with -1.
+ * k in 1..2048.
+ * score_aux: the sideband csa2_index_score wrote for these scores, or NULL
+ *   (it is then rebuilt from the scores inside ws, one more pass over them).
  * FULL mode only: when pool_out != NULL also builds the candidate pool of the
- * Hierarchical Sparse Indexer ([P1], [P4]): positions are grouped in
- * pool_block_size-aligned blocks, a block's score is the max over its visible
- * positions, and the top out_pool_blocks blocks by (max desc, block asc) are
- * written ascending to pool_out [batch][out_pool_blocks] (padded with -1),
- * with their number in pool_count [batch].
- * ws: device workspace of csa2_topk_workspace_size() bytes.
+ * Hierarchical Sparse Indexer ([P1], [P4]): positions are grouped in aligned
+ * blocks of pool_block_size = 8, a block's score is the max over its visible
+ * positions, and the top out_pool_blocks (1..2048) blocks by (max desc, block
+ * asc) are written ascending to pool_out [batch][out_pool_blocks] (padded with
+ * -1), with their number in pool_count [batch].
+ * ws: device workspace of csa2_topk_workspace_size() bytes (enough with or
+ *   without score_aux).
+ * The selection is exact for any input; rows whose k-th score falls in a bin
+ * holding more than 4096 scores take a slower exact path.
  */
 size_t csa2_topk_workspace_size(int32_t batch, int64_t score_stride, int32_t k,
                                 int32_t out_pool_blocks);
-csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
-                      const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
-                      int32_t pool_block_size, int32_t k, int32_t *idx_out,
+csa2_status csa2_topk(const float *scores, int64_t score_stride, const void *score_aux,
+                      int32_t batch, int32_t ratio, const int64_t *q_pos, const int32_t *pool,
+                      int32_t pool_blocks, int32_t pool_block_size, int32_t k, int32_t *idx_out,
                       int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count, void *ws,
                       size_t ws_bytes, int32_t *err_word, csa2_stream_t stream);
+
+/*
+ * csa2_topk_noalloc: csa2_topk without a caller workspace, for callers that
+ * may not allocate device memory while they run (a host framework that owns all
+ * device allocations, a service whose memory budget is fixed at start-up, code
+ * that must not hit the allocator's implicit synchronisation).  The source pages
+ * have no counterpart: this is a library convenience, not a step of the method.
+ * Same arguments and results as csa2_topk minus score_aux, ws and ws_bytes (the
+ * sideband is always rebuilt from the scores).  Its scratch is a 4 MiB array
+ * compiled into the library, resident on every GPU that loads it until the
+ * process exits; calls needing more (csa2_topk_workspace_size() > 4 MiB, i.e.
+ * large batch x score_stride) return CSA2_ERR_WORKSPACE with the sizes in
+ * csa2_last_error_detail().  The first call on each device looks up the
+ * array's device address (a runtime query), so make that first call before any
+ * stream capture.  Every call shares the array and leaves its contents behind
+ * (each call clears and rewrites what it reads): calls whose kernels may
+ * overlap on the GPU -- different streams without ordering -- race.
+ */
+csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
+                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
+                              int32_t pool_block_size, int32_t k, int32_t *idx_out,
+                              int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count,
+                              int32_t *err_word, csa2_stream_t stream);
 
 /*
  * csa2_sparse_attn_decode: core attention of one decode step over the k
@@ -232,28 +268,6 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, int32_t batch, 
  * ws: device workspace of csa2_attn_workspace_size() bytes (split partials).
  * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
  */
-/*
- * csa2_topk_noalloc: csa2_topk without a caller workspace, for callers that
- * may not allocate device memory while they run (a host framework that owns all
- * device allocations, a service whose memory budget is fixed at start-up, code
- * that must not hit the allocator's implicit synchronisation).  The source pages
- * have no counterpart: this is a library convenience, not a step of the method.
- * Same arguments and results as csa2_topk minus ws / ws_bytes.  Its scratch is
- * a 4 MiB array compiled into the library, resident on every GPU that loads it
- * until the process exits; calls needing more (csa2_topk_workspace_size() >
- * 4 MiB, i.e. large batch x score_stride) return CSA2_ERR_WORKSPACE with the
- * sizes in csa2_last_error_detail().  The first call on each device looks up the
- * array's device address (a runtime query), so make that first call before any
- * stream capture.  Every call shares the array and leaves its contents behind
- * (the histograms are cleared at the start of each call): calls whose kernels
- * may overlap on the GPU -- different streams without ordering -- race.
- */
-csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
-                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
-                              int32_t pool_block_size, int32_t k, int32_t *idx_out,
-                              int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count,
-                              int32_t *err_word, csa2_stream_t stream);
-
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k);
 csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t n_heads,
                                     const int64_t *q_pos, const int32_t *idx, int32_t k,

@@ -50,7 +50,7 @@ def test_host_validation_codes(lib):
     st = csa2.CacheStruct(1, 16, 3, 1, *([fake] * 10))
     assert lib.csa2_kv_append(ctypes.byref(st), None, None, 0, None, None, 1, 1, None, None, None) == 4
     st = csa2.CacheStruct(0, 16, 1, 1, *([fake] * 10))
-    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None, 0,
+    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None, None, 0,
                                 None, None) == 2
     st = csa2.CacheStruct(1, 16, 1, 1, *([fake] * 10))
     st.lat_codes = fake + 8  # misaligned
@@ -62,9 +62,15 @@ def test_host_validation_codes(lib):
     assert lib.csa2_sparse_attn_decode(ctypes.byref(st), p, 24, p, p, 512, None, 0.1, p, p, p, 1 << 20,
                                        None, None) == 2
     # k out of range
-    assert lib.csa2_topk(p, 100, 1, 1, p, None, 0, 8, 0, p, 0, None, None, p, 1 << 20, None, None) == 4
+    assert lib.csa2_topk(p, 100, None, 1, 1, p, None, 0, 8, 0, p, 0, None, None, p, 1 << 20, None, None) == 4
     # workspace too small
-    assert lib.csa2_topk(p, 100, 1, 1, p, None, 0, 8, 8, p, 0, None, None, p, 16, None, None) == 7
+    assert lib.csa2_topk(p, 100, None, 1, 1, p, None, 0, 8, 8, p, 0, None, None, p, 16, None, None) == 7
+    # the candidate pool: at most 2048 blocks, built from 8-position blocks
+    assert lib.csa2_topk(p, 100, None, 1, 1, p, None, 0, 8, 8, p, 4096, p, p, p, 1 << 20, None, None) == 4
+    assert lib.csa2_topk(p, 100, None, 1, 1, p, None, 0, 16, 8, p, 64, p, p, p, 1 << 20, None, None) == 5
+    # a misaligned sideband
+    assert lib.csa2_topk(p, 100, ctypes.c_void_p(fake + 4), 1, 1, p, None, 0, 8, 8, p, 0, None, None, p,
+                         1 << 20, None, None) == 3
     # prefill needs a ratio-2 cache
     assert lib.csa2_prefill_chunk(ctypes.byref(st), 0, None, p, 10, 4, p, p, 4, p, 16, 8, None, 0.1,
                                   p, p, p, p, 1 << 30, None, None) == 5

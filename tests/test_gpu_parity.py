@@ -87,8 +87,15 @@ def test_index_score_full_and_topk_bitexact(orc, H_I):
     pcount = torch.empty((B,), dtype=torch.int32, device="cuda")
     ws = csa2.topk_workspace(B, c.capacity, k, 32)
     csa2.topk(scores, 1, q_pos, k, idx, ws, pool_out=pool, pool_count=pcount, err=err)
+    # the same selection from the sideband the score kernel leaves
+    aux = csa2.score_aux(B, c.capacity)
+    scores2 = torch.full_like(scores, float("nan"))
+    csa2.index_score(c, q_idx.cuda(), w.cuda(), q_pos, scores2, err=err, aux=aux)
+    idx2, pool2, pcount2 = torch.empty_like(idx), torch.empty_like(pool), torch.empty_like(pcount)
+    csa2.topk(scores2, 1, q_pos, k, idx2, ws, pool_out=pool2, pool_count=pcount2, err=err, aux=aux)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    assert torch.equal(idx, idx2) and torch.equal(pool, pool2) and torch.equal(pcount, pcount2)
     Tv = T - 1
     for b in range(B):
         ref, flags = orc.index_scores(oc[b], u16(q_idx[b]), w[b].numpy(), n_vis=Tv)
@@ -166,8 +173,14 @@ def test_reindex_pool_bitexact(orc):
     idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
     ws = csa2.topk_workspace(B, stride, k)
     csa2.topk(scores, 1, q_pos, k, idx, ws, pool=pool.cuda(), err=err)
+    aux = csa2.score_aux(B, stride)
+    scores2 = torch.empty_like(scores)
+    csa2.index_score(c, q_idx.cuda(), w.cuda(), q_pos, scores2, pool=pool.cuda(), err=err, aux=aux)
+    idx2 = torch.empty_like(idx)
+    csa2.topk(scores2, 1, q_pos, k, idx2, ws, pool=pool.cuda(), err=err, aux=aux)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    assert torch.equal(idx, idx2)
     for b in range(B):
         pl = pool[b].numpy()
         cnt = int((pl >= 0).sum())
@@ -179,6 +192,55 @@ def test_reindex_pool_bitexact(orc):
         got = scores[b].cpu().numpy()[slots]
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
         assert idx[b].tolist() == orc.topk(ref, k, positions=pos).tolist()
+
+
+@pytest.mark.parametrize("levels,T,k,nblk", [
+    (4, 30000, 512, 2048),     # four distinct values: the threshold bin holds ~7,500 scores
+    (1, 9000, 100, 64),        # one value: every score ties, lowest positions win
+    (0, 70000, 2048, 2048),    # continuous scores, k and pool at their maxima
+    (3, 4000, 2048, 2048),     # fewer visible entries than k: everything is chosen
+])
+def test_topk_crowded_bins_against_oracle(orc, levels, T, k, nblk):
+    """Scores written directly (not from the indexer): heavy ties and crowded
+    histogram bins, both signs and -0/+0, FULL rows with the pool build."""
+    B = 2
+    g = torch.Generator().manual_seed(1000 + levels)
+    stride = T + 40
+    if levels:
+        vals = torch.tensor([-0.0, 0.0, 1.5, -2.25, 1.5 + 2 ** -20][:levels + 1])
+        sc = vals[torch.randint(0, len(vals), (B, stride), generator=g)]
+    else:
+        sc = torch.randn((B, stride), generator=g) * 3
+    sc = sc.float().contiguous()
+    q_pos = torch.tensor([T, T // 2 + 3], dtype=torch.int64)
+    if T == 4000:
+        q_pos = torch.tensor([1500, 7], dtype=torch.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    pool = torch.empty((B, nblk), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = csa2.topk_workspace(B, stride, k, nblk)
+    csa2.topk(sc.cuda(), 1, q_pos.cuda(), k, idx, ws, pool_out=pool, pool_count=cnt, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for b in range(B):
+        Tv = int(q_pos[b])
+        row = sc[b, :Tv].numpy()
+        assert idx[b].tolist() == orc.topk(row, k).tolist()
+        pids, n = orc.pool(row, Tv, 8, nblk)
+        assert cnt[b].item() == n and pool[b].tolist() == pids.tolist()
+
+
+def test_topk_nan_score_is_reported(orc):
+    sc = torch.randn((1, 5000))
+    sc[0, 123] = float("nan")
+    q_pos = torch.tensor([5000], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((1, 64), dtype=torch.int32, device="cuda")
+    csa2.topk(sc.cuda(), 1, q_pos, 64, idx, csa2.topk_workspace(1, 5000, 64), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & csa2.DEVERR_NAN
+    assert 123 not in idx[0].tolist()
 
 
 # ------------------------------------------------------------------ attention
