@@ -24,6 +24,7 @@ import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -56,29 +57,93 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clock, power and clock-event reasons sampled through NVML (the driver's
+    libnvidia-ml, read-only queries) by a thread polling every ~2 ms, so that
+    samples fall inside even a short timed region; mark() brackets that region.
+    Falls back to `nvidia-smi -lms 100` when NVML cannot be loaded."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReason bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+            "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
+    def __init__(self, device):
+        self.device = device
+        self.samples = []
+        self.region = None
         self.proc = None
-        self.path = None
+        self.thread = None
+        self.stop_flag = False
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(self.device).uuid)
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle for " + uuid)
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        return lib, h, reasons_fn, float(mx.value)
+
+    def _poll(self, lib, h, reasons_fn):
+        import ctypes
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag:
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    reasons_fn(h, ctypes.byref(rs)) == 0:
+                lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                self.samples.append((time.perf_counter(), float(clk.value), int(rs.value), pw.value / 1e3))
+            time.sleep(0.002)
 
     def start(self):
+        try:
+            lib, h, reasons_fn, self.smax = self._nvml()
+            self.thread = threading.Thread(target=self._poll, args=(lib, h, reasons_fn), daemon=True)
+            self.thread.start()
+            self.source = "nvml"
+        except Exception:
+            self._start_smi()
+        self.old_switch = sys.getswitchinterval()
+        sys.setswitchinterval(0.0005)  # let the poller run between the replay calls
+        time.sleep(0.05)
+
+    def _start_smi(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.device}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except Exception:
             self.proc = None
+            self.source = None
+
+    def mark(self, t0, t1):
+        self.region = (t0, t1)
 
     def stop(self):
+        sys.setswitchinterval(self.old_switch)
+        if self.thread is not None:
+            time.sleep(0.01)
+            self.stop_flag = True
+            self.thread.join(timeout=2)
+            t0, t1 = self.region
+            inside = [x for x in self.samples if t0 <= x[0] <= t1]
+            if not inside:
+                return None
+            reasons = sorted(n for n, bit in self.BITS.items() if any(x[2] & bit for x in inside))
+            return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.smax,
+                    "reasons": reasons, "samples": len(inside), "source": "nvml, during the timed region",
+                    "power_w_max": max(x[3] for x in inside)}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -106,7 +171,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, around the timed region"}
 
 
 # ----------------------------------------------------------------------------- workload
@@ -190,10 +255,10 @@ class FullDecode:
 
     @staticmethod
     def kernel_launches(n_splits_gt1=False):
-        # kv_append ratio 1: append + advance; index_score: q prep + score (the sideband clear is a
-        # memset); topk from the sideband: resolve, collect, final (top-k and pool in the same
-        # launches); attention: 1 (+ combine when split)
-        return 2 + 2 + 3 + 1 + (1 if n_splits_gt1 else 0)
+        # kv_append ratio 1, one token: 1 (it also advances n_tokens); index_score: q prep + score
+        # (the sideband clear is a memset); topk from the sideband: resolve, collect, final (top-k
+        # and pool in the same launches); attention: 1 (+ combine when split)
+        return 1 + 2 + 3 + 1 + (1 if n_splits_gt1 else 0)
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -243,6 +308,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_begin = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()  # L2 flushed between timed steps (outside the events)
         if graphs is not None:
@@ -253,6 +319,7 @@ def run_ours(args):
         else:
             bench.step(args.warmup + i, evs[i])
     torch.cuda.synchronize()
+    sampler.mark(t_begin, time.perf_counter())
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -407,7 +474,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full_decode", choices=["full_decode", "tiny_decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

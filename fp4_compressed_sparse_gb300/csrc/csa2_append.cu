@@ -8,9 +8,10 @@
 //      §2.3.1 (overlapping compression, m = 2) and §3.5.1 (compression buffer,
 //      fixed-size window state).
 //
-// One warp encodes one entry (or one window token): lane l quantises latent
-// group l (16 values), lanes 0..3 the four RoPE groups, lanes 4..7 the four
-// MXFP4 indexer blocks.  Stores are contiguous per warp (256 B codes, 32 B scales).
+// Ratio 1: one 256-thread block encodes one token (entry and window slot), each
+// thread a few values.  Ratio 2: one warp encodes one compressed entry (or one
+// window token): lane l quantises latent group l (16 values), lanes 0..3 the
+// four RoPE groups, lanes 4..7 the four MXFP4 indexer blocks.
 #include "csa2_encode.cuh"
 #include "csa2_internal.cuh"
 
@@ -40,32 +41,36 @@ __device__ __forceinline__ void append_fail(const csa2_cache &c, int64_t t0, int
 
 namespace {
 
-// Ratio 1: token t is entry t.  grid (ceil(n_new/8), batch), 256 threads.
-__global__ void __launch_bounds__(256) k_append_r1(csa2_cache c, const void *kv, const void *ik, int in_bf16,
-                                                   const float *rope_cs, int64_t rope_len, int n_new,
-                                                   int32_t *err) {
-  __shared__ float srow[kWarps][kDcmp];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
-  const int j = blockIdx.x * kWarps + warp;
+// Ratio 1: token t is entry t.  grid (n_new, batch), one 256-thread block per
+// token.  `advance`: this launch is the only one of the append (one token per
+// sequence), so the block also moves n_tokens on once it is done.
+__global__ void __launch_bounds__(kEncThreads) k_append_r1(csa2_cache c, const void *kv, const void *ik, int in_bf16,
+                                                           const float *rope_cs, int64_t rope_len, int n_new,
+                                                           int advance, int32_t *err) {
+  __shared__ __align__(16) float row[kDcmp];
+  __shared__ __align__(16) float rot[kRope];
+  const int b = blockIdx.y, j = blockIdx.x;
   const int64_t t0 = c.n_tokens[b];
   if (!append_ok(c, t0, n_new, rope_len)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) append_fail(c, t0, n_new, rope_len, err);
+    if (j == 0 && threadIdx.x == 0) append_fail(c, t0, n_new, rope_len, err);
     return;
   }
-  if (j >= n_new) return;
   const int64_t t = t0 + j;
   const size_t base = static_cast<size_t>(b) * n_new + j;
-  for (int i = lane; i < kDqk; i += 32) srow[warp][i] = load_in(kv, base * kDqk + i, in_bf16);
-  for (int i = lane; i < kDi; i += 32) srow[warp][kDqk + i] = load_in(ik, base * kDi + i, in_bf16);
-  __syncwarp();
-  const float *cs = rope_cs + t * 64;
-  warp_encode_entry(c, b, t, srow[warp], cs, lane);
+  for (int i = threadIdx.x; i < kDqk; i += blockDim.x) row[i] = load_in(kv, base * kDqk + i, in_bf16);
+  for (int i = threadIdx.x; i < kDi; i += blockDim.x) row[kDqk + i] = load_in(ik, base * kDi + i, in_bf16);
+  __syncthreads();
+  block_rope(row, rope_cs + t * 64, rot);
+  __syncthreads();
+  block_encode_entry(c, b, t, row, rot);
   if (j >= n_new - kWin) {
     const size_t slot = static_cast<size_t>(b) * kWin + (t % kWin);
-    warp_encode_swa(c.swa_codes + slot * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152),
-                    c.swa_scales ? c.swa_scales + slot * kSwaScaleStride : nullptr, c.swa_dtype, srow[warp],
-                    cs, lane);
+    block_encode_swa(c.swa_codes + slot * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152),
+                     c.swa_scales ? c.swa_scales + slot * kSwaScaleStride : nullptr, c.swa_dtype, row, rot);
+  }
+  if (advance) {
+    __syncthreads();  // every thread has read n_tokens
+    if (threadIdx.x == 0) c.n_tokens[b] = t0 + n_new;
   }
 }
 
@@ -176,8 +181,10 @@ cudaError_t launch_kv_append(const csa2_cache &c, const void *kv, const void *ik
                              float *cmp_dbg, int32_t *err, cudaStream_t s) {
   if (n_new <= 0) return cudaSuccess;
   if (c.ratio == 1) {
-    dim3 grid((n_new + kWarps - 1) / kWarps, c.batch);
-    k_append_r1<<<grid, 256, 0, s>>>(c, kv, ik, in_dtype == CSA2_IN_BF16, rope_cs, rope_len, n_new, err);
+    const int advance = n_new == 1 ? 1 : 0;
+    k_append_r1<<<dim3(n_new, c.batch), kEncThreads, 0, s>>>(c, kv, ik, in_dtype == CSA2_IN_BF16, rope_cs, rope_len,
+                                                             n_new, advance, err);
+    if (advance) return cudaGetLastError();
   } else {
     const int max_emit = n_new / 2 + 1;
     dim3 g1((max_emit + kWarps - 1) / kWarps, c.batch);

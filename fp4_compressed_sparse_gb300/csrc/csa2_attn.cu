@@ -3,164 +3,141 @@
 //
 // [P5] "DeepSeek-V4: Towards Highly Efficient Million-Token Context
 // Intelligence" §2.3.1 "Shared Key-Value MQA" (each selected entry is key and
-// value), §2.3.3 (window branch; sink exp(z'_h) in the denominator);
-// [P2] "DeepSeek Multi-Head Latent Attention(MLA) 해부" §4 (absorbed query: the
-// logit is q_lat . c + q_rope . k_rope, the value is the 512-dim latent c).
+// value, shared by all heads), §2.3.3 (window branch; sink exp(z'_h) in the
+// denominator); [P2] "DeepSeek Multi-Head Latent Attention(MLA) 해부" §4
+// (absorbed query: the logit is q_lat . c + q_rope . k_rope, the value is the
+// 512-dim latent c).
 //
-// One CTA = (16 heads, one split of the entry list, one row).  Entries are
-// gathered 32 at a time and dequantised exactly into shared memory (bf16 for
-// the 576-dim keys, fp16 for the 512-dim values: an E2M1 code times an E4M3 or
-// E8M0 scale has at most 6 significant bits), then
-//   S = Q K^T   (mma.sync m16n8k16 bf16, fp32 accumulate; warp w owns 8 entries)
-//   online softmax in the log2 domain (fp32)
-//   O += P V    (mma.sync m16n8k16 fp16, fp32 accumulate; warp w owns 128 dims)
-// Splits write unnormalised partials (O, m, l) and a combine kernel merges them
-// (flash-decoding LSE merge) and applies the sink.
+// One CTA = (one split of a row's entry list, up to 64 heads).  Every head
+// shares the entries, so each entry is dequantised once per CTA:
+//   producer warps (4)  gather 32 entries at a time and dequantise them into a
+//                       two-stage fp16 ring: E2M1 x E4M3 through a byte -> half2
+//                       table (exact: at most 6 significant bits, >= 2^-10);
+//                       window MXFP8 / bf16 entries, scaled by a power of two
+//                       2^-sigma_j only if they would not fit fp16
+//   consumer warps      S = Q K^T (mma.sync m16n8k16 f16, fp32 accumulate),
+//   (heads / 8)         online softmax in the log2 domain, O += P V with the
+//                       fp32 O tile in registers
+// The query is held as fp16 with a power-of-two scale per head (exact for bf16
+// values within 2^24 of the head's maximum).  Stage handover uses mbarriers
+// with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  Splits write
+// unnormalised partials (O, m, l) that a combine kernel merges (flash-decoding
+// LSE merge) and finishes with the sink.
+#include <cuda_fp16.h>
+
 #include "csa2_internal.cuh"
+#include "csa2_tc.cuh"
 
 namespace csa2 {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kEnt = 32;         // entries per chunk
-constexpr int kQS = kDqk + 8;    // bf16 row stride (odd multiple of 16 B: conflict-free ldmatrix)
-constexpr int kVS = kLat + 8;    // fp16 row stride
+constexpr int kE = 32;            // entries per chunk
+constexpr int kQS = kDqk + 8;     // fp16 row stride of Q and of the entry tiles (1168 B: conflict-free ldmatrix)
+constexpr int kPS = kE + 8;       // fp16 row stride of P (80 B)
+constexpr int kSS = kE + 4;       // fp32 row stride of the logits
+constexpr int kProdThreads = 128; // four producer warps
+constexpr int kHeadBlock = 64;    // heads per CTA at most
+constexpr uint32_t kWaitIters = 200;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-struct Smem {
-  __nv_bfloat16 q[16][kQS];
-  __nv_bfloat16 k[kEnt][kQS];
-  __half v[kEnt][kVS];
-  float s[16][kEnt + 1];
-  int64_t src[kEnt];
-  int kind[kEnt];  // 0 empty, 1 cache entry, 2 window ring slot, 3 window linear row
+template <int HP>
+struct __align__(16) AttnSmem {
+  __half q[HP][kQS];
+  __half kv[2][kE][kQS];
+  float s[HP][kSS];
+  __half p[HP][kPS];
+  float qf[HP];        // logit factor of head h: 2^e_h * sm_scale * log2(e)
+  float alpha[HP];     // this chunk's rescale of O
+  float fin[HP][2];    // m, l per head after the last chunk
+  float sig[2][kE];    // 2^sigma_j of entry j of a stage; 0 = empty entry
+  uint32_t lut[256];   // byte of two E2M1 codes -> half2 (low nibble in the low half)
+  __align__(8) uint64_t full[2];
+  __align__(8) uint64_t empty[2];
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ void mma_bf16(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                        uint32_t b1) {
+__device__ __forceinline__ void mma_f16(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
+__device__ __forceinline__ uint32_t hmul2u(uint32_t x, uint32_t y) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&x), *reinterpret_cast<__half2 *>(&y));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+// two E4M3 codes (low byte -> low half) to fp16, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(static_cast<uint16_t>(two_bytes)));
+  return r;
+}
+__device__ __forceinline__ uint32_t h2_splat(float v) {
+  __half2 h = __float2half2_rn(v);
   return *reinterpret_cast<uint32_t *>(&h);
 }
+__device__ __forceinline__ void bar_consumers(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
 
-__device__ __forceinline__ void put(Smem &sm, int e, int d, float v) {
-  sm.k[e][d] = __float2bfloat16_rn(v);
-  if (d < kLat) sm.v[e][d] = __float2half_rn(v);
-}
-
-// Dequantise entry e (kind/src resolved) into sm.k / sm.v; `part` in 0..3.
-__device__ __forceinline__ void load_entry(const AttnArgs &a, Smem &sm, int e, int part) {
-  const int kind = sm.kind[e];
-  const int64_t src = sm.src[e];
-  if (kind == 1) {
-    const uint4 *cp = reinterpret_cast<const uint4 *>(a.lat_codes + src * 256 + part * 64);
-    const uint2 sc8 = *reinterpret_cast<const uint2 *>(a.lat_scales + src * 32 + part * 8);
-    const uint32_t scw[2] = {sc8.x, sc8.y};
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 u = cp[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // word q of uint4 v holds dims part*128 + 32v + 8q .. +7 (group 2v + q/2)
-        const int g = 2 * v + (q >> 1);
-        const float s = e4m3_value((scw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
-        const int d0 = part * 128 + 32 * v + 8 * q;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) put(sm, e, d0 + i, e2m1_value((w[q] >> (4 * i)) & 15u) * s);
-      }
-    }
-    const uint2 rc = *reinterpret_cast<const uint2 *>(a.rope_codes + src * 32 + part * 8);
-    const float rs = e4m3_value(a.rope_scales[src * 4 + part]);
-    const uint32_t rw[2] = {rc.x, rc.y};
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) put(sm, e, kLat + 16 * part + 8 * q + i, e2m1_value((rw[q] >> (4 * i)) & 15u) * rs);
-  } else if (kind == 2 || kind == 3) {
-    const uint8_t *codes;
-    const uint8_t *scales;
-    if (kind == 2) {
-      codes = a.ring_codes + src * (a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
-      scales = a.ring_scales ? a.ring_scales + src * kSwaScaleStride : nullptr;
-    } else {
-      codes = a.lin_codes + src * (a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
-      scales = a.lin_scales ? a.lin_scales + src * kSwaScaleStride : nullptr;
-    }
-    const int d0 = part * 144;
-    if (a.swa_dtype == CSA2_SWA_MXFP8) {
-      const uint4 *cp = reinterpret_cast<const uint4 *>(codes + d0);
-#pragma unroll
-      for (int v = 0; v < 9; ++v) {
-        const uint4 u = cp[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int d = d0 + 16 * v + 4 * q + i;
-            put(sm, e, d, e4m3_value((w[q] >> (8 * i)) & 0xFFu) * e8m0_value(scales[d >> 5]));
-          }
-      }
-    } else {
-      const uint4 *cp = reinterpret_cast<const uint4 *>(codes + 2 * d0);
-#pragma unroll
-      for (int v = 0; v < 18; ++v) {
-        const uint4 u = cp[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int d = d0 + 8 * v + 2 * q;
-          put(sm, e, d, __uint_as_float(w[q] << 16));
-          put(sm, e, d + 1, __uint_as_float(w[q] & 0xFFFF0000u));
-        }
-      }
-    }
-  } else {
-    for (int d = part * 144; d < part * 144 + 144; ++d) put(sm, e, d, 0.0f);
+// Warp-uniform bounded wait on an mbarrier phase.
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, int32_t *err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = tc::mbar_wait_bounded(bar, parity, kWaitIters) ? 1 : 0;
+    if (!ok) raise_err(err, CSA2_DEVERR_TIMEOUT);
   }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__global__ void __launch_bounds__(kThreads) k_attn(AttnArgs a, int n_splits, int per_split) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+// Entry j of the row's list: the k selected cache entries, then the window.
+// kind 0 empty, 1 cache entry, 2 window ring slot, 3 window row of the call.
+__device__ __forceinline__ int entry_src(const AttnArgs &a, int row, int seq, int j, int64_t qpos, int64_t T,
+                                         int64_t ntok, int64_t lin_base, int64_t &src) {
+  src = 0;
+  if (j < a.k) {
+    const int32_t s = a.idx[static_cast<size_t>(row) * a.k + j];
+    if (s < 0) return 0;
+    if (s >= T || s >= a.cap) {
+      raise_err(a.err, CSA2_DEVERR_INDEX);
+      return 0;
+    }
+    src = static_cast<int64_t>(seq) * a.cap + s;
+    return 1;
+  }
+  const int64_t tok = qpos - (kWin - 1) + (j - a.k);
+  if (tok < 0 || tok >= ntok || tok > qpos) return 0;
+  if (tok >= lin_base) {
+    src = tok - lin_base;
+    return 3;
+  }
+  src = static_cast<int64_t>(a.ring_single ? 0 : seq) * kWin + (tok % kWin);
+  return 2;
+}
+
+template <int HP>
+__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits, int per_split) {
+  constexpr int kCons = HP * 4;         // consumer threads: HP / 8 warps
+  constexpr int kDW = 4096 / HP;        // output dims per consumer warp
+  constexpr int kNT = kDW / 8;          // n8 tiles per consumer warp
+  constexpr int kMT = HP / 16;          // m16 tiles (head groups)
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  AttnSmem<HP> &sm = *reinterpret_cast<AttnSmem<HP> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int hg = blockIdx.x, split = blockIdx.y, row = blockIdx.z;
-  const int H = a.heads;
+  const int split = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kHeadBlock;
+  const int nh = min(HP, a.heads - hbase);
   const int seq = a.cache_seq < 0 ? row : a.cache_seq;
   const int64_t qpos = a.q_pos[row];
   const int64_t T = qpos / a.ratio;
@@ -169,186 +146,338 @@ __global__ void __launch_bounds__(kThreads) k_attn(AttnArgs a, int n_splits, int
   const int L = a.k + kWin;
   const int e_begin = split * per_split;
   const int e_end = min(L, e_begin + per_split);
-  const float scale2 = a.sm_scale * kLog2e;
+  const int nchunks = e_begin < e_end ? (e_end - e_begin + kE - 1) / kE : 0;
 
-  // Q rows of this head group
-  {
-    const uint4 *qsrc = reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(row) * H + hg * 16) * kDqk);
-    for (int i = tid; i < 16 * 72; i += kThreads) {
-      const int r = i / 72, c = i % 72;
-      *reinterpret_cast<uint4 *>(&sm.q[r][8 * c]) = qsrc[r * 72 + c];
-    }
+  // ---- set-up: barriers, dequant table, the query as scaled fp16
+  if (tid == 0) {
+    tc::mbar_init(&sm.full[0], kProdThreads);
+    tc::mbar_init(&sm.full[1], kProdThreads);
+    tc::mbar_init(&sm.empty[0], kCons);
+    tc::mbar_init(&sm.empty[1], kCons);
+    tc::fence_mbar_init();
   }
-
-  float o[16][4];
+  for (int i = tid; i < 256; i += blockDim.x) {
+    __half2 h = __floats2half2_rn(e2m1_value(i & 15), e2m1_value(i >> 4));
+    sm.lut[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  for (int h = warp; h < HP; h += blockDim.x / 32) {
+    uint4 raw[3];
+    float amax = 0.0f;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk);
 #pragma unroll
-  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
+    for (int i = 0; i < 3; ++i) {
+      const int c = lane + 32 * i;
+      raw[i] = make_uint4(0, 0, 0, 0);
+      if (h < nh && c < kDqk / 8) raw[i] = src[c];
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2)
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k2] << 16)), fabsf(__uint_as_float(w[k2] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // |q * 2^-e| < 2^15: inside fp16, exact for every bf16 value >= amax * 2^-24
+    int e = amax > 0.0f ? floor_log2f(amax) - 14 : 0;
+    e = max(e, -110);
+    const float inv = pow2f(-e);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int c = lane + 32 * i;
+      if (c < kDqk / 8) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[k2] << 16), inv),
+                                         __fmul_rn(__uint_as_float(w[k2] & 0xFFFF0000u), inv));
+          hv[k2] = *reinterpret_cast<uint32_t *>(&t2);
+        }
+        *reinterpret_cast<uint4 *>(&sm.q[h][8 * c]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+    }
+    if (lane == 0) sm.qf[h] = h < nh ? pow2f(e) * a.sm_scale * kLog2e : 0.0f;
+  }
+  __syncthreads();
 
-  for (int c0 = e_begin; c0 < e_end; c0 += kEnt) {
-    __syncthreads();  // previous chunk fully consumed (and Q stored on the first pass)
-    if (tid < kEnt) {
-      const int j = c0 + tid;
-      int kind = 0;
-      int64_t src = 0;
-      if (j < e_end) {
-        if (j < a.k) {
-          const int32_t s = a.idx[static_cast<size_t>(row) * a.k + j];
-          if (s >= 0) {
-            if (s < T && s < a.cap) {
-              kind = 1;
-              src = static_cast<int64_t>(seq) * a.cap + s;
-            } else {
-              raise_err(a.err, CSA2_DEVERR_INDEX);
+  if (tid >= kCons) {
+    // ================================================================ producers
+    const int pt = tid - kCons;
+    const int e = pt >> 2, q4 = pt & 3;
+    const uint32_t qmask = 0xFu << (lane & ~3);  // the four lanes of this entry
+    bool dead = false;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c & 1;
+      if (c >= 2 && !dead) dead = !wait_warp(&sm.empty[st], ((c - 2) >> 1) & 1, a.err);
+      if (!dead) {
+        const int j = e_begin + c * kE + e;
+        int64_t src = 0;
+        const int kind = j < e_end ? entry_src(a, row, seq, j, qpos, T, ntok, lin_base, src) : 0;
+        uint4 *dst = reinterpret_cast<uint4 *>(&sm.kv[st][e][0]);  // 16-dim unit u at dst[2u], dst[2u+1]
+        float sig = 0.0f;
+        if (kind == 1) {
+          // FP4 entry: unit u < 32 = latent dims 16u.. (8 code bytes, scale u), u = 32 + q4 the RoPE group q4
+          const uint2 *lc = reinterpret_cast<const uint2 *>(a.lat_codes + src * 256);
+          const uint4 *ls = reinterpret_cast<const uint4 *>(a.lat_scales + src * 32);
+          uint2 cw[9];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cw[i] = lc[q4 + 4 * i];
+          cw[8] = reinterpret_cast<const uint2 *>(a.rope_codes + src * 32)[q4];
+          const uint4 s0 = ls[0], s1 = ls[1];
+          const uint32_t rsc = a.rope_scales[src * 4 + q4];
+          const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+          for (int i = 0; i < 9; ++i) {
+            const int u = i < 8 ? q4 + 4 * i : 32 + q4;
+            const uint32_t sb = i < 8 ? (sw[u >> 2] >> (8 * (u & 3))) & 0xFFu : rsc;
+            const uint32_t s2 = e4m3x2_to_h2(sb | (sb << 8));
+            uint32_t o[8];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              o[b] = hmul2u(sm.lut[(cw[i].x >> (8 * b)) & 0xFFu], s2);
+              o[4 + b] = hmul2u(sm.lut[(cw[i].y >> (8 * b)) & 0xFFu], s2);
             }
+            dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          sig = 1.0f;
+        } else if (kind == 2 || kind == 3) {
+          const bool ring = kind == 2;
+          const int rec = a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+          const uint8_t *cb = (ring ? a.ring_codes : a.lin_codes) + src * rec;
+          if (a.swa_dtype == CSA2_SWA_MXFP8) {
+            const uint4 *sp = reinterpret_cast<const uint4 *>((ring ? a.ring_scales : a.lin_scales) +
+                                                              src * kSwaScaleStride);
+            const uint4 s0 = sp[0], s1 = sp[1];
+            const uint32_t sw[5] = {s0.x, s0.y, s0.z, s0.w, s1.x};
+            uint32_t mx = 0;
+#pragma unroll
+            for (int g = 0; g < 18; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+            // values < 448 * 2^(sc-127): keep them below 2^16 with sigma >= 0
+            const int sigma = min(15, max(0, static_cast<int>(mx) - 134));
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+              const int u = q4 + 4 * i;
+              const uint4 cw = reinterpret_cast<const uint4 *>(cb)[u];
+              const int sc = static_cast<int>((sw[u >> 3] >> (8 * ((u >> 1) & 3))) & 0xFFu);
+              const int kx = sc - 127 - sigma;
+              const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
+              const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
+                o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
+              }
+              dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+              dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            sig = pow2f(sigma);
+          } else {
+            const uint4 *cw = reinterpret_cast<const uint4 *>(cb);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+              const int u = q4 + 4 * i;
+              const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
+              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+              for (int b = 0; b < 8; ++b)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[b] << 16)), fabsf(__uint_as_float(w[b] & 0xFFFF0000u))));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
+            const int sigma = amax > 0.0f ? min(15, max(0, floor_log2f(amax) - 14)) : 0;
+            const float inv = pow2f(-sigma);
+#pragma unroll
+            for (int i = 0; i < 9; ++i) {
+              const int u = q4 + 4 * i;
+              const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
+              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int b = 0; b < 8; ++b) {
+                __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[b] << 16), inv),
+                                               __fmul_rn(__uint_as_float(w[b] & 0xFFFF0000u), inv));
+                o[b] = *reinterpret_cast<uint32_t *>(&t2);
+              }
+              dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+              dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            sig = pow2f(sigma);
           }
         } else {
-          const int64_t tok = qpos - (kWin - 1) + (j - a.k);
-          if (tok >= 0 && tok < ntok && tok <= qpos) {
-            if (tok >= lin_base) {
-              kind = 3;
-              src = tok - lin_base;
-            } else {
-              kind = 2;
-              src = static_cast<int64_t>(a.ring_single ? 0 : seq) * kWin + (tok % kWin);
-            }
+#pragma unroll
+          for (int i = 0; i < 9; ++i) {
+            const int u = q4 + 4 * i;
+            dst[2 * u] = make_uint4(0, 0, 0, 0);
+            dst[2 * u + 1] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (q4 == 0) sm.sig[st][e] = sig;
+      }
+      tc::mbar_arrive(&sm.full[st]);
+    }
+    return;
+  }
+
+  // ================================================================== consumers
+  const int g = lane >> 2, t = lane & 3;
+  float o[kMT][kNT][4];
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.0f;
+  const int sh = tid >> 2, sq = tid & 3;  // softmax: head sh, entries 8 sq .. 8 sq + 7
+  float m_run = -INFINITY, l_run = 0.0f;
+  bool dead = false;
+  const int hg = warp >> 1, eh = warp & 1;  // QK: heads 16 hg.., entries 16 eh..
+  const int d0 = warp * kDW;                // PV: dims d0 .. d0 + kDW - 1
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c & 1;
+    if (!dead) dead = !wait_warp(&sm.full[st], (c >> 1) & 1, a.err);
+    if (!dead) {
+      // ---- logits of heads 16hg.. x entries 16eh..
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t qa = smem_u32(&sm.q[16 * hg + (lane & 15)][(lane >> 4) * 8]);
+      const uint32_t kb = smem_u32(&sm.kv[st][16 * eh + (lane & 7) + ((lane >> 4) << 3)][((lane >> 3) & 1) * 8]);
+#pragma unroll 6
+      for (int kk = 0; kk < kDqk / 16; ++kk) {
+        uint32_t af[4], b0, b1, b2, b3;
+        ldsm_x4(qa + kk * 32, af[0], af[1], af[2], af[3]);
+        ldsm_x4(kb + kk * 32, b0, b1, b2, b3);
+        mma_f16(acc[0], af, b0, b1);
+        mma_f16(acc[1], af, b2, b3);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int h = 16 * hg + g + 8 * r;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int col = 16 * eh + 8 * nt + 2 * t + cc;
+            const float sg = sm.sig[st][col];
+            sm.s[h][col] = sg > 0.0f ? acc[nt][2 * r + cc] * sm.qf[h] * sg : -INFINITY;
+          }
+        }
+    }
+    bar_consumers(kCons);
+    if (!dead) {
+      // ---- online softmax, 4 threads per head
+      float z[8], mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        z[i] = sm.s[sh][8 * sq + i];
+        mx = fmaxf(mx, z[i]);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
+      float sum = 0.0f;
+      uint32_t pw[4];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const float p0 = m_new == -INFINITY ? 0.0f : exp2f(z[i] - m_new);
+        const float p1 = m_new == -INFINITY ? 0.0f : exp2f(z[i + 1] - m_new);
+        sum += p0 + p1;
+        __half2 h2 = __floats2half2_rn(p0 * sm.sig[st][8 * sq + i], p1 * sm.sig[st][8 * sq + i + 1]);
+        pw[i / 2] = *reinterpret_cast<uint32_t *>(&h2);
+      }
+      *reinterpret_cast<uint4 *>(&sm.p[sh][8 * sq]) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      if (sq == 0) sm.alpha[sh] = alpha;
+    }
+    bar_consumers(kCons);
+    if (!dead) {
+      // ---- O = O * alpha + P V over dims d0..
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const float a0 = sm.alpha[16 * mt + g], a1 = sm.alpha[16 * mt + g + 8];
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          o[mt][nt][0] *= a0;
+          o[mt][nt][1] *= a0;
+          o[mt][nt][2] *= a1;
+          o[mt][nt][3] *= a1;
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < kE / 16; ++ks) {
+        uint32_t af[kMT][4];
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt)
+          ldsm_x4(smem_u32(&sm.p[16 * mt + (lane & 15)][16 * ks + (lane >> 4) * 8]), af[mt][0], af[mt][1], af[mt][2],
+                  af[mt][3]);
+        const uint32_t vb = smem_u32(&sm.kv[st][16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8][d0 + (lane >> 4) * 8]);
+#pragma unroll
+        for (int nt = 0; nt < kNT; nt += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + nt * 16, b0, b1, b2, b3);
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt) {
+            mma_f16(o[mt][nt], af[mt], b0, b1);
+            mma_f16(o[mt][nt + 1], af[mt], b2, b3);
           }
         }
       }
-      sm.kind[tid] = kind;
-      sm.src[tid] = src;
     }
-    __syncthreads();
-    load_entry(a, sm, tid >> 2, tid & 3);
-    __syncthreads();
-
-    // S = Q K^T for entries 8*warp .. 8*warp+7
-    {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t qa = smem_u32(&sm.q[lane & 15][(lane >> 4) * 8]);
-      const uint32_t kb = smem_u32(&sm.k[8 * warp + (lane & 7)][((lane >> 3) & 1) * 8]);
-#pragma unroll 4
-      for (int kk = 0; kk < kDqk / 16; ++kk) {
-        uint32_t a0, a1, a2, a3, b0, b1;
-        ldsm_x4(qa + kk * 32, a0, a1, a2, a3);
-        ldsm_x2(kb + kk * 32, b0, b1);
-        mma_bf16(acc, a0, a1, a2, a3, b0, b1);
-      }
-      sm.s[g][8 * warp + 2 * t] = acc[0] * scale2;
-      sm.s[g][8 * warp + 2 * t + 1] = acc[1] * scale2;
-      sm.s[g + 8][8 * warp + 2 * t] = acc[2] * scale2;
-      sm.s[g + 8][8 * warp + 2 * t + 1] = acc[3] * scale2;
-    }
-    __syncthreads();
-
-    // online softmax (every warp redundantly for its two rows g, g+8)
-    float p[2][2][4];  // [row g/g+8][kk][4 cols]
-    float rmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int col = kk * 16 + 2 * t + (c & 1) + (c >> 1) * 8;
-        const bool ok = sm.kind[col] != 0;
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const float v = ok ? sm.s[g + 8 * rr][col] : -INFINITY;
-          p[rr][kk][c] = v;
-          rmax[rr] = fmaxf(rmax[rr], v);
-        }
-      }
-    float alpha[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      rmax[rr] = fmaxf(rmax[rr], __shfl_xor_sync(0xffffffffu, rmax[rr], 1));
-      rmax[rr] = fmaxf(rmax[rr], __shfl_xor_sync(0xffffffffu, rmax[rr], 2));
-      const float m_new = fmaxf(m_run[rr], rmax[rr]);
-      alpha[rr] = (m_new == -INFINITY) ? 1.0f : exp2f(m_run[rr] - m_new);
-      float sum = 0.0f;
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float e = (m_new == -INFINITY) ? 0.0f : exp2f(p[rr][kk][c] - m_new);
-          p[rr][kk][c] = e;
-          sum += e;
-        }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      l_run[rr] = l_run[rr] * alpha[rr] + sum;
-      m_run[rr] = m_new;
-    }
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= alpha[0];
-      o[n][1] *= alpha[0];
-      o[n][2] *= alpha[1];
-      o[n][3] *= alpha[1];
-    }
-
-    // O += P V for dims 128*warp .. +127
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const uint32_t a0 = pack_half2(p[0][kk][0], p[0][kk][1]);
-      const uint32_t a1 = pack_half2(p[1][kk][0], p[1][kk][1]);
-      const uint32_t a2 = pack_half2(p[0][kk][2], p[0][kk][3]);
-      const uint32_t a3 = pack_half2(p[1][kk][2], p[1][kk][3]);
-      const uint32_t vb =
-          smem_u32(&sm.v[kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8][128 * warp + (lane >> 4) * 8]);
-#pragma unroll
-      for (int n = 0; n < 16; n += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + n * 16, b0, b1, b2, b3);
-        mma_f16(o[n], a0, a1, a2, a3, b0, b1);
-        mma_f16(o[n + 1], a0, a1, a2, a3, b2, b3);
-      }
-    }
+    tc::mbar_arrive(&sm.empty[st]);
   }
 
-  // epilogue
-  const int h0 = hg * 16 + g, h1 = h0 + 8;
+  // ---- epilogue
+  if (sq == 0) {
+    sm.fin[sh][0] = m_run;
+    sm.fin[sh][1] = l_run;
+  }
+  bar_consumers(kCons);
+  if (dead) return;
   if (n_splits == 1) {
-    float inv[2], lse_v[2];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int h = rr ? h1 : h0;
-      float m = m_run[rr], l = l_run[rr], f = 1.0f;
-      if (a.sink) {
-        const float s2 = a.sink[h] * kLog2e;
-        const float mf = fmaxf(m, s2);
-        f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
-        l = l * f + exp2f(s2 - mf);
-        m = mf;
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int hl = 16 * mt + g + 8 * r;
+        if (hl >= nh) continue;
+        const int h = hbase + hl;
+        float m = sm.fin[hl][0], l = sm.fin[hl][1], f = 1.0f;
+        if (a.sink) {
+          const float s2 = a.sink[h] * kLog2e;
+          const float mf = fmaxf(m, s2);
+          f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
+          l = l * f + exp2f(s2 - mf);
+          m = mf;
+        }
+        const float inv = l > 0.0f ? f / l : 0.0f;
+        float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat + d0;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          *reinterpret_cast<float2 *>(out + 8 * nt + 2 * t) =
+              make_float2(o[mt][nt][2 * r] * inv, o[mt][nt][2 * r + 1] * inv);
+        if (warp == 0 && t == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
       }
-      inv[rr] = l > 0.0f ? f / l : 0.0f;
-      lse_v[rr] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
-    }
-    float *out0 = a.out + (static_cast<size_t>(row) * H + h0) * kLat;
-    float *out1 = a.out + (static_cast<size_t>(row) * H + h1) * kLat;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int d = 128 * warp + 8 * n + 2 * t;
-      *reinterpret_cast<float2 *>(out0 + d) = make_float2(o[n][0] * inv[0], o[n][1] * inv[0]);
-      *reinterpret_cast<float2 *>(out1 + d) = make_float2(o[n][2] * inv[1], o[n][3] * inv[1]);
-    }
-    if (warp == 0 && t == 0) {
-      a.lse[static_cast<size_t>(row) * H + h0] = lse_v[0];
-      a.lse[static_cast<size_t>(row) * H + h1] = lse_v[1];
-    }
   } else {
-    const size_t base = (static_cast<size_t>(row) * n_splits + split) * H;
-    float *po = a.part;                                                       // [rows][splits][H][512]
-    float *pml = a.part + static_cast<size_t>(a.rows) * n_splits * H * kLat;  // [rows][splits][H][2]
+    const size_t base = (static_cast<size_t>(row) * n_splits + split) * a.heads;
+    float *po = a.part;                                                              // [rows][splits][H][512]
+    float *pml = a.part + static_cast<size_t>(a.rows) * n_splits * a.heads * kLat;  // [rows][splits][H][2]
 #pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      const int d = 128 * warp + 8 * n + 2 * t;
-      *reinterpret_cast<float2 *>(po + (base + h0) * kLat + d) = make_float2(o[n][0], o[n][1]);
-      *reinterpret_cast<float2 *>(po + (base + h1) * kLat + d) = make_float2(o[n][2], o[n][3]);
-    }
-    if (warp == 0 && t == 0) {
-      *reinterpret_cast<float2 *>(pml + (base + h0) * 2) = make_float2(m_run[0], l_run[0]);
-      *reinterpret_cast<float2 *>(pml + (base + h1) * 2) = make_float2(m_run[1], l_run[1]);
-    }
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int hl = 16 * mt + g + 8 * r;
+        if (hl >= nh) continue;
+        const int h = hbase + hl;
+        float *out = po + (base + h) * kLat + d0;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt)
+          *reinterpret_cast<float2 *>(out + 8 * nt + 2 * t) = make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
+        if (warp == 0 && t == 0)
+          *reinterpret_cast<float2 *>(pml + (base + h) * 2) = make_float2(sm.fin[hl][0], sm.fin[hl][1]);
+      }
   }
 }
 
@@ -384,15 +513,32 @@ __global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int n_splits) 
   if (threadIdx.x == 0) a.lse[static_cast<size_t>(row) * H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
+int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
+
+// Entry splits per (row, head block): fill the 152 SMs once (one CTA per SM),
+// at least one 32-entry chunk per split.
 int choose_splits(int rows, int heads, int k) {
   const int L = k + kWin;
-  const int ctas = rows * (heads / 16);
-  if (ctas >= 120) return 1;            // the rows alone fill most of the 152 SMs
-  int s = (2 * 152 + ctas - 1) / ctas;  // aim for ~2 CTAs per SM
-  const int max_s = (L + 63) / 64;      // at least 64 entries per split
+  const int ctas = rows * head_blocks(heads);
+  int s = 152 / ctas;
+  const int max_s = (L + kE - 1) / kE;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
   return s;
+}
+
+template <int HP>
+cudaError_t launch_hp(const AttnArgs &a, int n_splits, int per, cudaStream_t st) {
+  static bool attr_set = false;
+  const int smem = static_cast<int>(sizeof(AttnSmem<HP>));
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(n_splits, a.rows, head_blocks(a.heads));
+  k_attn<HP><<<grid, HP * 4 + kProdThreads, smem, st>>>(a, n_splits, per);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -409,19 +555,15 @@ cudaError_t launch_attn(const AttnArgs &a0, void *ws, size_t ws_bytes, cudaStrea
   const int n_splits = choose_splits(a.rows, a.heads, a.k);
   const int L = a.k + kWin;
   int per = (L + n_splits - 1) / n_splits;
-  per = (per + kEnt - 1) / kEnt * kEnt;
+  per = (per + kE - 1) / kE * kE;
   a.part = static_cast<float *>(ws);
-  static bool attr_set = false;
-  const int smem = static_cast<int>(sizeof(Smem));
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  dim3 grid(a.heads / 16, n_splits, a.rows);
-  k_attn<<<grid, kThreads, smem, st>>>(a, n_splits, per);
-  if (n_splits > 1) k_attn_combine<<<dim3(a.heads, a.rows), 128, 0, st>>>(a, n_splits);
   (void)ws_bytes;
+  cudaError_t e;
+  if (a.heads <= 16) e = launch_hp<16>(a, n_splits, per, st);
+  else if (a.heads <= 32) e = launch_hp<32>(a, n_splits, per, st);
+  else e = launch_hp<64>(a, n_splits, per, st);
+  if (e != cudaSuccess) return e;
+  if (n_splits > 1) k_attn_combine<<<dim3(a.heads, a.rows), 128, 0, st>>>(a, n_splits);
   return cudaGetLastError();
 }
 

@@ -90,4 +90,114 @@ __device__ __forceinline__ void warp_encode_swa(uint8_t *codes, uint8_t *scales,
   }
 }
 
+// ---------------------------------------------------------------- block encoders
+// The same encodings with a whole 256-thread block on one token: every thread
+// quantises 1..4 values and group maxima are lane shuffles, so the token's
+// ~1,300 values take a few dependent steps instead of one warp's long loops.
+constexpr int kEncThreads = 256;
+
+// rot[0:64] = RoPE dims of row (row[512:576]) rotated with cs; threads 0..31.
+__device__ __forceinline__ void block_rope(const float *row, const float *cs, float *rot) {
+  const int t = threadIdx.x;
+  if (t < 32) {
+    float a = row[kLat + 2 * t], bb = row[kLat + 2 * t + 1];
+    rope_pair(a, bb, cs[2 * t], cs[2 * t + 1]);
+    rot[2 * t] = a;
+    rot[2 * t + 1] = bb;
+  }
+}
+
+// Two values of an NVFP4 group of 16 held by 8 consecutive lanes: returns the
+// packed byte (first value in the low nibble); *sc = the group's scale code.
+__device__ __forceinline__ uint32_t nvfp4_pair(float x0, float x1, uint32_t *sc) {
+  float amax = fmaxf(fabsf(x0), fabsf(x1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  uint32_t code = e4m3_code(__fdiv_rn(amax, 6.0f));
+  const float s = e4m3_value(code);
+  if (s == 0.0f) {
+    *sc = 0;
+    return 0;
+  }
+  *sc = code;
+  return e2m1_code(__fdiv_rn(x0, s)) | (e2m1_code(__fdiv_rn(x1, s)) << 4);
+}
+
+// Entry e of sequence b from row[0:704] (smem: main vector, RoPE dims
+// unrotated, then the indexer key) and rot[0:64] (smem, rotated RoPE dims).
+__device__ __forceinline__ void block_encode_entry(const csa2_cache &c, int b, int64_t e, const float *row,
+                                                   const float *rot) {
+  const int t = threadIdx.x, lane = t & 31;
+  const size_t ent = static_cast<size_t>(b) * c.capacity + e;
+  uint32_t sc;
+  {  // latent: thread t has dims 2t, 2t+1 (group t / 8)
+    const float2 v = reinterpret_cast<const float2 *>(row)[t];
+    const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
+    c.lat_codes[ent * 256 + t] = static_cast<uint8_t>(byte);
+    if ((t & 7) == 0) c.lat_scales[ent * 32 + (t >> 3)] = static_cast<uint8_t>(sc);
+  }
+  if (t < 32) {  // RoPE sidecar: rotated dims 2t, 2t+1 (group t / 8)
+    const float2 v = reinterpret_cast<const float2 *>(rot)[t];
+    const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
+    c.rope_codes[ent * 32 + t] = static_cast<uint8_t>(byte);
+    if ((t & 7) == 0) c.rope_scales[ent * 4 + (t >> 3)] = static_cast<uint8_t>(sc);
+  } else if (t < 64) {  // indexer key, MXFP4: lane l has dims 4l..4l+3 (block l / 8)
+    const float4 v = reinterpret_cast<const float4 *>(row + kDqk)[lane];
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    uint32_t codes = 0;
+    sc = 0;
+    if (amax != 0.0f) {
+      int ex = floor_log2f(amax) - 2;
+      ex = max(-127, min(127, ex));
+      const float inv = pow2f(-ex);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) codes |= e2m1_code(__fmul_rn(x[i], inv)) << (4 * i);
+      sc = static_cast<uint32_t>(ex + 127);
+    }
+    const int blk = lane >> 3;
+    const int64_t tbase = static_cast<int64_t>(b) * idx_tiles(c.capacity);
+    *reinterpret_cast<uint16_t *>(c.idx_codes + idx_code_off(tbase, e, blk) + 2 * (lane & 7)) =
+        static_cast<uint16_t>(codes);
+    if ((lane & 7) == 0) c.idx_scales[idx_scale_off(tbase, e) + blk] = static_cast<uint8_t>(sc);
+  }
+}
+
+// One window token from row[0:512] (smem) and rot[0:64] (smem) into codes
+// (576 B MXFP8 or 1152 B bf16) and scales (18 B, MXFP8).
+__device__ __forceinline__ void block_encode_swa(uint8_t *codes, uint8_t *scales, int swa_dtype, const float *row,
+                                                 const float *rot) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (swa_dtype == CSA2_SWA_MXFP8) {
+    // group g (32 dims) on warp g % 8, one dim per lane
+    for (int g = warp; g < 18; g += kEncThreads / 32) {
+      const int d = 32 * g + lane;
+      const float x = d < kLat ? row[d] : rot[d - kLat];
+      float amax = fabsf(x);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      uint32_t code = 0, sc = 0;
+      if (amax != 0.0f) {
+        int ex = floor_log2f(amax) - 8;
+        ex = max(-127, min(127, ex));
+        code = e4m3_code(__fmul_rn(x, pow2f(-ex)));
+        sc = static_cast<uint32_t>(ex + 127);
+      }
+      // four lanes' bytes into one word
+      uint32_t w = code << (8 * (lane & 3));
+      w |= __shfl_xor_sync(0xffffffffu, w, 1);
+      w |= __shfl_xor_sync(0xffffffffu, w, 2);
+      if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(codes + 32 * g)[lane >> 2] = w;
+      if (lane == 0) scales[g] = static_cast<uint8_t>(sc);
+    }
+  } else {
+    __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(codes);
+    for (int d = t; d < kDqk; d += kEncThreads) h[d] = __float2bfloat16_rn(d < kLat ? row[d] : rot[d - kLat]);
+  }
+}
+
 }  // namespace csa2

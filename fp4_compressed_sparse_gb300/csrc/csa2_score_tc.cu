@@ -48,27 +48,46 @@ constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait
 // chunk c of head h at c*NP*16 + h*16), SFB atom (512 B), w (NP floats).
 __host__ __device__ __forceinline__ int qrec_bytes(int np) { return np * 64 + 512 + np * 4; }
 
-__global__ void __launch_bounds__(128) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out) {
-  const int r = blockIdx.x;
+// grid (rows, np / 8), 256 threads: one warp per (row, head); lane l quantises
+// dims 4l..4l+3 (MX block l / 8; the block's amax is a max over its 8 lanes).
+__global__ void __launch_bounds__(256) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out) {
+  const int r = blockIdx.x, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
   uint8_t *rec = out + static_cast<size_t>(r) * qrec_bytes(np);
   uint8_t *sfb = rec + np * 64;
-  float *wr = reinterpret_cast<float *>(sfb + 512);
-  for (int i = threadIdx.x; i < 512 / 16; i += blockDim.x) reinterpret_cast<uint4 *>(sfb)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  for (int task = threadIdx.x; task < np * 4; task += blockDim.x) {
-    const int h = task >> 2, blk = task & 3;
-    uint32_t w4[4] = {0, 0, 0, 0}, sc = 0;
-    if (h < H) {
-      const uint16_t *src = q_idx + (static_cast<size_t>(r) * H + h) * kDi + 32 * blk;
-      float x[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(static_cast<uint32_t>(src[i]) << 16);
-      quant_mxfp4_32(x, w4, &sc);
-    }
-    *reinterpret_cast<uint4 *>(rec + blk * np * 16 + h * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    sfb[16 * (h % 32) + 4 * (h / 32) + blk] = static_cast<uint8_t>(sc);
+  if (blockIdx.y == 0) {
+    // scale-factor rows of heads np..127 are never written below: zero them
+    for (int i = threadIdx.x; i < 512; i += blockDim.x)
+      if ((i / 16) + 32 * ((i % 16) / 4) >= np) sfb[i] = 0;
+    float *wr = reinterpret_cast<float *>(sfb + 512);
+    for (int j = threadIdx.x; j < np; j += blockDim.x) wr[j] = j < H ? w[static_cast<size_t>(r) * H + j] : 0.0f;
   }
-  for (int h = threadIdx.x; h < np; h += blockDim.x) wr[h] = h < H ? w[static_cast<size_t>(r) * H + h] : 0.0f;
+  if (h >= np) return;
+  float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (h < H) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(q_idx + (static_cast<size_t>(r) * H + h) * kDi + 4 * lane);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  }
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  uint32_t codes = 0, sc = 0;
+  if (amax != 0.0f) {
+    // MXFP4: e = floor(log2 amax) - 2 (clamped to [-127, 127]); codes E2M1(x * 2^-e)
+    int e = floor_log2f(amax) - 2;
+    e = max(-127, min(127, e));
+    const float inv = pow2f(-e);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) codes |= e2m1_code(__fmul_rn(x[i], inv)) << (4 * i);
+    sc = static_cast<uint32_t>(e + 127);
+  }
+  const int blk = lane >> 3;
+  *reinterpret_cast<uint16_t *>(rec + blk * np * 16 + h * 16 + 2 * (lane & 7)) = static_cast<uint16_t>(codes);
+  if ((lane & 7) == 0) sfb[16 * (h % 32) + 4 * (h / 32) + blk] = static_cast<uint8_t>(sc);
 }
 
 struct TcArgs {
@@ -432,7 +451,7 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   a.qrec = static_cast<const uint8_t *>(ws);
   const int cols = kAcc * a.np + 8 * kAcc + 16;
   a.ncols = cols <= 128 ? 128 : (cols <= 256 ? 256 : 512);
-  k_qprep<<<s.rows, 128, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
+  k_qprep<<<dim3(s.rows, a.np / 8), 256, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
   const int max_tiles = static_cast<int>(
       s.pool ? (static_cast<int64_t>(s.pool_blocks) * s.pool_bs + kIdxTile - 1) / kIdxTile
              : idx_tiles(s.cap < s.stride ? s.cap : s.stride));

@@ -14,13 +14,19 @@
 // Per (row, problem) -- problem 0 is the top-k over the row's slots, problem 1
 // the top blocks by block maximum (FULL rows building a pool):
 //   resolve  one CTA: the 13-bit histogram (from the score kernel's sideband)
-//            gives the threshold bin, where the count from the top reaches k
-//   collect  many CTAs: keys in bins >= the threshold go to a candidate buffer
-//            (at most kSelCap; overflow is flagged)
-//   final    one CTA: bitonic sort of the candidates by K, the first k kept,
-//            then their positions sorted ascending and written (-1 padded).
-//            After an overflow (a very crowded threshold bin) it instead runs an
-//            exact radix select over the whole row.
+//            gives the threshold bin, where the count from the top reaches k,
+//            and how many keys lie strictly above it
+//   collect  many CTAs: every slot whose key lies above the threshold bin is
+//            chosen outright and marked in a per-row bitmap (one warp ballot per
+//            32 slots writes one word); keys in the threshold bin go to a
+//            candidate list (at most kSelCap; overflow is flagged)
+//   final    one CTA: an exact radix select over the candidates' low 51 key
+//            bits picks the ones still needed and marks them, then a block scan
+//            over the bitmap writes the chosen positions in ascending order
+//            (-1 padded).  After an overflow (a very crowded threshold bin) the
+//            radix select runs over the whole row instead.
+// Slots run in ascending position order in every mode, so the bitmap order is
+// the output order and no sort is needed.
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -28,13 +34,15 @@ namespace {
 
 constexpr int kChunk = 4096;  // slots per collect CTA
 constexpr int kCollectThreads = 256;
-constexpr int kFinalThreads = 1024;
+constexpr int kFinalThreads = 512;
 
 struct SelState {
-  uint32_t thr_bin;   // lowest bin that holds candidates
+  uint32_t thr_bin;   // the bin where the count from the top reaches k
+  uint32_t above;     // valid keys in bins above thr_bin (all chosen)
   uint32_t total;     // valid slots
-  uint32_t ncand;     // candidates appended (may exceed kSelCap)
+  uint32_t ncand;     // keys of bin thr_bin appended (may exceed kSelCap)
   uint32_t overflow;  // 1: ncand > kSelCap
+  uint32_t pad[3];
 };
 
 __device__ __forceinline__ uint32_t key_of(float f) { return isnan(f) ? 0u : orderable(f); }
@@ -128,13 +136,18 @@ __global__ void __launch_bounds__(256) k_fill_aux(TopkArgs a, uint8_t *aux, int6
 // ----------------------------------------------------------------------------- resolve
 // grid (rows, problems), 256 threads
 __global__ void __launch_bounds__(256) k_resolve(TopkArgs a, const uint8_t *aux, int64_t aux_row, SelState *st) {
+  __shared__ uint32_t hs[kSelBins];
   __shared__ uint32_t warp_tot[8];
   const int row = blockIdx.x, p = blockIdx.y;
-  const uint32_t *h = aux_hist(aux, aux_row, row, p);
-  const int per = kSelBins / 256;  // 32 bins per thread, thread 0 owns the top bins
+  const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
+  for (int i = threadIdx.x; i < kSelBins / 4; i += blockDim.x) reinterpret_cast<uint4 *>(hs)[i] = h4[i];
+  __syncthreads();
+  // thread t owns the 32 bins kSelBins-1-32t-i, i = 0..31 (thread 0 the top ones);
+  // the rotated index keeps the 32 reads of a step in distinct banks
+  constexpr int per = kSelBins / 256;
+  const int top = kSelBins - 1 - threadIdx.x * per;
   uint32_t local = 0;
-  for (int i = 0; i < per; ++i) local += h[kSelBins - 1 - (threadIdx.x * per + i)];
-  // exclusive scan over threads (counts strictly above this thread's bins)
+  for (int i = 0; i < per; ++i) local += hs[top - ((i + threadIdx.x) & (per - 1))];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = local;
   for (int o = 1; o < 32; o <<= 1) {
@@ -148,30 +161,38 @@ __global__ void __launch_bounds__(256) k_resolve(TopkArgs a, const uint8_t *aux,
     if (w < warp) before += warp_tot[w];
     total += warp_tot[w];
   }
-  const uint32_t above = before + x - local;
+  const uint32_t above = before + x - local;  // keys in bins above this thread's
   SelState *s = st + static_cast<size_t>(row) * 2 + p;
   const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
   if (total <= k) {
-    if (threadIdx.x == 0) *s = SelState{0u, total, 0u, 0u};  // every valid slot is chosen
+    // every valid slot is chosen: bin 0 is the threshold bin
+    if (threadIdx.x == 0) *s = SelState{0u, total - hs[0], total, 0u, 0u, {0u, 0u, 0u}};
     return;
   }
   if (above < k && k <= above + local) {
     uint32_t acc = above;
     for (int i = 0; i < per; ++i) {
-      const uint32_t bin = kSelBins - 1 - (threadIdx.x * per + i);
-      acc += h[bin];
-      if (acc >= k) {
-        *s = SelState{bin, total, 0u, 0u};
+      const uint32_t bin = top - i;
+      if (acc + hs[bin] >= k) {
+        *s = SelState{bin, acc, total, 0u, 0u, {0u, 0u, 0u}};
         break;
       }
+      acc += hs[bin];
     }
   }
 }
 
 // ----------------------------------------------------------------------------- collect
-// grid (chunks, rows, problems), 256 threads
+__device__ __forceinline__ uint32_t *row_bitmap(uint32_t *bm, int64_t stride, int row, int p) {
+  const int64_t w0 = (stride + 31) / 32, w1 = ((stride + 7) / 8 + 31) / 32;
+  return bm + static_cast<size_t>(row) * (w0 + w1) + (p ? w0 : 0);
+}
+
+// grid (chunks, rows, problems), 256 threads; thread i of a step handles slot
+// s0 + 256*step + i, so warp w covers one aligned 32-slot bitmap word
 __global__ void __launch_bounds__(kCollectThreads) k_collect(TopkArgs a, const uint8_t *aux, int64_t aux_row,
-                                                             SelState *st, uint64_t *cand) {
+                                                             SelState *st, uint64_t *cand, uint32_t *bitmap) {
+  constexpr int kSteps = kChunk / kCollectThreads;
   const int row = blockIdx.y, p = blockIdx.z;
   const int64_t ns = n_slots(a, row, p);
   const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kChunk;
@@ -180,19 +201,45 @@ __global__ void __launch_bounds__(kCollectThreads) k_collect(TopkArgs a, const u
   const uint32_t thr = s->thr_bin;
   const int64_t T = row_T(a, row);
   uint64_t *cb = cand + (static_cast<size_t>(row) * 2 + p) * kSelCap;
+  uint32_t *bm = row_bitmap(bitmap, a.stride, row, p);
   const int lane = threadIdx.x & 31;
-  for (int i = 0; i < kChunk / kCollectThreads; ++i) {
+  // all loads of the chunk first (independent, no side effects between them),
+  // then the keys and the ballots
+  float f[kSteps];
+  int32_t pid[kSteps];
+  const float *src = p == 1 ? aux_bmax(aux, aux_row, row) : a.scores + static_cast<size_t>(row) * a.stride;
+  const bool pooled = p == 0 && a.pool != nullptr;
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
     const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
-    bool want = false;
-    uint64_t K = 0;
-    if (slot < ns) {
-      uint32_t key;
-      int32_t pos;
-      if (slot_key(a, aux, aux_row, row, p, slot, T, key, pos) && (key >> kSelBinShift) >= thr) {
-        want = true;
-        K = (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(slot));
-      }
-    }
+    f[i] = slot < ns ? src[slot] : 0.0f;
+    pid[i] = pooled && slot < ns ? a.pool[static_cast<size_t>(row) * a.pool_blocks + slot / a.bs] : 0;
+  }
+  uint32_t key[kSteps];
+  uint32_t valid = 0;
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
+    bool ok = slot < ns;
+    if (pooled) ok = ok && pid[i] >= 0 && static_cast<int64_t>(pid[i]) * a.bs + slot % a.bs < T;
+    key[i] = key_of(f[i]);
+    if (ok) valid |= 1u << i;
+  }
+  if (p == 0) {
+#pragma unroll
+    for (int i = 0; i < kSteps; ++i)
+      if (((valid >> i) & 1u) && isnan(f[i])) raise_err(a.err, CSA2_DEVERR_NAN);
+  }
+#pragma unroll
+  for (int i = 0; i < kSteps; ++i) {
+    const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
+    const int64_t wbase = slot - lane;
+    if (wbase >= ns) break;  // warp-uniform
+    const bool ok = (valid >> i) & 1u;
+    const uint32_t bin = key[i] >> kSelBinShift;
+    const uint32_t word = __ballot_sync(0xffffffffu, ok && bin > thr);
+    if (lane == 0) bm[wbase >> 5] = word;
+    const bool want = ok && bin == thr;
     const uint32_t mask = __ballot_sync(0xffffffffu, want);
     if (mask) {
       const int leader = __ffs(mask) - 1;
@@ -201,8 +248,10 @@ __global__ void __launch_bounds__(kCollectThreads) k_collect(TopkArgs a, const u
       base = __shfl_sync(0xffffffffu, base, leader);
       if (want) {
         const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
-        if (at < kSelCap) cb[at] = K;
-        else s->overflow = 1;
+        if (at < kSelCap)
+          cb[at] = (static_cast<uint64_t>(key[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(slot));
+        else
+          s->overflow = 1;
       }
     }
   }
@@ -215,168 +264,169 @@ __device__ __forceinline__ int32_t slot_position(const TopkArgs &a, int row, int
   return pid * a.bs + static_cast<int32_t>(slot % a.bs);
 }
 
-// bitonic sort of n (a power of two) 64-bit keys in shared memory, descending
-__device__ void bitonic_desc_u64(uint64_t *v, int n) {
-  for (int size = 2; size <= n; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const uint64_t x = v[lo], y = v[hi];
-        if ((x < y) == desc) {
-          v[lo] = y;
-          v[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-}
-// ascending sort of n (a power of two) int32 in shared memory
-__device__ void bitonic_asc_i32(int32_t *v, int n) {
-  for (int size = 2; size <= n; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool asc = (lo & size) == 0;
-        const int32_t x = v[lo], y = v[hi];
-        if ((x > y) == asc) {
-          v[lo] = y;
-          v[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
+constexpr uint64_t kLow = (1ull << 51) - 1;  // key bits below the 13-bit bin: 19 score bits, 32 slot bits
+
+__device__ __forceinline__ uint64_t low_of(uint32_t key, uint32_t slot) {
+  return (static_cast<uint64_t>(key & ((1u << kSelBinShift) - 1)) << 32) | (0xFFFFFFFFu - slot);
 }
 
-__device__ __forceinline__ int pow2_at_least(int n) {
-  int m = 1;
-  while (m < n) m <<= 1;
-  return m;
+// One radix digit of the select: hist holds the counts of the digit values
+// among the keys that match the prefix so far; find the digit where the count
+// from the top reaches *rem, extend the prefix, reduce *rem.  Warp 0 only.
+__device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_t *rem, uint64_t *prefix,
+                                           uint32_t *done) {
+  const int lane = threadIdx.x & 31;
+  uint32_t local = 0;
+  for (int i = 0; i < 8; ++i) local += hist[255 - 8 * lane - i];
+  uint32_t x = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  const uint32_t above = x - local;
+  const uint32_t r = *rem;
+  __syncwarp();
+  if (above < r && r <= above + local) {
+    uint32_t acc = above;
+    for (int i = 0; i < 8; ++i) {
+      const int dg = 255 - 8 * lane - i;
+      if (acc + hist[dg] >= r) {
+        *rem = r - acc;
+        *prefix |= static_cast<uint64_t>(dg) << sh;
+        // every key under this prefix is needed: the prefix (lower bits 0) is the cut
+        if (hist[dg] == r - acc) *done = 1;
+        break;
+      }
+      acc += hist[dg];
+    }
+  }
 }
 
-// grid (rows, problems), 1024 threads; dynamic smem: kSelCap u64 + 2048 int32 + scratch
+// grid (rows, problems), kFinalThreads threads; dynamic smem: kSelCap u64
 __global__ void __launch_bounds__(kFinalThreads) k_final(TopkArgs a, const uint8_t *aux, int64_t aux_row,
-                                                         const SelState *st, const uint64_t *cand) {
+                                                         const SelState *st, const uint64_t *cand,
+                                                         uint32_t *bitmap) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint64_t *v = reinterpret_cast<uint64_t *>(smem);
-  int32_t *pos = reinterpret_cast<int32_t *>(smem + kSelCap * 8);
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t s_cnt, s_prefix_hi, s_prefix_lo, s_krem;
+  __shared__ uint32_t s_rem, s_done;
+  __shared__ uint64_t s_prefix;
+  __shared__ uint32_t warp_tot[kFinalThreads / 32];
   const int row = blockIdx.x, p = blockIdx.y;
   const SelState s = st[static_cast<size_t>(row) * 2 + p];
   const int k = prob_k(a, p);
-  const int kt = static_cast<int>(min(static_cast<uint32_t>(k), s.total));  // positions to output
-  int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
-                        : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
+  const uint32_t kt = min(static_cast<uint32_t>(k), s.total);  // positions to output
+  const uint32_t need = kt - s.above;                           // still to choose from bin thr_bin
+  const int64_t ns = n_slots(a, row, p);
+  const int64_t T = row_T(a, row);
+  uint32_t *bm = row_bitmap(bitmap, a.stride, row, p);
+  const int n = static_cast<int>(min(s.ncand, static_cast<uint32_t>(kSelCap)));
+  const bool from_row = s.overflow != 0;  // the candidates did not all fit: select over the row
 
-  if (!s.overflow) {
-    const int n = static_cast<int>(min(s.ncand, static_cast<uint32_t>(kSelCap)));
-    const int n2 = pow2_at_least(max(n, 1));
+  if (!from_row) {
     const uint64_t *cb = cand + (static_cast<size_t>(row) * 2 + p) * kSelCap;
-    for (int i = threadIdx.x; i < n2; i += blockDim.x) v[i] = i < n ? cb[i] : 0ull;
-    __syncthreads();
-    bitonic_desc_u64(v, n2);
-    for (int i = threadIdx.x; i < kt; i += blockDim.x)
-      pos[i] = slot_position(a, row, p, 0xFFFFFFFFu - static_cast<uint32_t>(v[i]));
-  } else {
-    // Exact radix select over the whole row: the threshold bin holds more than
-    // kSelCap keys.  Find the kr-th largest K among the keys of that bin,
-    // digit by digit (8 bits) over its low 51 bits, then gather.
-    const int64_t ns = n_slots(a, row, p);
-    const int64_t T = row_T(a, row);
-    const uint32_t thr = s.thr_bin;
-    if (threadIdx.x == 0) {
-      s_prefix_hi = 0;
-      s_prefix_lo = 0;
-      s_cnt = 0;
-    }
-    // keys strictly above the bin
-    __shared__ uint32_t s_above;
-    if (threadIdx.x == 0) s_above = 0;
-    __syncthreads();
-    uint32_t above_local = 0;
-    for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
-      uint32_t key;
-      int32_t q;
-      if (slot_key(a, aux, aux_row, row, p, slot, T, key, q) && (key >> kSelBinShift) > thr) ++above_local;
-    }
-    atomicAdd(&s_above, above_local);
-    __syncthreads();
-    if (threadIdx.x == 0) s_krem = static_cast<uint32_t>(kt) - s_above;
-    __syncthreads();
-    // 51 low bits (19 score bits, then 32 slot bits), digits from the top:
-    // bits 50..43, 42..35, 34..27, 26..19, 18..11, 10..3, then 2..0
-    constexpr uint64_t kLow = (1ull << 51) - 1;
-    uint64_t prefix = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) v[i] = cb[i];
+  }
+  if (threadIdx.x == 0) {
+    s_rem = need;
+    s_prefix = 0;
+    s_done = 0;
+  }
+  __syncthreads();
+  // exact select of the need-th largest low key among bin thr_bin: 8-bit digits
+  // over bits 50..3, then bits 2..0
+  const bool all = !from_row && need == static_cast<uint32_t>(n);
+  if (need > 0 && !all) {
     for (int d = 0; d < 7; ++d) {
       const int sh = d < 6 ? 43 - 8 * d : 0;
-      const int width = d < 6 ? 8 : 3;
-      const uint64_t hi_mask = kLow & ~((1ull << (sh + width)) - 1);
+      const uint32_t dmask = d < 6 ? 0xFFu : 0x7u;
+      const uint64_t hi_mask = kLow & ~((1ull << (sh + (d < 6 ? 8 : 3))) - 1);
       for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
-        uint32_t key;
-        int32_t q;
-        if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q) || (key >> kSelBinShift) != thr) continue;
-        const uint64_t low = (static_cast<uint64_t>(key & ((1u << kSelBinShift) - 1)) << 32) |
-                             (0xFFFFFFFFu - static_cast<uint32_t>(slot));
-        if ((low & hi_mask) != (prefix & hi_mask)) continue;
-        atomicAdd(&hist[(low >> sh) & ((1u << width) - 1)], 1u);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        uint32_t acc = 0;
-        for (int dg = (1 << width) - 1; dg >= 0; --dg) {
-          if (acc + hist[dg] >= s_krem) {
-            s_krem -= acc;
-            const uint64_t np_ = prefix | (static_cast<uint64_t>(dg) << sh);
-            s_prefix_lo = static_cast<uint32_t>(np_);
-            s_prefix_hi = static_cast<uint32_t>(np_ >> 32);
-            break;
-          }
-          acc += hist[dg];
+      const uint64_t prefix = s_prefix;
+      if (!from_row) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+          const uint64_t low = v[i] & kLow;
+          if ((low & hi_mask) == prefix) atomicAdd(&hist[(low >> sh) & dmask], 1u);
+        }
+      } else {
+        for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
+          uint32_t key;
+          int32_t q;
+          if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q) || (key >> kSelBinShift) != s.thr_bin) continue;
+          const uint64_t low = low_of(key, static_cast<uint32_t>(slot));
+          if ((low & hi_mask) == prefix) atomicAdd(&hist[(low >> sh) & dmask], 1u);
         }
       }
       __syncthreads();
-      prefix = (static_cast<uint64_t>(s_prefix_hi) << 32) | s_prefix_lo;
+      if (threadIdx.x < 32) pick_digit(hist, sh, &s_rem, &s_prefix, &s_done);
+      __syncthreads();
+      if (s_done) break;
     }
-    // chosen: bin above thr, or in thr with low51 >= prefix (the kr-th largest)
-    for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
-      uint32_t key;
-      int32_t q;
-      if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q)) continue;
-      const uint32_t bin = key >> kSelBinShift;
-      bool take = bin > thr;
-      if (bin == thr) {
-        const uint64_t low = (static_cast<uint64_t>(key & ((1u << kSelBinShift) - 1)) << 32) |
-                             (0xFFFFFFFFu - static_cast<uint32_t>(slot));
-        take = low >= prefix;
+  }
+  // mark the chosen keys of bin thr_bin: low >= the need-th largest
+  const uint64_t cut = s_prefix;
+  if (need > 0) {
+    if (!from_row) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const uint64_t K = v[i];
+        if (all || (K & kLow) >= cut) {
+          const uint32_t slot = 0xFFFFFFFFu - static_cast<uint32_t>(K);
+          atomicOr(&bm[slot >> 5], 1u << (slot & 31));
+        }
       }
-      if (take) {
-        const uint32_t at = atomicAdd(&s_cnt, 1u);
-        if (at < static_cast<uint32_t>(kt)) pos[at] = q;
+    } else {
+      for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
+        uint32_t key;
+        int32_t q;
+        if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q) || (key >> kSelBinShift) != s.thr_bin) continue;
+        if (low_of(key, static_cast<uint32_t>(slot)) >= cut) atomicOr(&bm[slot >> 5], 1u << (slot & 31));
       }
     }
-    __syncthreads();
   }
   __syncthreads();
-  const int kp = pow2_at_least(max(kt, 1));
-  for (int i = kt + threadIdx.x; i < kp; i += blockDim.x) pos[i] = 0x7FFFFFFF;
+  // ascending output: block scan of the bitmap's popcounts
+  const int64_t nw = (ns + 31) / 32;
+  const int64_t per = (nw + blockDim.x - 1) / blockDim.x;
+  const int64_t w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
+  uint32_t cnt = 0;
+  for (int64_t w = w0; w < w1; ++w) cnt += __popc(bm[w]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
-  bitonic_asc_i32(pos, kp);
+  uint32_t off = x - cnt;
+  for (int w = 0; w < warp; ++w) off += warp_tot[w];
+  int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
+                        : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
+  for (int64_t w = w0; w < w1; ++w) {
+    uint32_t word = bm[w];
+    while (word) {
+      const int b = __ffs(word) - 1;
+      word &= word - 1;
+      if (off < kt) out[off] = slot_position(a, row, p, static_cast<uint32_t>(w * 32 + b));
+      ++off;
+    }
+  }
   const int kout = p == 0 ? a.k : a.out_pool_blocks;
-  for (int i = threadIdx.x; i < kout; i += blockDim.x) out[i] = i < kt ? pos[i] : -1;
-  if (p == 1 && threadIdx.x == 0) a.pool_count[row] = kt;
+  for (int i = kt + threadIdx.x; i < kout; i += blockDim.x) out[i] = -1;
+  if (p == 1 && threadIdx.x == 0) a.pool_count[row] = static_cast<int32_t>(kt);
 }
 
 }  // namespace
 
+// Workspace: selection state | candidates | bitmaps | (sideband, when the
+// caller has none)
 size_t topk_workspace_bytes(int rows, int64_t stride, bool have_aux) {
   size_t b = static_cast<size_t>(rows) * 2 * sizeof(SelState);
   b = (b + 255) & ~size_t(255);
   b += static_cast<size_t>(rows) * 2 * kSelCap * 8;
+  const int64_t w0 = (stride + 31) / 32, w1 = ((stride + 7) / 8 + 31) / 32;
+  b += (static_cast<size_t>(rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
   if (!have_aux) b += static_cast<size_t>(rows) * aux_row_bytes(stride);
   return (b + 255) & ~size_t(255);
 }
@@ -399,6 +449,9 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
   size_t off = (static_cast<size_t>(a.rows) * 2 * sizeof(SelState) + 255) & ~size_t(255);
   uint64_t *cand = reinterpret_cast<uint64_t *>(w + off);
   off += static_cast<size_t>(a.rows) * 2 * kSelCap * 8;
+  uint32_t *bitmap = reinterpret_cast<uint32_t *>(w + off);
+  const int64_t w0 = (a.stride + 31) / 32, w1 = ((a.stride + 7) / 8 + 31) / 32;
+  off += (static_cast<size_t>(a.rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
   const int64_t aux_row = aux_row_bytes(a.stride);
   const uint8_t *aux = a.aux;
   if (!aux) {
@@ -411,15 +464,10 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
   const int64_t slots = a.pool ? static_cast<int64_t>(a.pool_blocks) * a.bs : a.stride;
   const int chunks = static_cast<int>((slots + kChunk - 1) / kChunk);
   k_resolve<<<dim3(a.rows, nprob), 256, 0, s>>>(a, aux, aux_row, st);
-  k_collect<<<dim3(chunks > 0 ? chunks : 1, a.rows, nprob), kCollectThreads, 0, s>>>(a, aux, aux_row, st, cand);
-  static bool attr = false;
-  const int smem = kSelCap * 8 + 2048 * 4;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_final, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  k_final<<<dim3(a.rows, nprob), kFinalThreads, smem, s>>>(a, aux, aux_row, st, cand);
+  k_collect<<<dim3(chunks > 0 ? chunks : 1, a.rows, nprob), kCollectThreads, 0, s>>>(a, aux, aux_row, st, cand,
+                                                                                     bitmap);
+  const int smem = kSelCap * 8;
+  k_final<<<dim3(a.rows, nprob), kFinalThreads, smem, s>>>(a, aux, aux_row, st, cand, bitmap);
   return cudaGetLastError();
 }
 
