@@ -102,22 +102,25 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, int32_
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Entry j of the row's list: the k selected cache entries, then the window.
-// kind 0 empty, 1 cache entry, 2 window ring slot, 3 window row of the call.
-__device__ __forceinline__ int entry_src(const AttnArgs &a, int row, int seq, int j, int64_t qpos, int64_t T,
-                                         int64_t ntok, int64_t lin_base, int64_t &src) {
+// The row's entry list: the k selected cache entries padded with empties to
+// kpad = ceil(k / 32) * 32, then the 128 window tokens; chunk c = entries
+// 32c .. 32c + 31.  Split s of S takes chunks s, s + S, s + 2S, ... so every
+// split gets its share of the window.
+// Kind of entry j: 0 empty, 1 cache entry, 2 window ring slot, 3 window row
+// of the call.  `sel` is the raw index of a selected entry (read ahead).
+__device__ __forceinline__ int entry_kind(const AttnArgs &a, int seq, int j, int kpad, int32_t sel, int64_t qpos,
+                                          int64_t T, int64_t ntok, int64_t lin_base, int64_t &src) {
   src = 0;
-  if (j < a.k) {
-    const int32_t s = a.idx[static_cast<size_t>(row) * a.k + j];
-    if (s < 0) return 0;
-    if (s >= T || s >= a.cap) {
+  if (j < kpad) {
+    if (j >= a.k || sel < 0) return 0;
+    if (sel >= T || sel >= a.cap) {
       raise_err(a.err, CSA2_DEVERR_INDEX);
       return 0;
     }
-    src = static_cast<int64_t>(seq) * a.cap + s;
+    src = static_cast<int64_t>(seq) * a.cap + sel;
     return 1;
   }
-  const int64_t tok = qpos - (kWin - 1) + (j - a.k);
+  const int64_t tok = qpos - (kWin - 1) + (j - kpad);
   if (tok < 0 || tok >= ntok || tok > qpos) return 0;
   if (tok >= lin_base) {
     src = tok - lin_base;
@@ -127,8 +130,26 @@ __device__ __forceinline__ int entry_src(const AttnArgs &a, int row, int seq, in
   return 2;
 }
 
+// Raw bytes of one FP4 cache entry held by one producer thread (its quarter).
+struct Fp4Raw {
+  uint2 cw[9];   // code bytes of units q4 + 4i (i < 8) and RoPE unit q4
+  uint4 s0, s1;  // the 32 latent scale bytes
+  uint32_t rsc;  // RoPE scale byte of group q4
+};
+
+__device__ __forceinline__ void load_fp4(const AttnArgs &a, int64_t src, int q4, Fp4Raw &r) {
+  const uint2 *lc = reinterpret_cast<const uint2 *>(a.lat_codes + src * 256);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r.cw[i] = lc[q4 + 4 * i];
+  r.cw[8] = reinterpret_cast<const uint2 *>(a.rope_codes + src * 32)[q4];
+  const uint4 *ls = reinterpret_cast<const uint4 *>(a.lat_scales + src * 32);
+  r.s0 = ls[0];
+  r.s1 = ls[1];
+  r.rsc = a.rope_scales[src * 4 + q4];
+}
+
 template <int HP>
-__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits, int per_split) {
+__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits) {
   constexpr int kCons = HP * 4;         // consumer threads: HP / 8 warps
   constexpr int kDW = 4096 / HP;        // output dims per consumer warp
   constexpr int kNT = kDW / 8;          // n8 tiles per consumer warp
@@ -143,12 +164,11 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   const int64_t T = qpos / a.ratio;
   const int64_t ntok = a.n_tokens[seq];
   const int64_t lin_base = a.lin_base ? *a.lin_base : INT64_MAX;
-  const int L = a.k + kWin;
-  const int e_begin = split * per_split;
-  const int e_end = min(L, e_begin + per_split);
-  const int nchunks = e_begin < e_end ? (e_end - e_begin + kE - 1) / kE : 0;
+  const int kpad = (a.k + kE - 1) / kE * kE;
+  const int total_chunks = (kpad + kWin) / kE;
+  const int nchunks = split < total_chunks ? (total_chunks - split + n_splits - 1) / n_splits : 0;
 
-  // ---- set-up: barriers, dequant table, the query as scaled fp16
+  // ---- set-up: barriers, dequant table
   if (tid == 0) {
     tc::mbar_init(&sm.full[0], kProdThreads);
     tc::mbar_init(&sm.full[1], kProdThreads);
@@ -160,81 +180,50 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     __half2 h = __floats2half2_rn(e2m1_value(i & 15), e2m1_value(i >> 4));
     sm.lut[i] = *reinterpret_cast<uint32_t *>(&h);
   }
-  for (int h = warp; h < HP; h += blockDim.x / 32) {
-    uint4 raw[3];
-    float amax = 0.0f;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk);
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int c = lane + 32 * i;
-      raw[i] = make_uint4(0, 0, 0, 0);
-      if (h < nh && c < kDqk / 8) raw[i] = src[c];
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2)
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k2] << 16)), fabsf(__uint_as_float(w[k2] & 0xFFFF0000u))));
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // |q * 2^-e| < 2^15: inside fp16, exact for every bf16 value >= amax * 2^-24
-    int e = amax > 0.0f ? floor_log2f(amax) - 14 : 0;
-    e = max(e, -110);
-    const float inv = pow2f(-e);
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int c = lane + 32 * i;
-      if (c < kDqk / 8) {
-        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t hv[4];
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[k2] << 16), inv),
-                                         __fmul_rn(__uint_as_float(w[k2] & 0xFFFF0000u), inv));
-          hv[k2] = *reinterpret_cast<uint32_t *>(&t2);
-        }
-        *reinterpret_cast<uint4 *>(&sm.q[h][8 * c]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-      }
-    }
-    if (lane == 0) sm.qf[h] = h < nh ? pow2f(e) * a.sm_scale * kLog2e : 0.0f;
-  }
-  __syncthreads();
+  __syncthreads();  // barriers and table ready
 
   if (tid >= kCons) {
     // ================================================================ producers
     const int pt = tid - kCons;
     const int e = pt >> 2, q4 = pt & 3;
     const uint32_t qmask = 0xFu << (lane & ~3);  // the four lanes of this entry
+    const int32_t *idx_row = a.idx + static_cast<size_t>(row) * a.k;
+    // software pipeline: once chunk c is handed over, the raw bytes of chunk
+    // c+1 and the indices of chunk c+2 are requested; they land while this
+    // producer waits for a free stage
+    auto sel_of = [&](int i) -> int32_t {  // selected index of entry e of local chunk i, or -1
+      const int j = (split + n_splits * i) * kE + e;
+      return j < a.k ? idx_row[j] : -1;
+    };
+    int64_t src = 0;
+    int kind = 0;
+    Fp4Raw raw;
+    int32_t sel_next = -1;
+    if (nchunks > 0) {
+      kind = entry_kind(a, seq, split * kE + e, kpad, sel_of(0), qpos, T, ntok, lin_base, src);
+      if (kind == 1) load_fp4(a, src, q4, raw);
+      if (nchunks > 1) sel_next = sel_of(1);
+    }
     bool dead = false;
     for (int c = 0; c < nchunks; ++c) {
       const int st = c & 1;
       if (c >= 2 && !dead) dead = !wait_warp(&sm.empty[st], ((c - 2) >> 1) & 1, a.err);
       if (!dead) {
-        const int j = e_begin + c * kE + e;
-        int64_t src = 0;
-        const int kind = j < e_end ? entry_src(a, row, seq, j, qpos, T, ntok, lin_base, src) : 0;
         uint4 *dst = reinterpret_cast<uint4 *>(&sm.kv[st][e][0]);  // 16-dim unit u at dst[2u], dst[2u+1]
         float sig = 0.0f;
         if (kind == 1) {
           // FP4 entry: unit u < 32 = latent dims 16u.. (8 code bytes, scale u), u = 32 + q4 the RoPE group q4
-          const uint2 *lc = reinterpret_cast<const uint2 *>(a.lat_codes + src * 256);
-          const uint4 *ls = reinterpret_cast<const uint4 *>(a.lat_scales + src * 32);
-          uint2 cw[9];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cw[i] = lc[q4 + 4 * i];
-          cw[8] = reinterpret_cast<const uint2 *>(a.rope_codes + src * 32)[q4];
-          const uint4 s0 = ls[0], s1 = ls[1];
-          const uint32_t rsc = a.rope_scales[src * 4 + q4];
-          const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          const uint32_t sw[8] = {raw.s0.x, raw.s0.y, raw.s0.z, raw.s0.w, raw.s1.x, raw.s1.y, raw.s1.z, raw.s1.w};
 #pragma unroll
           for (int i = 0; i < 9; ++i) {
             const int u = i < 8 ? q4 + 4 * i : 32 + q4;
-            const uint32_t sb = i < 8 ? (sw[u >> 2] >> (8 * (u & 3))) & 0xFFu : rsc;
+            const uint32_t sb = i < 8 ? (sw[u >> 2] >> (8 * (u & 3))) & 0xFFu : raw.rsc;
             const uint32_t s2 = e4m3x2_to_h2(sb | (sb << 8));
             uint32_t o[8];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-              o[b] = hmul2u(sm.lut[(cw[i].x >> (8 * b)) & 0xFFu], s2);
-              o[4 + b] = hmul2u(sm.lut[(cw[i].y >> (8 * b)) & 0xFFu], s2);
+              o[b] = hmul2u(sm.lut[(raw.cw[i].x >> (8 * b)) & 0xFFu], s2);
+              o[4 + b] = hmul2u(sm.lut[(raw.cw[i].y >> (8 * b)) & 0xFFu], s2);
             }
             dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -316,11 +305,68 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
         if (q4 == 0) sm.sig[st][e] = sig;
       }
       tc::mbar_arrive(&sm.full[st]);
+      if (c + 1 < nchunks) {
+        kind = entry_kind(a, seq, (split + n_splits * (c + 1)) * kE + e, kpad, sel_next, qpos, T, ntok, lin_base,
+                          src);
+        if (kind == 1) load_fp4(a, src, q4, raw);
+        if (c + 2 < nchunks) sel_next = sel_of(c + 2);
+      }
     }
     return;
   }
 
   // ================================================================== consumers
+  // the query: raw bf16 rows into sm.q (one round trip), then in place to fp16
+  // with a power-of-two scale per head: |q * 2^-e| < 2^15, exact for every bf16
+  // value >= amax * 2^-24
+  for (int i = tid; i < HP * (kDqk / 8); i += kCons) {
+    const int h = i / (kDqk / 8), c8 = i % (kDqk / 8);
+    __half *dq = &sm.q[h][8 * c8];
+    if (h < nh) {
+      const uint16_t *gq = a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk + 8 * c8;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dq)), "l"(gq) : "memory");
+    } else {
+      *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+  bar_consumers(kCons);
+  for (int h = warp; h < HP; h += kCons / 32) {
+    uint4 raw[3];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int c8 = lane + 32 * i;
+      raw[i] = c8 < kDqk / 8 ? *reinterpret_cast<const uint4 *>(&sm.q[h][8 * c8]) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2)
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k2] << 16)), fabsf(__uint_as_float(w[k2] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int ex = amax > 0.0f ? floor_log2f(amax) - 14 : 0;
+    ex = max(ex, -110);
+    const float inv = pow2f(-ex);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int c8 = lane + 32 * i;
+      if (c8 < kDqk / 8) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        uint32_t hv[4];
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[k2] << 16), inv),
+                                         __fmul_rn(__uint_as_float(w[k2] & 0xFFFF0000u), inv));
+          hv[k2] = *reinterpret_cast<uint32_t *>(&t2);
+        }
+        *reinterpret_cast<uint4 *>(&sm.q[h][8 * c8]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+      }
+    }
+    if (lane == 0) sm.qf[h] = h < nh ? pow2f(ex) * a.sm_scale * kLog2e : 0.0f;
+  }
+  bar_consumers(kCons);
+
   const int g = lane >> 2, t = lane & 3;
   float o[kMT][kNT][4];
 #pragma unroll
@@ -518,17 +564,16 @@ int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
 // Entry splits per (row, head block): fill the 152 SMs once (one CTA per SM),
 // at least one 32-entry chunk per split.
 int choose_splits(int rows, int heads, int k) {
-  const int L = k + kWin;
   const int ctas = rows * head_blocks(heads);
   int s = 152 / ctas;
-  const int max_s = (L + kE - 1) / kE;
+  const int max_s = ((k + kE - 1) / kE * kE + kWin) / kE;
   if (s > max_s) s = max_s;
   if (s < 1) s = 1;
   return s;
 }
 
 template <int HP>
-cudaError_t launch_hp(const AttnArgs &a, int n_splits, int per, cudaStream_t st) {
+cudaError_t launch_hp(const AttnArgs &a, int n_splits, cudaStream_t st) {
   static bool attr_set = false;
   const int smem = static_cast<int>(sizeof(AttnSmem<HP>));
   if (!attr_set) {
@@ -537,7 +582,7 @@ cudaError_t launch_hp(const AttnArgs &a, int n_splits, int per, cudaStream_t st)
     attr_set = true;
   }
   dim3 grid(n_splits, a.rows, head_blocks(a.heads));
-  k_attn<HP><<<grid, HP * 4 + kProdThreads, smem, st>>>(a, n_splits, per);
+  k_attn<HP><<<grid, HP * 4 + kProdThreads, smem, st>>>(a, n_splits);
   return cudaGetLastError();
 }
 
@@ -553,15 +598,12 @@ cudaError_t launch_attn(const AttnArgs &a0, void *ws, size_t ws_bytes, cudaStrea
   if (a0.rows <= 0) return cudaSuccess;
   AttnArgs a = a0;
   const int n_splits = choose_splits(a.rows, a.heads, a.k);
-  const int L = a.k + kWin;
-  int per = (L + n_splits - 1) / n_splits;
-  per = (per + kE - 1) / kE * kE;
   a.part = static_cast<float *>(ws);
   (void)ws_bytes;
   cudaError_t e;
-  if (a.heads <= 16) e = launch_hp<16>(a, n_splits, per, st);
-  else if (a.heads <= 32) e = launch_hp<32>(a, n_splits, per, st);
-  else e = launch_hp<64>(a, n_splits, per, st);
+  if (a.heads <= 16) e = launch_hp<16>(a, n_splits, st);
+  else if (a.heads <= 32) e = launch_hp<32>(a, n_splits, st);
+  else e = launch_hp<64>(a, n_splits, st);
   if (e != cudaSuccess) return e;
   if (n_splits > 1) k_attn_combine<<<dim3(a.heads, a.rows), 128, 0, st>>>(a, n_splits);
   return cudaGetLastError();

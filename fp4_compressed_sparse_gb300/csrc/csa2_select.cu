@@ -11,20 +11,20 @@
 // every mode); -0 == +0, NaN ranks lowest.  Every K is distinct, so the chosen
 // set never depends on scheduling.
 //
-// Per (row, problem) -- problem 0 is the top-k over the row's slots, problem 1
-// the top blocks by block maximum (FULL rows building a pool):
-//   resolve  one CTA: the 13-bit histogram (from the score kernel's sideband)
-//            gives the threshold bin, where the count from the top reaches k,
-//            and how many keys lie strictly above it
-//   collect  many CTAs: every slot whose key lies above the threshold bin is
-//            chosen outright and marked in a per-row bitmap (one warp ballot per
-//            32 slots writes one word); keys in the threshold bin go to a
-//            candidate list (at most kSelCap; overflow is flagged)
-//   final    one CTA: an exact radix select over the candidates' low 51 key
-//            bits picks the ones still needed and marks them, then a block scan
-//            over the bitmap writes the chosen positions in ascending order
-//            (-1 padded).  After an overflow (a very crowded threshold bin) the
-//            radix select runs over the whole row instead.
+// One 1024-thread CTA per (row, problem) -- problem 0 is the top-k over the
+// row's slots, problem 1 the top blocks by block maximum (FULL rows building a
+// pool) -- and everything in shared memory:
+//   1. the row's 13-bit key histogram (the score kernel's sideband) gives the
+//      threshold bin, where the count from the top reaches k, and how many
+//      keys lie strictly above it;
+//   2. one pass over the row (just written, so mostly from L2): a slot whose
+//      key lies above the threshold bin is chosen outright and marked in a
+//      bitmap (one warp ballot per 32 slots writes one word); keys in the
+//      threshold bin go to a candidate list (at most kSelCap);
+//   3. an exact radix select over the candidates' low 51 key bits marks the
+//      ones still needed (after an overflow of the list it runs over the row);
+//   4. a block scan of the bitmap writes the chosen positions in ascending
+//      order, -1 padded.
 // Slots run in ascending position order in every mode, so the bitmap order is
 // the output order and no sort is needed.
 #include "csa2_internal.cuh"
@@ -32,20 +32,17 @@
 namespace csa2 {
 namespace {
 
-constexpr int kChunk = 4096;  // slots per collect CTA
-constexpr int kCollectThreads = 256;
-constexpr int kFinalThreads = 512;
-
-struct SelState {
-  uint32_t thr_bin;   // the bin where the count from the top reaches k
-  uint32_t above;     // valid keys in bins above thr_bin (all chosen)
-  uint32_t total;     // valid slots
-  uint32_t ncand;     // keys of bin thr_bin appended (may exceed kSelCap)
-  uint32_t overflow;  // 1: ncand > kSelCap
-  uint32_t pad[3];
-};
+constexpr int kChunk = 4096;  // slots per sideband-fill CTA
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int64_t kSmemBitmapWords = 32768;  // rows up to 2^20 slots keep the bitmap in shared memory
 
 __device__ __forceinline__ uint32_t key_of(float f) { return isnan(f) ? 0u : orderable(f); }
+
+// The float whose order key is k (k >= 1; the inverse of orderable()).
+__device__ __forceinline__ float float_of_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 __device__ __forceinline__ int prob_k(const TopkArgs &a, int p) { return p == 0 ? a.k : a.out_pool_blocks; }
 
@@ -133,131 +130,7 @@ __global__ void __launch_bounds__(256) k_fill_aux(TopkArgs a, uint8_t *aux, int6
   }
 }
 
-// ----------------------------------------------------------------------------- resolve
-// grid (rows, problems), 256 threads
-__global__ void __launch_bounds__(256) k_resolve(TopkArgs a, const uint8_t *aux, int64_t aux_row, SelState *st) {
-  __shared__ uint32_t hs[kSelBins];
-  __shared__ uint32_t warp_tot[8];
-  const int row = blockIdx.x, p = blockIdx.y;
-  const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
-  for (int i = threadIdx.x; i < kSelBins / 4; i += blockDim.x) reinterpret_cast<uint4 *>(hs)[i] = h4[i];
-  __syncthreads();
-  // thread t owns the 32 bins kSelBins-1-32t-i, i = 0..31 (thread 0 the top ones);
-  // the rotated index keeps the 32 reads of a step in distinct banks
-  constexpr int per = kSelBins / 256;
-  const int top = kSelBins - 1 - threadIdx.x * per;
-  uint32_t local = 0;
-  for (int i = 0; i < per; ++i) local += hs[top - ((i + threadIdx.x) & (per - 1))];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = local;
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  uint32_t before = 0, total = 0;
-  for (int w = 0; w < 8; ++w) {
-    if (w < warp) before += warp_tot[w];
-    total += warp_tot[w];
-  }
-  const uint32_t above = before + x - local;  // keys in bins above this thread's
-  SelState *s = st + static_cast<size_t>(row) * 2 + p;
-  const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
-  if (total <= k) {
-    // every valid slot is chosen: bin 0 is the threshold bin
-    if (threadIdx.x == 0) *s = SelState{0u, total - hs[0], total, 0u, 0u, {0u, 0u, 0u}};
-    return;
-  }
-  if (above < k && k <= above + local) {
-    uint32_t acc = above;
-    for (int i = 0; i < per; ++i) {
-      const uint32_t bin = top - i;
-      if (acc + hs[bin] >= k) {
-        *s = SelState{bin, acc, total, 0u, 0u, {0u, 0u, 0u}};
-        break;
-      }
-      acc += hs[bin];
-    }
-  }
-}
-
-// ----------------------------------------------------------------------------- collect
-__device__ __forceinline__ uint32_t *row_bitmap(uint32_t *bm, int64_t stride, int row, int p) {
-  const int64_t w0 = (stride + 31) / 32, w1 = ((stride + 7) / 8 + 31) / 32;
-  return bm + static_cast<size_t>(row) * (w0 + w1) + (p ? w0 : 0);
-}
-
-// grid (chunks, rows, problems), 256 threads; thread i of a step handles slot
-// s0 + 256*step + i, so warp w covers one aligned 32-slot bitmap word
-__global__ void __launch_bounds__(kCollectThreads) k_collect(TopkArgs a, const uint8_t *aux, int64_t aux_row,
-                                                             SelState *st, uint64_t *cand, uint32_t *bitmap) {
-  constexpr int kSteps = kChunk / kCollectThreads;
-  const int row = blockIdx.y, p = blockIdx.z;
-  const int64_t ns = n_slots(a, row, p);
-  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kChunk;
-  if (s0 >= ns) return;
-  SelState *s = st + static_cast<size_t>(row) * 2 + p;
-  const uint32_t thr = s->thr_bin;
-  const int64_t T = row_T(a, row);
-  uint64_t *cb = cand + (static_cast<size_t>(row) * 2 + p) * kSelCap;
-  uint32_t *bm = row_bitmap(bitmap, a.stride, row, p);
-  const int lane = threadIdx.x & 31;
-  // all loads of the chunk first (independent, no side effects between them),
-  // then the keys and the ballots
-  float f[kSteps];
-  int32_t pid[kSteps];
-  const float *src = p == 1 ? aux_bmax(aux, aux_row, row) : a.scores + static_cast<size_t>(row) * a.stride;
-  const bool pooled = p == 0 && a.pool != nullptr;
-#pragma unroll
-  for (int i = 0; i < kSteps; ++i) {
-    const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
-    f[i] = slot < ns ? src[slot] : 0.0f;
-    pid[i] = pooled && slot < ns ? a.pool[static_cast<size_t>(row) * a.pool_blocks + slot / a.bs] : 0;
-  }
-  uint32_t key[kSteps];
-  uint32_t valid = 0;
-#pragma unroll
-  for (int i = 0; i < kSteps; ++i) {
-    const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
-    bool ok = slot < ns;
-    if (pooled) ok = ok && pid[i] >= 0 && static_cast<int64_t>(pid[i]) * a.bs + slot % a.bs < T;
-    key[i] = key_of(f[i]);
-    if (ok) valid |= 1u << i;
-  }
-  if (p == 0) {
-#pragma unroll
-    for (int i = 0; i < kSteps; ++i)
-      if (((valid >> i) & 1u) && isnan(f[i])) raise_err(a.err, CSA2_DEVERR_NAN);
-  }
-#pragma unroll
-  for (int i = 0; i < kSteps; ++i) {
-    const int64_t slot = s0 + static_cast<int64_t>(i) * kCollectThreads + threadIdx.x;
-    const int64_t wbase = slot - lane;
-    if (wbase >= ns) break;  // warp-uniform
-    const bool ok = (valid >> i) & 1u;
-    const uint32_t bin = key[i] >> kSelBinShift;
-    const uint32_t word = __ballot_sync(0xffffffffu, ok && bin > thr);
-    if (lane == 0) bm[wbase >> 5] = word;
-    const bool want = ok && bin == thr;
-    const uint32_t mask = __ballot_sync(0xffffffffu, want);
-    if (mask) {
-      const int leader = __ffs(mask) - 1;
-      uint32_t base = 0;
-      if (lane == leader) base = atomicAdd(&s->ncand, static_cast<uint32_t>(__popc(mask)));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      if (want) {
-        const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
-        if (at < kSelCap)
-          cb[at] = (static_cast<uint64_t>(key[i]) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(slot));
-        else
-          s->overflow = 1;
-      }
-    }
-  }
-}
-
-// ----------------------------------------------------------------------------- final
+// ----------------------------------------------------------------------------- select
 __device__ __forceinline__ int32_t slot_position(const TopkArgs &a, int row, int p, uint32_t slot) {
   if (p == 1 || !a.pool) return static_cast<int32_t>(slot);
   const int32_t pid = a.pool[static_cast<size_t>(row) * a.pool_blocks + slot / a.bs];
@@ -270,9 +143,43 @@ __device__ __forceinline__ uint64_t low_of(uint32_t key, uint32_t slot) {
   return (static_cast<uint64_t>(key & ((1u << kSelBinShift) - 1)) << 32) | (0xFFFFFFFFu - slot);
 }
 
-// One radix digit of the select: hist holds the counts of the digit values
-// among the keys that match the prefix so far; find the digit where the count
-// from the top reaches *rem, extend the prefix, reduce *rem.  Warp 0 only.
+__device__ __forceinline__ uint32_t *row_bitmap(uint32_t *bm, int64_t stride, int row, int p) {
+  const int64_t w0 = (stride + 31) / 32, w1 = ((stride + 7) / 8 + 31) / 32;
+  return bm + static_cast<size_t>(row) * (w0 + w1) + (p ? w0 : 0);
+}
+
+// Block-wide exclusive scan of one value per thread; *total = the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = lane < kSelWarps ? warp_tot[lane] : 0u, inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane < kSelWarps) warp_tot[lane] = inc - t;  // exclusive warp offsets
+    if (lane == kSelWarps - 1) warp_tot[kSelWarps] = inc;
+  }
+  __syncthreads();
+  const uint32_t r = warp_tot[warp] + x - v;
+  *total = warp_tot[kSelWarps];
+  __syncthreads();  // warp_tot may be reused right away
+  return r;
+}
+
+// One radix digit of the select (warp 0): hist holds the counts of the digit
+// values among the keys matching the prefix so far; find the digit where the
+// count from the top reaches *rem, extend the prefix, reduce *rem; *done when
+// every key under the new prefix is needed.
 __device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_t *rem, uint64_t *prefix,
                                            uint32_t *done) {
   const int lane = threadIdx.x & 31;
@@ -293,7 +200,6 @@ __device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_
       if (acc + hist[dg] >= r) {
         *rem = r - acc;
         *prefix |= static_cast<uint64_t>(dg) << sh;
-        // every key under this prefix is needed: the prefix (lower bits 0) is the cut
         if (hist[dg] == r - acc) *done = 1;
         break;
       }
@@ -302,108 +208,318 @@ __device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_
   }
 }
 
-// grid (rows, problems), kFinalThreads threads; dynamic smem: kSelCap u64
-__global__ void __launch_bounds__(kFinalThreads) k_final(TopkArgs a, const uint8_t *aux, int64_t aux_row,
-                                                         const SelState *st, const uint64_t *cand,
-                                                         uint32_t *bitmap) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint64_t *v = reinterpret_cast<uint64_t *>(smem);
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t s_rem, s_done;
-  __shared__ uint64_t s_prefix;
-  __shared__ uint32_t warp_tot[kFinalThreads / 32];
+struct SelSmem {
+  uint32_t hist[kSelBins];
+  uint64_t cand[kSelCap];
+  uint32_t warp_tot[kSelWarps + 1];
+  uint32_t dhist[256];
+  uint64_t prefix;
+  uint32_t thr, above, total, ncand, overflow, rem, done;
+};
+
+// Key of slot `slot` (valid only when *ok): reads of one warp step go to 32
+// consecutive slots.
+__device__ __forceinline__ float slot_value(const TopkArgs &a, const float *src, const int32_t *prow, int p,
+                                            int64_t slot, int64_t ns, int64_t T, bool &ok) {
+  ok = slot < ns;
+  if (!ok) return 0.0f;
+  if (p == 0 && a.pool) {
+    const int32_t pid = prow[slot / a.bs];
+    ok = pid >= 0 && static_cast<int64_t>(pid) * a.bs + slot % a.bs < T;
+  }
+  return src[slot];
+}
+
+// grid (rows, problems), kSelThreads; dynamic smem: SelSmem (+ the bitmap when it fits)
+__global__ void __launch_bounds__(kSelThreads, 1) k_select(TopkArgs a, const uint8_t *aux, int64_t aux_row,
+                                                           uint32_t *bitmap_g, int bitmap_in_smem) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, p = blockIdx.y;
-  const SelState s = st[static_cast<size_t>(row) * 2 + p];
-  const int k = prob_k(a, p);
-  const uint32_t kt = min(static_cast<uint32_t>(k), s.total);  // positions to output
-  const uint32_t need = kt - s.above;                           // still to choose from bin thr_bin
   const int64_t ns = n_slots(a, row, p);
   const int64_t T = row_T(a, row);
-  uint32_t *bm = row_bitmap(bitmap, a.stride, row, p);
-  const int n = static_cast<int>(min(s.ncand, static_cast<uint32_t>(kSelCap)));
-  const bool from_row = s.overflow != 0;  // the candidates did not all fit: select over the row
+  const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
+  const int64_t nw = (ns + 31) / 32;
+  uint32_t *bm = bitmap_in_smem ? reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem))
+                                : row_bitmap(bitmap_g, a.stride, row, p);
+  const float *src = p == 1 ? aux_bmax(aux, aux_row, row) : a.scores + static_cast<size_t>(row) * a.stride;
+  const int32_t *prow = a.pool ? a.pool + static_cast<size_t>(row) * a.pool_blocks : nullptr;
 
-  if (!from_row) {
-    const uint64_t *cb = cand + (static_cast<size_t>(row) * 2 + p) * kSelCap;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) v[i] = cb[i];
+  // the first batch of the streaming pass does not depend on the threshold:
+  // request it now (FULL rows and block maxima)
+  constexpr int kFB = 32;  // words per warp per batch in the fast pass
+  const bool plain = p == 1 || a.pool == nullptr;
+  const uint32_t nwu = static_cast<uint32_t>(nw), nsu = static_cast<uint32_t>(ns);
+  float fb[kFB];
+  if (plain) {
+#pragma unroll
+    for (int b = 0; b < kFB; ++b) {
+      const uint32_t slot = (static_cast<uint32_t>(warp) * kFB + b) * 32 + lane;
+      fb[b] = slot < nsu ? src[slot] : __uint_as_float(0x7FC00000u);
+    }
   }
-  if (threadIdx.x == 0) {
-    s_rem = need;
-    s_prefix = 0;
-    s_done = 0;
+
+  // ---- 1. threshold bin from the histogram
+  {
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
+    for (int i = tid; i < kSelBins / 4; i += kSelThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
+    if (tid == 0) {
+      sm.ncand = 0;
+      sm.overflow = 0;
+      sm.rem = 0;
+      sm.done = 0;
+      sm.prefix = 0;
+    }
+    __syncthreads();
+    // thread t owns the 8 bins kSelBins-1-8t-i (thread 0 the top ones)
+    constexpr int per = kSelBins / kSelThreads;
+    const int top = kSelBins - 1 - tid * per;
+    uint32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) local += sm.hist[top - ((i + tid) & (per - 1))];
+    uint32_t total;
+    const uint32_t above = block_excl_scan(local, sm.warp_tot, &total);
+    if (total <= k) {
+      if (tid == 0) {  // every valid slot is chosen: bin 0 is the threshold bin
+        sm.thr = 0;
+        sm.above = total - sm.hist[0];
+        sm.total = total;
+      }
+    } else if (above < k && k <= above + local) {
+      uint32_t acc = above;
+      for (int i = 0; i < per; ++i) {
+        const uint32_t bin = top - i;
+        if (acc + sm.hist[bin] >= k) {
+          sm.thr = bin;
+          sm.above = acc;
+          sm.total = total;
+          break;
+        }
+        acc += sm.hist[bin];
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  // exact select of the need-th largest low key among bin thr_bin: 8-bit digits
-  // over bits 50..3, then bits 2..0
+  const uint32_t thr = sm.thr;
+  const uint32_t kt = min(k, sm.total);
+  const uint32_t need = kt - sm.above;
+
+  // ---- 2. one pass: bitmap words of the keys above the bin, candidates in it
+  if (plain && thr > 0) {
+    // order keys are monotone in the float value: "above the bin" is f > hi and
+    // "in the bin" is lo <= f <= hi (exact, -0 == +0; NaN is neither, like its
+    // key 0 when the threshold bin is above 0); invalid slots read as NaN
+    const float lo = float_of_key(thr << kSelBinShift);
+    const float hi = float_of_key(((thr + 1) << kSelBinShift) - 1);
+    for (uint32_t w0 = static_cast<uint32_t>(warp) * kFB; w0 < nwu; w0 += kSelWarps * kFB) {
+      if (w0 != static_cast<uint32_t>(warp) * kFB) {
+#pragma unroll
+        for (int b = 0; b < kFB; ++b) {
+          const uint32_t slot = (w0 + b) * 32 + lane;
+          fb[b] = slot < nsu ? src[slot] : __uint_as_float(0x7FC00000u);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kFB; ++b) {
+        const uint32_t w = w0 + b;
+        if (w >= nwu) break;  // warp-uniform
+        const float f = fb[b];
+        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && w * 32 + lane < nsu)) {
+          if (isnan(f) && w * 32 + lane < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
+        }
+        const uint32_t word = __ballot_sync(0xffffffffu, f > hi);
+        if (lane == 0) bm[w] = word;
+        const bool want = f >= lo && f <= hi;
+        const uint32_t mask = __ballot_sync(0xffffffffu, want);
+        if (mask) {
+          const int leader = __ffs(mask) - 1;
+          uint32_t base = 0;
+          if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          if (want) {
+            const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
+            const uint32_t slot = w * 32 + lane;
+            if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot);
+            else sm.overflow = 1;
+          }
+        }
+      }
+    }
+    if (tid == 0) sm.rem = need;
+    __syncthreads();
+  } else {
+    // vector path: lane l of a warp step takes slots 4l..4l+3 of 128; rows of
+    // a whole number of float4 (or the padded block maxima) only
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0 && (p == 1 || (a.stride & 3) == 0);
+    if (vec) {
+      constexpr int kB = 4;  // float4 in flight per lane
+      const int64_t nsteps = (ns + 127) / 128;
+      for (int64_t s0 = static_cast<int64_t>(warp) * kB; s0 < nsteps; s0 += static_cast<int64_t>(kSelWarps) * kB) {
+        float4 f[kB];
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const int64_t slot = (s0 + b) * 128 + 4 * lane;
+          f[b] = slot < ns ? *reinterpret_cast<const float4 *>(src + slot) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const int64_t stp = s0 + b;
+          if (stp >= nsteps) break;  // warp-uniform
+          const int64_t slot0 = stp * 128 + 4 * lane;
+          const float v[4] = {f[b].x, f[b].y, f[b].z, f[b].w};
+          uint32_t above = 0, candm = 0, key[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int64_t slot = slot0 + e;
+            bool ok = slot < ns;
+            if (ok && p == 0 && a.pool) {
+              const int32_t pid = prow[slot / a.bs];
+              ok = pid >= 0 && static_cast<int64_t>(pid) * a.bs + slot % a.bs < T;
+            }
+            key[e] = key_of(v[e]);
+            if (ok) {
+              if (p == 0 && isnan(v[e])) raise_err(a.err, CSA2_DEVERR_NAN);
+              const uint32_t bin = key[e] >> kSelBinShift;
+              if (bin > thr) above |= 1u << e;
+              if (bin == thr) candm |= 1u << e;
+            }
+          }
+          // word j of the step = slots 32j..32j+31 = lanes 8j..8j+7
+          uint32_t wv = above << (4 * (lane & 7));
+          wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+          wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+          wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+          const int64_t wi = stp * 4 + (lane >> 3);
+          if ((lane & 7) == 0 && wi < nw) bm[wi] = wv;
+          if (__any_sync(0xffffffffu, candm != 0)) {
+            const uint32_t c = __popc(candm);
+            uint32_t inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+              if (lane >= o) inc += y;
+            }
+            uint32_t base = 0;
+            if (lane == 31) base = atomicAdd(&sm.ncand, inc);
+            base = __shfl_sync(0xffffffffu, base, 31);
+            uint32_t at = base + inc - c;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if ((candm >> e) & 1u) {
+                const uint32_t slot = static_cast<uint32_t>(slot0 + e);
+                if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(key[e]) << 32) | (0xFFFFFFFFu - slot);
+                else sm.overflow = 1;
+                ++at;
+              }
+          }
+        }
+      }
+    } else {
+      constexpr int kBatch = 8;  // words in flight per warp
+      for (int64_t w0 = static_cast<int64_t>(warp) * kBatch; w0 < nw;
+           w0 += static_cast<int64_t>(kSelWarps) * kBatch) {
+        float f[kBatch];
+        bool ok[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) f[b] = slot_value(a, src, prow, p, (w0 + b) * 32 + lane, ns, T, ok[b]);
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int64_t w = w0 + b;
+          if (w >= nw) break;  // warp-uniform
+          if (p == 0 && ok[b] && isnan(f[b])) raise_err(a.err, CSA2_DEVERR_NAN);
+          const uint32_t key = key_of(f[b]);
+          const uint32_t bin = key >> kSelBinShift;
+          const uint32_t word = __ballot_sync(0xffffffffu, ok[b] && bin > thr);
+          if (lane == 0) bm[w] = word;
+          const bool want = ok[b] && bin == thr;
+          const uint32_t mask = __ballot_sync(0xffffffffu, want);
+          if (mask) {
+            const int leader = __ffs(mask) - 1;
+            uint32_t base = 0;
+            if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
+            base = __shfl_sync(0xffffffffu, base, leader);
+            if (want) {
+              const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
+              const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
+              if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - slot);
+              else sm.overflow = 1;
+            }
+          }
+        }
+      }
+    }
+    if (tid == 0) sm.rem = need;
+    __syncthreads();
+  }
+
+  // ---- 3. exact select of the need-th largest low key in the bin: 8-bit
+  // digits over bits 50..3, then bits 2..0
+  const bool from_row = sm.overflow != 0;
+  const int n = static_cast<int>(min(sm.ncand, static_cast<uint32_t>(kSelCap)));
   const bool all = !from_row && need == static_cast<uint32_t>(n);
   if (need > 0 && !all) {
     for (int d = 0; d < 7; ++d) {
       const int sh = d < 6 ? 43 - 8 * d : 0;
       const uint32_t dmask = d < 6 ? 0xFFu : 0x7u;
       const uint64_t hi_mask = kLow & ~((1ull << (sh + (d < 6 ? 8 : 3))) - 1);
-      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      for (int i = tid; i < 256; i += kSelThreads) sm.dhist[i] = 0;
       __syncthreads();
-      const uint64_t prefix = s_prefix;
+      const uint64_t prefix = sm.prefix;
       if (!from_row) {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-          const uint64_t low = v[i] & kLow;
-          if ((low & hi_mask) == prefix) atomicAdd(&hist[(low >> sh) & dmask], 1u);
+        for (int i = tid; i < n; i += kSelThreads) {
+          const uint64_t low = sm.cand[i] & kLow;
+          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
         }
       } else {
-        for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
-          uint32_t key;
-          int32_t q;
-          if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q) || (key >> kSelBinShift) != s.thr_bin) continue;
+        for (int64_t slot = tid; slot < ns; slot += kSelThreads) {
+          bool ok;
+          const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+          const uint32_t key = key_of(f);
+          if (!ok || (key >> kSelBinShift) != thr) continue;
           const uint64_t low = low_of(key, static_cast<uint32_t>(slot));
-          if ((low & hi_mask) == prefix) atomicAdd(&hist[(low >> sh) & dmask], 1u);
+          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
         }
       }
       __syncthreads();
-      if (threadIdx.x < 32) pick_digit(hist, sh, &s_rem, &s_prefix, &s_done);
+      if (warp == 0) pick_digit(sm.dhist, sh, &sm.rem, &sm.prefix, &sm.done);
       __syncthreads();
-      if (s_done) break;
+      if (sm.done) break;
     }
   }
-  // mark the chosen keys of bin thr_bin: low >= the need-th largest
-  const uint64_t cut = s_prefix;
+  // mark the chosen keys of the bin: low >= the need-th largest
+  const uint64_t cut = sm.prefix;
   if (need > 0) {
     if (!from_row) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
-        const uint64_t K = v[i];
+      for (int i = tid; i < n; i += kSelThreads) {
+        const uint64_t K = sm.cand[i];
         if (all || (K & kLow) >= cut) {
           const uint32_t slot = 0xFFFFFFFFu - static_cast<uint32_t>(K);
           atomicOr(&bm[slot >> 5], 1u << (slot & 31));
         }
       }
     } else {
-      for (int64_t slot = threadIdx.x; slot < ns; slot += blockDim.x) {
-        uint32_t key;
-        int32_t q;
-        if (!slot_key(a, aux, aux_row, row, p, slot, T, key, q) || (key >> kSelBinShift) != s.thr_bin) continue;
+      for (int64_t slot = tid; slot < ns; slot += kSelThreads) {
+        bool ok;
+        const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+        const uint32_t key = key_of(f);
+        if (!ok || (key >> kSelBinShift) != thr) continue;
         if (low_of(key, static_cast<uint32_t>(slot)) >= cut) atomicOr(&bm[slot >> 5], 1u << (slot & 31));
       }
     }
   }
   __syncthreads();
-  // ascending output: block scan of the bitmap's popcounts
-  const int64_t nw = (ns + 31) / 32;
-  const int64_t per = (nw + blockDim.x - 1) / blockDim.x;
-  const int64_t w0 = threadIdx.x * per, w1 = min(nw, w0 + per);
+
+  // ---- 4. ascending output: block scan of the bitmap's popcounts
+  const int64_t per = (nw + kSelThreads - 1) / kSelThreads;
+  const int64_t wb = tid * per, we = min(nw, wb + per);
   uint32_t cnt = 0;
-  for (int64_t w = w0; w < w1; ++w) cnt += __popc(bm[w]);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = cnt;
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  uint32_t off = x - cnt;
-  for (int w = 0; w < warp; ++w) off += warp_tot[w];
+  for (int64_t w = wb; w < we; ++w) cnt += __popc(bm[w]);
+  uint32_t tot;
+  uint32_t off = block_excl_scan(cnt, sm.warp_tot, &tot);
   int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
                         : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
-  for (int64_t w = w0; w < w1; ++w) {
+  for (int64_t w = wb; w < we; ++w) {
     uint32_t word = bm[w];
     while (word) {
       const int b = __ffs(word) - 1;
@@ -413,20 +529,17 @@ __global__ void __launch_bounds__(kFinalThreads) k_final(TopkArgs a, const uint8
     }
   }
   const int kout = p == 0 ? a.k : a.out_pool_blocks;
-  for (int i = kt + threadIdx.x; i < kout; i += blockDim.x) out[i] = -1;
-  if (p == 1 && threadIdx.x == 0) a.pool_count[row] = static_cast<int32_t>(kt);
+  for (int i = kt + tid; i < kout; i += kSelThreads) out[i] = -1;
+  if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
 }
 
 }  // namespace
 
-// Workspace: selection state | candidates | bitmaps | (sideband, when the
-// caller has none)
+// Workspace: bitmaps (used when a row has more than 2^20 slots) | the
+// sideband, when the caller has none
 size_t topk_workspace_bytes(int rows, int64_t stride, bool have_aux) {
-  size_t b = static_cast<size_t>(rows) * 2 * sizeof(SelState);
-  b = (b + 255) & ~size_t(255);
-  b += static_cast<size_t>(rows) * 2 * kSelCap * 8;
   const int64_t w0 = (stride + 31) / 32, w1 = ((stride + 7) / 8 + 31) / 32;
-  b += (static_cast<size_t>(rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
+  size_t b = (static_cast<size_t>(rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
   if (!have_aux) b += static_cast<size_t>(rows) * aux_row_bytes(stride);
   return (b + 255) & ~size_t(255);
 }
@@ -445,13 +558,9 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
   if (a0.rows <= 0) return cudaSuccess;
   TopkArgs a = a0;
   uint8_t *w = static_cast<uint8_t *>(ws);
-  SelState *st = reinterpret_cast<SelState *>(w);
-  size_t off = (static_cast<size_t>(a.rows) * 2 * sizeof(SelState) + 255) & ~size_t(255);
-  uint64_t *cand = reinterpret_cast<uint64_t *>(w + off);
-  off += static_cast<size_t>(a.rows) * 2 * kSelCap * 8;
-  uint32_t *bitmap = reinterpret_cast<uint32_t *>(w + off);
+  uint32_t *bitmap = reinterpret_cast<uint32_t *>(w);
   const int64_t w0 = (a.stride + 31) / 32, w1 = ((a.stride + 7) / 8 + 31) / 32;
-  off += (static_cast<size_t>(a.rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
+  const size_t off = (static_cast<size_t>(a.rows) * (w0 + w1) * 4 + 255) & ~size_t(255);
   const int64_t aux_row = aux_row_bytes(a.stride);
   const uint8_t *aux = a.aux;
   if (!aux) {
@@ -461,13 +570,15 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
     aux = own;
   }
   const int nprob = (!a.pool && a.out_pool_blocks > 0) ? 2 : 1;
-  const int64_t slots = a.pool ? static_cast<int64_t>(a.pool_blocks) * a.bs : a.stride;
-  const int chunks = static_cast<int>((slots + kChunk - 1) / kChunk);
-  k_resolve<<<dim3(a.rows, nprob), 256, 0, s>>>(a, aux, aux_row, st);
-  k_collect<<<dim3(chunks > 0 ? chunks : 1, a.rows, nprob), kCollectThreads, 0, s>>>(a, aux, aux_row, st, cand,
-                                                                                     bitmap);
-  const int smem = kSelCap * 8;
-  k_final<<<dim3(a.rows, nprob), kFinalThreads, smem, s>>>(a, aux, aux_row, st, cand, bitmap);
+  const int in_smem = w0 <= kSmemBitmapWords ? 1 : 0;
+  const int smem = static_cast<int>(sizeof(SelSmem) + (in_smem ? w0 * 4 : 0));
+  static int attr = 0;
+  if (smem > attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = smem;
+  }
+  k_select<<<dim3(a.rows, nprob), kSelThreads, smem, s>>>(a, aux, aux_row, bitmap, in_smem);
   return cudaGetLastError();
 }
 

@@ -199,6 +199,7 @@ def test_reindex_pool_bitexact(orc):
     (1, 9000, 100, 64),        # one value: every score ties, lowest positions win
     (0, 70000, 2048, 2048),    # continuous scores, k and pool at their maxima
     (3, 4000, 2048, 2048),     # fewer visible entries than k: everything is chosen
+    (2, 5001, 64, 100),        # an odd row stride (unaligned rows take the scalar pass)
 ])
 def test_topk_crowded_bins_against_oracle(orc, levels, T, k, nblk):
     """Scores written directly (not from the indexer): heavy ties and crowded
