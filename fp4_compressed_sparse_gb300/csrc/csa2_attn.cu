@@ -20,9 +20,11 @@
 //                       fp32 O tile in registers
 // The query is held as fp16 with a power-of-two scale per head (exact for bf16
 // values within 2^24 of the head's maximum).  Stage handover uses mbarriers
-// with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  Splits write
-// unnormalised partials (O, m, l) that a combine kernel merges (flash-decoding
-// LSE merge) and finishes with the sink.
+// with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  The splits of a
+// row are one thread-block cluster: each keeps its unnormalised (O, m, l) in
+// shared memory and, after a cluster barrier, merges a slice of the heads from
+// its peers' shared memory (flash-decoding LSE merge, then the sink) -- no
+// global partials and no second kernel.
 #include <cuda_fp16.h>
 
 #include "csa2_internal.cuh"
@@ -90,7 +92,42 @@ __device__ __forceinline__ uint32_t h2_splat(float v) {
   __half2 h = __float2half2_rn(v);
   return *reinterpret_cast<uint32_t *>(&h);
 }
+constexpr int kMaxSplits = 8;  // splits of a row = one portable thread-block cluster
+
+// every non-exited thread of the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// a float / float4 at the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
+  uint32_t r;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem4(const float *p, uint32_t rank) {
+  uint32_t r;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(r)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void bar_consumers(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
+// consumer barrier returning the AND of v over the consumer threads
+__device__ __forceinline__ int bar_consumers_and(int n, int v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v), "r"(n)
+      : "memory");
+  return r;
+}
 
 // Warp-uniform bounded wait on an mbarrier phase.
 __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, int32_t *err) {
@@ -312,6 +349,10 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
         if (c + 2 < nchunks) sel_next = sel_of(c + 2);
       }
     }
+    if (n_splits > 1) {  // the consumers' two cluster barriers, matched here
+      cluster_sync();
+      cluster_sync();
+    }
     return;
   }
 
@@ -480,9 +521,11 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     sm.fin[sh][0] = m_run;
     sm.fin[sh][1] = l_run;
   }
-  bar_consumers(kCons);
-  if (dead) return;
+  // a wait that ran out in any consumer warp: the CTA's result is void (the
+  // error bit is raised); it still takes part in every barrier below
+  const int alive = bar_consumers_and(kCons, dead ? 0 : 1);
   if (n_splits == 1) {
+    if (!alive) return;
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
@@ -506,68 +549,83 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
               make_float2(o[mt][nt][2 * r] * inv, o[mt][nt][2 * r + 1] * inv);
         if (warp == 0 && t == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
       }
-  } else {
-    const size_t base = (static_cast<size_t>(row) * n_splits + split) * a.heads;
-    float *po = a.part;                                                              // [rows][splits][H][512]
-    float *pml = a.part + static_cast<size_t>(a.rows) * n_splits * a.heads * kLat;  // [rows][splits][H][2]
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int hl = 16 * mt + g + 8 * r;
-        if (hl >= nh) continue;
-        const int h = hbase + hl;
-        float *out = po + (base + h) * kLat + d0;
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          *reinterpret_cast<float2 *>(out + 8 * nt + 2 * t) = make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
-        if (warp == 0 && t == 0)
-          *reinterpret_cast<float2 *>(pml + (base + h) * 2) = make_float2(sm.fin[hl][0], sm.fin[hl][1]);
-      }
+    return;
   }
-}
-
-// LSE merge of the split partials: grid (H, rows), 128 threads x 4 dims.
-__global__ void __launch_bounds__(128) k_attn_combine(AttnArgs a, int n_splits) {
-  const int h = blockIdx.x, row = blockIdx.y, H = a.heads;
-  const float *po = a.part;
-  const float *pml = a.part + static_cast<size_t>(a.rows) * n_splits * H * kLat;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, pml[((static_cast<size_t>(row) * n_splits + s) * H + h) * 2]);
-  const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-  M = fmaxf(M, s2);
-  float L = 0.0f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const size_t base = (static_cast<size_t>(row) * n_splits + s) * H + h;
-      const float m = pml[base * 2], l = pml[base * 2 + 1];
-      if (m == -INFINITY) continue;
-      const float f = exp2f(m - M);
-      L += l * f;
-      const float4 v = reinterpret_cast<const float4 *>(po + base * kLat)[threadIdx.x];
-      acc.x += v.x * f;
-      acc.y += v.y * f;
-      acc.z += v.z * f;
-      acc.w += v.w * f;
+  // ---- the row's splits form one thread-block cluster: each CTA leaves its
+  // unnormalised O (fp32) and (m, l) in its own shared memory, then CTA `split`
+  // merges heads split, split + S, ... from its peers' shared memory
+  // (flash-decoding LSE merge, then the sink)
+  float *osm = reinterpret_cast<float *>(&sm.q[0][0]);  // [HP][512]: the query and the ring are done with
+  static_assert(sizeof(float) * HP * kLat <= sizeof(sm.q) + sizeof(sm.kv), "partial O does not fit");
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int hl = 16 * mt + g + 8 * r;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+        *reinterpret_cast<float2 *>(osm + hl * kLat + d0 + 8 * nt + 2 * t) =
+            make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
     }
-    if (a.sink) L += exp2f(s2 - M);
+  if (!alive && sq == 0) {  // contribute nothing
+    sm.fin[sh][0] = -INFINITY;
+    sm.fin[sh][1] = 0.0f;
   }
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(row) * H + h) * kLat)[threadIdx.x] =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (threadIdx.x == 0) a.lse[static_cast<size_t>(row) * H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  cluster_sync();
+  for (int hl = split + n_splits * warp; hl < nh; hl += n_splits * (kCons / 32)) {
+    const int h = hbase + hl;
+    // lane s < n_splits holds split s's (m, l)
+    float ms = -INFINITY, ls = 0.0f;
+    if (lane < n_splits) {
+      ms = ld_dsmem(&sm.fin[hl][0], lane);
+      ls = ld_dsmem(&sm.fin[hl][1], lane);
+    }
+    float M = ms;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
+    M = fmaxf(M, s2);
+    const float f = (M == -INFINITY || ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+    float L = ls * f;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    if (a.sink && M != -INFINITY) L += exp2f(s2 - M);
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    float fs[kMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) fs[sp] = __shfl_sync(0xffffffffu, f, sp) * inv;
+    float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat;
+#pragma unroll
+    for (int c = 0; c < kLat / 128; ++c) {
+      const int d = 128 * c + 4 * lane;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        if (sp < n_splits && fs[sp] != 0.0f) {
+          const float4 v = ld_dsmem4(osm + hl * kLat + d, sp);
+          acc.x += v.x * fs[sp];
+          acc.y += v.y * fs[sp];
+          acc.z += v.z * fs[sp];
+          acc.w += v.w * fs[sp];
+        }
+      }
+      *reinterpret_cast<float4 *>(out + d) = acc;
+    }
+    if (lane == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
 int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
 
 // Entry splits per (row, head block): fill the 152 SMs once (one CTA per SM),
-// at least one 32-entry chunk per split.
+// at least one 32-entry chunk per split, at most one portable cluster (8).
 int choose_splits(int rows, int heads, int k) {
   const int ctas = rows * head_blocks(heads);
   int s = 152 / ctas;
   const int max_s = ((k + kE - 1) / kE * kE + kWin) / kE;
   if (s > max_s) s = max_s;
+  if (s > kMaxSplits) s = kMaxSplits;
   if (s < 1) s = 1;
   return s;
 }
@@ -581,32 +639,39 @@ cudaError_t launch_hp(const AttnArgs &a, int n_splits, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(n_splits, a.rows, head_blocks(a.heads));
-  k_attn<HP><<<grid, HP * 4 + kProdThreads, smem, st>>>(a, n_splits);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_splits, a.rows, head_blocks(a.heads));
+  cfg.blockDim = dim3(HP * 4 + kProdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n_splits;  // the row's splits: one cluster
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_splits);
 }
 
 }  // namespace
 
+// The splits merge through distributed shared memory: no workspace.
 size_t attn_workspace_bytes(int rows, int heads, int k) {
-  const int s = choose_splits(rows, heads, k);
-  if (s == 1) return 256;
-  return static_cast<size_t>(rows) * s * heads * (kLat + 2) * sizeof(float) + 256;
+  (void)rows;
+  (void)heads;
+  (void)k;
+  return 256;
 }
 
 cudaError_t launch_attn(const AttnArgs &a0, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (a0.rows <= 0) return cudaSuccess;
-  AttnArgs a = a0;
-  const int n_splits = choose_splits(a.rows, a.heads, a.k);
-  a.part = static_cast<float *>(ws);
+  const int n_splits = choose_splits(a0.rows, a0.heads, a0.k);
+  (void)ws;
   (void)ws_bytes;
-  cudaError_t e;
-  if (a.heads <= 16) e = launch_hp<16>(a, n_splits, st);
-  else if (a.heads <= 32) e = launch_hp<32>(a, n_splits, st);
-  else e = launch_hp<64>(a, n_splits, st);
-  if (e != cudaSuccess) return e;
-  if (n_splits > 1) k_attn_combine<<<dim3(a.heads, a.rows), 128, 0, st>>>(a, n_splits);
-  return cudaGetLastError();
+  if (a0.heads <= 16) return launch_hp<16>(a0, n_splits, st);
+  if (a0.heads <= 32) return launch_hp<32>(a0, n_splits, st);
+  return launch_hp<64>(a0, n_splits, st);
 }
 
 }  // namespace csa2

@@ -90,7 +90,6 @@ struct AttnArgs {
   const float *sink;          // [H] or nullptr
   float sm_scale;
   float *out, *lse;
-  float *part;                // split partials
   int32_t *err;
 };
 size_t attn_workspace_bytes(int rows, int heads, int k);

@@ -16,13 +16,17 @@
 // acc = fma(w_h, max(d_h, +0), acc).
 //
 // Persistent CTA per SM, warp-specialised:
-//   warp 0      producer: bulk copies of the key tiles (8 KB codes + 512 B
-//               scales, already stored in the MMA operand layout) into an
-//               8-stage ring; Reindex (POOL) tiles are gathered by the warp;
-//               the per-row query operand goes to one of two B slots
-//   warp 1      MMA issuer: scale factors to TMEM (tcgen05.cp), two MMAs,
-//               commits that free the stage and hand the accumulator over
-//   warps 2..13 epilogue: three TMEM accumulators, four warps each (one per
+//   warps 0, 1  producers, alternate tiles (a single thread issuing every bulk
+//               copy caps the stream well below HBM speed): bulk copies of
+//               the key tiles (8 KB codes + 512 B scales, already stored in the
+//               MMA operand layout) into an 8-stage ring; Reindex (POOL) tiles
+//               are gathered by warp 0 alone; warp 0 also puts each row's
+//               query operand into one of two B slots
+//   warps 2, 3  MMA issuers, alternate tiles (one thread issuing every tcgen05
+//               op of the CTA could not keep up): scale factors to TMEM
+//               (tcgen05.cp), two MMAs, commits that free the stage and hand
+//               the accumulator over
+//   warps 4..15 epilogue: three TMEM accumulators, four warps each (one per
 //               32-lane quarter); tile j of the CTA goes to accumulator j % 3.
 //               With a sideband buffer the epilogue also histograms the score
 //               keys (and, in FULL mode, the 8-position block maxima) in shared
@@ -39,7 +43,10 @@ namespace {
 constexpr int kStages = 8;
 constexpr int kAcc = 3;                 // TMEM accumulator buffers (tiles in flight in the epilogue)
 constexpr int kEpiWarps = 4 * kAcc;     // four warps (one per TMEM lane quarter) per accumulator
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kProducers = 2;            // copy-issuing warps (FULL mode), alternate tiles
+constexpr int kIssuers = 2;              // MMA-issuing warps, alternate tiles
+constexpr int kFirstEpiWarp = kProducers + kIssuers;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
@@ -120,7 +127,7 @@ struct __align__(1024) Smem {
   __align__(128) uint64_t bempty[2];
   __align__(128) uint32_t tmem;
   int abort;   // written only when a wait gives up
-  int issued;  // items whose copies the producer started (written once, at exit)
+  int issued[kProducers];  // tiles whose copies each producer started (written once, at exit)
   __align__(128) int nt[kMaxRowsPerCta];  // visible tiles of the rows this CTA touches (row - row0)
   uint32_t hist[2][kSelBins];  // this CTA's share of the current row's sideband histograms
 };
@@ -142,6 +149,20 @@ __device__ __forceinline__ bool wait_warp(Smem &sm, uint64_t *bar, uint32_t phas
 }
 
 __device__ __forceinline__ uint32_t sel_key(float f) { return isnan(f) ? 0u : orderable(f); }
+
+// Named barrier over `count` threads returning the AND of `v` across them.
+__device__ __forceinline__ int bar_and(uint32_t id, uint32_t count, int v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(count)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
@@ -175,14 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
     }
     for (int i = 0; i < kAcc; ++i) {
       tc::mbar_init(&sm.tfull[i], 1);
-      tc::mbar_init(&sm.tempty[i], 4);
+      tc::mbar_init(&sm.tempty[i], 1);  // the group leader, after a named barrier of its 4 warps
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sm.bfull[i], 1);
-      tc::mbar_init(&sm.bempty[i], 1 + kEpiWarps);
+      tc::mbar_init(&sm.bempty[i], kIssuers + kEpiWarps);
     }
     sm.abort = 0;
-    sm.issued = 0;
+    for (int i = 0; i < kProducers; ++i) sm.issued[i] = 0;
     tc::fence_mbar_init();
   }
   // visible tile count of every row in this CTA's item range, computed once
@@ -201,37 +222,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
   };
   // TMEM columns: accumulators [0, kAcc*np), SFA per accumulator at kAcc*np + 8*i,
   // SFB per B slot at kAcc*np + 8*kAcc + 8*i
+  // SFB: one copy per (issuer, B slot) at col_sfb + 8 * (2 * issuer + slot)
   const uint32_t col_sfa = kAcc * np, col_sfb = kAcc * np + 8 * kAcc;
 
   // Every role walks the same (row, tile) sequence and skips the same empty
   // tiles; a row's visible tile count is read once, when the walk enters it.
   const int tile_begin = static_cast<int>(i0 - static_cast<int64_t>(row0) * max_tiles);
 
-  if (warp == 0 && (lane == 0 || pool_mode)) {
-    // ------------------------------------------------------------ producer
-    // FULL: lane 0 alone issues two bulk copies per tile; POOL: the warp gathers.
-    int prev_row = -1, bchanges = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
+  if ((warp == 0 && (lane == 0 || pool_mode)) || (warp > 0 && warp < kProducers && lane == 0 && !pool_mode)) {
+    // ------------------------------------------------------------ producers
+    // FULL: lane 0 of warps 0..kProducers-1, alternate tiles, two bulk copies per
+    // tile; POOL: warp 0 gathers every tile.  Producer 0 also loads each row's
+    // query record into a B slot.
+    const int pw = warp, nprod = pool_mode ? 1 : kProducers;
+    int prev_row = -1, bchanges = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0), mine = 0;
     for (int64_t it = i0; it < i1; ++it) {
       if (tile < nt) {
         const int s = j % kStages;
         bool ok = true;
-        if (j >= kStages) ok = pool_mode ? wait_warp(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err)
-                                         : wait1(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err);
-        if (!ok) break;
         if (row != prev_row) {
           const int bs = bchanges & 1;
-          if (bchanges >= 2) {
-            ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
-                           : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
-            if (!ok) break;
-          }
-          if (lane == 0) {
-            tc::mbar_expect_tx(&sm.bfull[bs], brec);
-            bulk_g2s(tc::smem_addr(sm.bslot[bs]), a.qrec + static_cast<size_t>(row) * brec, brec, &sm.bfull[bs]);
+          if (pw == 0) {
+            if (bchanges >= 2) {
+              ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
+                             : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
+              if (!ok) break;
+            }
+            if (lane == 0) {
+              tc::mbar_expect_tx(&sm.bfull[bs], brec);
+              bulk_g2s(tc::smem_addr(sm.bslot[bs]), a.qrec + static_cast<size_t>(row) * brec, brec, &sm.bfull[bs]);
+            }
           }
           prev_row = row;
           ++bchanges;
         }
+        if (j % nprod != pw) {
+          ++j;
+        } else {
+        if (j >= kStages) ok = pool_mode ? wait_warp(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err)
+                                         : wait1(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err);
+        if (!ok) break;
         const int seq = a.s.cache_seq < 0 ? row : a.s.cache_seq;
         uint8_t *dst = sm.stage[s];
         if (!pool_mode) {
@@ -267,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
           if (lane == 0) tc::mbar_arrive(&sm.full[s]);
         }
         ++j;
+        mine = j;
+        }
       }
       if (++tile == max_tiles) {
         tile = 0;
@@ -274,36 +306,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
         if (it + 1 < i1) nt = tiles_of(row);
       }
     }
-    if (lane == 0) sm.issued = j;
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) sm.issued[pw] = mine;
+  } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
+    // ------------------------------------------------------------ MMA issuers (one thread each)
+    // issuer `who` takes the CTA's tiles j with j % kIssuers == who; each keeps its
+    // own copy of the row's query scale factors in TMEM
+    const int who = warp - kProducers;
     int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
     const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
-    for (int64_t it = i0; it < i1; ++it) {
+    bool dead = false;
+    for (int64_t it = i0; it < i1 && !dead; ++it) {
       if (tile < nt) {
         const int s = j % kStages, acc = j % kAcc;
         if (row != prev_row) {
           bs = bchanges & 1;
-          if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) break;
+          if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
+            dead = true;
+            break;
+          }
           prev_row = row;
           ++bchanges;
           tc::tc_fence_after();
-          tc::tmem_cp_32x128b_x4(tmem + col_sfb + 8 * bs,
+          tc::tmem_cp_32x128b_x4(tmem + col_sfb + 8 * (2 * who + bs),
                                  tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
         }
-        if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) break;
-        if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) break;
-        tc::tc_fence_after();
-        const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
-        tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
-        const uint32_t d = tmem + acc * np;
-        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
-                     tmem + col_sfa + 8 * acc, tmem + col_sfb + 8 * bs, 0);
-        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
-                     tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc,
-                     tmem + col_sfb + 8 * bs, 1);
-        tc::mma_commit(&sm.empty[s]);
-        tc::mma_commit(&sm.tfull[acc]);
+        if (j % kIssuers == who) {
+          if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) break;
+          if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) break;
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
+          const uint32_t sfb = tmem + col_sfb + 8 * (2 * who + bs);
+          tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
+          const uint32_t d = tmem + acc * np;
+          tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
+                       tmem + col_sfa + 8 * acc, sfb, 0);
+          tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
+                       tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb, 1);
+          tc::mma_commit(&sm.empty[s]);
+          tc::mma_commit(&sm.tfull[acc]);
+        }
+        // the row's B slot is free once both issuers' MMAs of the row are done
         if (tile + 1 >= nt || it + 1 >= i1) tc::mma_commit(&sm.bempty[bs]);
         ++j;
       }
@@ -313,16 +355,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
         if (it + 1 < i1) nt = tiles_of(row);
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - 2;           // 0 .. kEpiWarps-1
+    const int e = warp - kFirstEpiWarp;  // 0 .. kEpiWarps-1
     const int parity = e >> 2;        // accumulator buffer this warp drains (tiles j % kAcc == parity)
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int m = 32 * quarter + lane;
+    // the group's first warp waits on the mbarriers; named barriers (ids 2.. and
+    // 2 + kAcc..) hand the result to the other three and collect them back
+    const bool leader = (e & 3) == 0;
+    const uint32_t bar_full = 2 + parity, bar_done = 2 + kAcc + parity;
     int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
     int64_t row_nslots = row_slots(a, row0);
     const int64_t aux_row = aux_row_bytes(a.s.stride);
     bool dead = false;
+    // the row's head weights: in registers up to 64 heads, else read from shared memory
+    constexpr bool kWReg = np <= 64;
+    float wreg[kWReg ? np : 1];
+    const float *wsm = nullptr;
+    int w_row = -1;
     for (int64_t it = i0; it < i1; ++it) {
       if (tile < nt) {
         if (row != prev_row) {
@@ -332,33 +383,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
         }
         const bool last_of_row = tile + 1 >= nt || it + 1 >= i1;
         if (j % kAcc == parity && !dead) {
-          if (!wait_warp(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) ||
-              !wait_warp(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err)) {
-            dead = true;  // keep walking (the named barriers below), but do no more work
+          int ok = 1;
+          if (leader && lane == 0)
+            ok = wait1(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) &&
+                 wait1(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err);
+          if (!bar_and(bar_full, 128, ok)) {
+            dead = true;  // the whole group: keep walking (the flush barriers below), no more work
           } else {
             tc::tc_fence_after();
+            if (w_row != row) {
+              w_row = row;
+              wsm = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
+              if constexpr (kWReg) {
+                const float4 *wv = reinterpret_cast<const float4 *>(wsm);
+#pragma unroll
+                for (int h = 0; h < np / 4; ++h) {
+                  const float4 v = wv[h];
+                  wreg[4 * h] = v.x;
+                  wreg[4 * h + 1] = v.y;
+                  wreg[4 * h + 2] = v.z;
+                  wreg[4 * h + 3] = v.w;
+                }
+              }
+            }
             const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
-            // heads in chunks of at most 64 columns (bounded register use), the
-            // fma chain still runs over the heads in order
-            constexpr int kCh = np < 64 ? np : 64;
-            const float *wv = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
+            // 16-column chunks, the load of chunk c+1 in flight while chunk c is
+            // summed; the fma chain runs over the heads in order
+            constexpr int kNC = np / 16;
+            uint32_t ra[16], rb[16];
+            tc::tmem_ld_32x32b_x16(base, ra);
+            tc::tmem_ld_wait_x16(ra);
             float acc = 0.0f;
 #pragma unroll
-            for (int c0 = 0; c0 < np; c0 += kCh) {
-              uint32_t r[kCh];
-#pragma unroll
-              for (int h0 = 0; h0 < kCh; h0 += 16) tc::tmem_ld_32x32b_x16(base + c0 + h0, r + h0);
-              tc::tmem_ld_wait();
-              if (c0 + kCh >= np) {
+            for (int c = 0; c < kNC; ++c) {
+              uint32_t *cur = (c & 1) ? rb : ra;
+              uint32_t *nxt = (c & 1) ? ra : rb;
+              if (c + 1 < kNC) {
+                tc::tmem_ld_32x32b_x16(base + 16 * (c + 1), nxt);
+              } else {
+                // every TMEM read of the group has completed: hand the accumulator back
                 tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
+                bar_sync(bar_done, 128);
+                if (leader && lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
               }
 #pragma unroll
-              for (int h = 0; h < kCh; ++h) {
-                const float d = __uint_as_float(r[h]);
-                acc = __fmaf_rn(wv[c0 + h], d > 0.0f ? d : 0.0f, acc);
+              for (int h = 0; h < 16; ++h) {
+                const float d = __uint_as_float(cur[h]);
+                const float wh = kWReg ? wreg[kWReg ? 16 * c + h : 0] : wsm[16 * c + h];
+                acc = __fmaf_rn(wh, d > 0.0f ? d : 0.0f, acc);
               }
+              if (c + 1 < kNC) tc::tmem_ld_wait_x16(nxt);
             }
             const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
             bool valid;
@@ -398,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
           // to the row's sideband and clear them
           asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
           uint32_t *gh = reinterpret_cast<uint32_t *>(a.s.aux + static_cast<size_t>(row) * aux_row);
-          for (int i = threadIdx.x - 64; i < 2 * kSelBins; i += kEpiWarps * 32) {
+          for (int i = threadIdx.x - 32 * kFirstEpiWarp; i < 2 * kSelBins; i += kEpiWarps * 32) {
             const uint32_t c = (&sm.hist[0][0])[i];
             if (c) {
               atomicAdd(&gh[i], c);
@@ -426,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
   if (warp == 0) {
     // copies still in flight (only after an abort): bounded wait on the last items issued
     if (*reinterpret_cast<volatile int *>(&sm.abort) && lane == 0) {  // after a timeout only
-      const int n = sm.issued;
+      int n = 0;
+      for (int i = 0; i < kProducers; ++i) n = max(n, sm.issued[i]);
       for (int jj = n > kStages ? n - kStages : 0; jj < n; ++jj)
         tc::mbar_wait_bounded(&sm.full[jj % kStages], (jj / kStages) & 1, kWaitIters);
     }
@@ -449,7 +524,7 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   a.s = s;
   a.np = ((s.heads + 15) / 16) * 16;
   a.qrec = static_cast<const uint8_t *>(ws);
-  const int cols = kAcc * a.np + 8 * kAcc + 16;
+  const int cols = kAcc * a.np + 8 * kAcc + 8 * 2 * kIssuers;
   a.ncols = cols <= 128 ? 128 : (cols <= 256 ? 256 : 512);
   k_qprep<<<dim3(s.rows, a.np / 8), 256, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
   const int max_tiles = static_cast<int>(
