@@ -49,6 +49,24 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def score_traffic():
+    """dram read + write bytes per launch of the score kernel from the committed ncu
+    summary, or None when the kernel source has changed since that capture."""
+    import hashlib
+    here = os.path.dirname(os.path.abspath(__file__))
+    prof = os.path.join(here, "profiles", "index_score_tc_full_decode_b32_t65536.md")
+    src = os.path.join(here, "fp4_compressed_sparse_gb300", "csrc", "csa2_score_tc.cu")
+    try:
+        text = open(prof).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        rec = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("source_sha256:", "traffic_bytes")))
+        if rec.get("source_sha256", "").strip() != sha:
+            return None
+        return int(rec["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -418,7 +436,7 @@ def run_ours(args):
                    "frac": round(kv_gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind},
         "roofline": {"kernel": "index_score (Full scan: query prep + tensor-core score + sideband)", "bound": "hbm",
                      "achieved": round(achieved, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": score_traffic(),
                      "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": round(score_avg, 5),
                      "peak_kind": hbm_kind},
         "step_breakdown_ms": {k: round(statistics.mean(v), 5) for k, v in parts.items()},
