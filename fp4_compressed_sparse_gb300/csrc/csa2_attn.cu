@@ -425,17 +425,27 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     if (!dead) dead = !wait_warp(&sm.full[st], (c >> 1) & 1, a.err);
     if (!dead) {
       // ---- logits of heads 16hg.. x entries 16eh..
+      // four independent accumulator chains (2 entry tiles x even / odd k-steps)
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const uint32_t qa = smem_u32(&sm.q[16 * hg + (lane & 15)][(lane >> 4) * 8]);
       const uint32_t kb = smem_u32(&sm.kv[st][16 * eh + (lane & 7) + ((lane >> 4) << 3)][((lane >> 3) & 1) * 8]);
-#pragma unroll 6
-      for (int kk = 0; kk < kDqk / 16; ++kk) {
-        uint32_t af[4], b0, b1, b2, b3;
+#pragma unroll 3
+      for (int kk = 0; kk < kDqk / 16; kk += 2) {
+        uint32_t af[4], b0, b1, b2, b3, ag[4], c0, c1, c2, c3;
         ldsm_x4(qa + kk * 32, af[0], af[1], af[2], af[3]);
         ldsm_x4(kb + kk * 32, b0, b1, b2, b3);
+        ldsm_x4(qa + kk * 32 + 32, ag[0], ag[1], ag[2], ag[3]);
+        ldsm_x4(kb + kk * 32 + 32, c0, c1, c2, c3);
         mma_f16(acc[0], af, b0, b1);
         mma_f16(acc[1], af, b2, b3);
+        mma_f16(acc2[0], ag, c0, c1);
+        mma_f16(acc2[1], ag, c2, c3);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -595,21 +605,24 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
 #pragma unroll
     for (int sp = 0; sp < kMaxSplits; ++sp) fs[sp] = __shfl_sync(0xffffffffu, f, sp) * inv;
     float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat;
+    // every peer load of the head first (independent), then the sums
+    float4 v[kMaxSplits][kLat / 128];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp)
+#pragma unroll
+      for (int c = 0; c < kLat / 128; ++c)
+        v[sp][c] = sp < n_splits ? ld_dsmem4(osm + hl * kLat + 128 * c + 4 * lane, sp) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < kLat / 128; ++c) {
-      const int d = 128 * c + 4 * lane;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int sp = 0; sp < kMaxSplits; ++sp) {
-        if (sp < n_splits && fs[sp] != 0.0f) {
-          const float4 v = ld_dsmem4(osm + hl * kLat + d, sp);
-          acc.x += v.x * fs[sp];
-          acc.y += v.y * fs[sp];
-          acc.z += v.z * fs[sp];
-          acc.w += v.w * fs[sp];
-        }
+        acc.x += v[sp][c].x * fs[sp];
+        acc.y += v[sp][c].y * fs[sp];
+        acc.z += v[sp][c].z * fs[sp];
+        acc.w += v[sp][c].w * fs[sp];
       }
-      *reinterpret_cast<float4 *>(out + d) = acc;
+      *reinterpret_cast<float4 *>(out + 128 * c + 4 * lane) = acc;
     }
     if (lane == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }

@@ -33,9 +33,10 @@ namespace csa2 {
 namespace {
 
 constexpr int kChunk = 4096;  // slots per sideband-fill CTA
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int64_t kSmemBitmapWords = 32768;  // rows up to 2^20 slots keep the bitmap in shared memory
+constexpr int kSelCluster = 4;               // CTAs per (row, problem): one cluster shares the row
+constexpr int64_t kSmemBitmapWords = 32768;  // a CTA's bitmap slice stays in shared memory up to 128 KB
 
 __device__ __forceinline__ uint32_t key_of(float f) { return isnan(f) ? 0u : orderable(f); }
 
@@ -210,11 +211,11 @@ __device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_
 
 struct SelSmem {
   uint32_t hist[kSelBins];
-  uint64_t cand[kSelCap];
+  uint64_t cand[kSelCap];  // this CTA's keys of the threshold bin; the leader then gathers everyone's
   uint32_t warp_tot[kSelWarps + 1];
   uint32_t dhist[256];
   uint64_t prefix;
-  uint32_t thr, above, total, ncand, overflow, rem, done;
+  uint32_t thr, above, total, ncand, overflow, rem, done, cnt;
 };
 
 // Key of slot `slot` (valid only when *ok): reads of one warp step go to 32
@@ -230,37 +231,74 @@ __device__ __forceinline__ float slot_value(const TopkArgs &a, const float *src,
   return src[slot];
 }
 
-// grid (rows, problems), kSelThreads; dynamic smem: SelSmem (+ the bitmap when it fits)
-__global__ void __launch_bounds__(kSelThreads, 1) k_select(TopkArgs a, const uint8_t *aux, int64_t aux_row,
+// ---- distributed shared memory (the CTAs of one cluster)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void *p, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];\n" : "=r"(v) : "r"(dsmem_addr(p, rank)) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_dsmem_u64(const void *p, uint32_t rank) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];\n" : "=l"(v) : "r"(dsmem_addr(p, rank)) : "memory");
+  return v;
+}
+__device__ __forceinline__ void or_dsmem(uint32_t *p, uint32_t rank, uint32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;\n" ::"r"(dsmem_addr(p, rank)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// bitmap words of one cluster CTA: a multiple of 4 (the vector pass takes 4 words per step)
+__host__ __device__ __forceinline__ int64_t span_words(int64_t nw) {
+  return ((nw + kSelCluster - 1) / kSelCluster + 3) / 4 * 4;
+}
+
+// grid (kSelCluster, rows, problems), cluster (kSelCluster, 1, 1), kSelThreads;
+// dynamic smem: SelSmem + this CTA's bitmap slice (when it fits)
+__global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uint8_t *aux, int64_t aux_row,
                                                            uint32_t *bitmap_g, int bitmap_in_smem) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x, p = blockIdx.y;
+  const uint32_t rank = blockIdx.x;  // rank in the cluster
+  const int row = blockIdx.y, p = blockIdx.z;
   const int64_t ns = n_slots(a, row, p);
   const int64_t T = row_T(a, row);
   const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
   const int64_t nw = (ns + 31) / 32;
-  uint32_t *bm = bitmap_in_smem ? reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem))
-                                : row_bitmap(bitmap_g, a.stride, row, p);
+  const int64_t span = span_words(nw);
+  const int64_t w_lo = min(nw, static_cast<int64_t>(rank) * span), w_hi = min(nw, w_lo + span);
+  uint32_t *bm_local = bitmap_in_smem ? reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem))
+                                      : row_bitmap(bitmap_g, a.stride, row, p) + w_lo;
+  // word w of the row lives in CTA w / span at offset w % span
   const float *src = p == 1 ? aux_bmax(aux, aux_row, row) : a.scores + static_cast<size_t>(row) * a.stride;
   const int32_t *prow = a.pool ? a.pool + static_cast<size_t>(row) * a.pool_blocks : nullptr;
 
   // the first batch of the streaming pass does not depend on the threshold:
   // request it now (FULL rows and block maxima)
-  constexpr int kFB = 32;  // words per warp per batch in the fast pass
+  constexpr int kFB = 16;  // words per warp per batch in the fast pass
   const bool plain = p == 1 || a.pool == nullptr;
-  const uint32_t nwu = static_cast<uint32_t>(nw), nsu = static_cast<uint32_t>(ns);
+  const uint32_t nsu = static_cast<uint32_t>(ns);
   float fb[kFB];
   if (plain) {
 #pragma unroll
     for (int b = 0; b < kFB; ++b) {
-      const uint32_t slot = (static_cast<uint32_t>(warp) * kFB + b) * 32 + lane;
-      fb[b] = slot < nsu ? src[slot] : __uint_as_float(0x7FC00000u);
+      const int64_t w = w_lo + static_cast<int64_t>(warp) * kFB + b;
+      const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
+      fb[b] = (w < w_hi && slot < nsu) ? src[slot] : __uint_as_float(0x7FC00000u);
     }
   }
 
-  // ---- 1. threshold bin from the histogram
+  // ---- 1. threshold bin from the histogram (every CTA of the cluster, identically)
   {
     const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
     for (int i = tid; i < kSelBins / 4; i += kSelThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
@@ -272,7 +310,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) k_select(TopkArgs a, const uin
       sm.prefix = 0;
     }
     __syncthreads();
-    // thread t owns the 8 bins kSelBins-1-8t-i (thread 0 the top ones)
+    // thread t owns the bins kSelBins-1-per*t-i (thread 0 the top ones)
     constexpr int per = kSelBins / kSelThreads;
     const int top = kSelBins - 1 - tid * per;
     uint32_t local = 0;
@@ -305,171 +343,132 @@ __global__ void __launch_bounds__(kSelThreads, 1) k_select(TopkArgs a, const uin
   const uint32_t kt = min(k, sm.total);
   const uint32_t need = kt - sm.above;
 
-  // ---- 2. one pass: bitmap words of the keys above the bin, candidates in it
+  // ---- 2. one pass over this CTA's words: bitmap words of the keys above the
+  // bin, candidates in it
+  auto add_cands = [&](uint32_t mask, bool want, uint64_t K) {
+    if (!mask) return;
+    const int leader = __ffs(mask) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (want) {
+      const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
+      if (at < kSelCap) sm.cand[at] = K;
+      else sm.overflow = 1;
+    }
+  };
   if (plain && thr > 0) {
     // order keys are monotone in the float value: "above the bin" is f > hi and
     // "in the bin" is lo <= f <= hi (exact, -0 == +0; NaN is neither, like its
-    // key 0 when the threshold bin is above 0); invalid slots read as NaN
+    // key 0 when the threshold bin is above 0); slots outside the row read as NaN
     const float lo = float_of_key(thr << kSelBinShift);
     const float hi = float_of_key(((thr + 1) << kSelBinShift) - 1);
-    for (uint32_t w0 = static_cast<uint32_t>(warp) * kFB; w0 < nwu; w0 += kSelWarps * kFB) {
-      if (w0 != static_cast<uint32_t>(warp) * kFB) {
+    for (int64_t w0 = w_lo + static_cast<int64_t>(warp) * kFB; w0 < w_hi; w0 += static_cast<int64_t>(kSelWarps) * kFB) {
+      if (w0 != w_lo + static_cast<int64_t>(warp) * kFB) {
 #pragma unroll
         for (int b = 0; b < kFB; ++b) {
-          const uint32_t slot = (w0 + b) * 32 + lane;
-          fb[b] = slot < nsu ? src[slot] : __uint_as_float(0x7FC00000u);
+          const int64_t w = w0 + b;
+          const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
+          fb[b] = (w < w_hi && slot < nsu) ? src[slot] : __uint_as_float(0x7FC00000u);
         }
       }
 #pragma unroll
       for (int b = 0; b < kFB; ++b) {
-        const uint32_t w = w0 + b;
-        if (w >= nwu) break;  // warp-uniform
+        const int64_t w = w0 + b;
+        if (w >= w_hi) break;  // warp-uniform
         const float f = fb[b];
-        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && w * 32 + lane < nsu)) {
-          if (isnan(f) && w * 32 + lane < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
+        const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
+        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && slot < nsu)) {
+          if (isnan(f) && slot < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
         }
         const uint32_t word = __ballot_sync(0xffffffffu, f > hi);
-        if (lane == 0) bm[w] = word;
+        if (lane == 0) bm_local[w - w_lo] = word;
         const bool want = f >= lo && f <= hi;
-        const uint32_t mask = __ballot_sync(0xffffffffu, want);
-        if (mask) {
-          const int leader = __ffs(mask) - 1;
-          uint32_t base = 0;
-          if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          if (want) {
-            const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
-            const uint32_t slot = w * 32 + lane;
-            if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot);
-            else sm.overflow = 1;
-          }
-        }
+        add_cands(__ballot_sync(0xffffffffu, want), want,
+                  (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
       }
     }
-    if (tid == 0) sm.rem = need;
-    __syncthreads();
   } else {
-    // vector path: lane l of a warp step takes slots 4l..4l+3 of 128; rows of
-    // a whole number of float4 (or the padded block maxima) only
-    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0 && (p == 1 || (a.stride & 3) == 0);
-    if (vec) {
-      constexpr int kB = 4;  // float4 in flight per lane
-      const int64_t nsteps = (ns + 127) / 128;
-      for (int64_t s0 = static_cast<int64_t>(warp) * kB; s0 < nsteps; s0 += static_cast<int64_t>(kSelWarps) * kB) {
-        float4 f[kB];
-#pragma unroll
-        for (int b = 0; b < kB; ++b) {
-          const int64_t slot = (s0 + b) * 128 + 4 * lane;
-          f[b] = slot < ns ? *reinterpret_cast<const float4 *>(src + slot) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int b = 0; b < kB; ++b) {
-          const int64_t stp = s0 + b;
-          if (stp >= nsteps) break;  // warp-uniform
-          const int64_t slot0 = stp * 128 + 4 * lane;
-          const float v[4] = {f[b].x, f[b].y, f[b].z, f[b].w};
-          uint32_t above = 0, candm = 0, key[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int64_t slot = slot0 + e;
-            bool ok = slot < ns;
-            if (ok && p == 0 && a.pool) {
-              const int32_t pid = prow[slot / a.bs];
-              ok = pid >= 0 && static_cast<int64_t>(pid) * a.bs + slot % a.bs < T;
-            }
-            key[e] = key_of(v[e]);
-            if (ok) {
-              if (p == 0 && isnan(v[e])) raise_err(a.err, CSA2_DEVERR_NAN);
-              const uint32_t bin = key[e] >> kSelBinShift;
-              if (bin > thr) above |= 1u << e;
-              if (bin == thr) candm |= 1u << e;
-            }
-          }
-          // word j of the step = slots 32j..32j+31 = lanes 8j..8j+7
-          uint32_t wv = above << (4 * (lane & 7));
-          wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
-          wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
-          wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
-          const int64_t wi = stp * 4 + (lane >> 3);
-          if ((lane & 7) == 0 && wi < nw) bm[wi] = wv;
-          if (__any_sync(0xffffffffu, candm != 0)) {
-            const uint32_t c = __popc(candm);
-            uint32_t inc = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-              if (lane >= o) inc += y;
-            }
-            uint32_t base = 0;
-            if (lane == 31) base = atomicAdd(&sm.ncand, inc);
-            base = __shfl_sync(0xffffffffu, base, 31);
-            uint32_t at = base + inc - c;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if ((candm >> e) & 1u) {
-                const uint32_t slot = static_cast<uint32_t>(slot0 + e);
-                if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(key[e]) << 32) | (0xFFFFFFFFu - slot);
-                else sm.overflow = 1;
-                ++at;
-              }
-          }
-        }
-      }
-    } else {
-      constexpr int kBatch = 8;  // words in flight per warp
-      for (int64_t w0 = static_cast<int64_t>(warp) * kBatch; w0 < nw;
-           w0 += static_cast<int64_t>(kSelWarps) * kBatch) {
-        float f[kBatch];
-        bool ok[kBatch];
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) f[b] = slot_value(a, src, prow, p, (w0 + b) * 32 + lane, ns, T, ok[b]);
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int64_t w = w0 + b;
-          if (w >= nw) break;  // warp-uniform
-          if (p == 0 && ok[b] && isnan(f[b])) raise_err(a.err, CSA2_DEVERR_NAN);
-          const uint32_t key = key_of(f[b]);
-          const uint32_t bin = key >> kSelBinShift;
-          const uint32_t word = __ballot_sync(0xffffffffu, ok[b] && bin > thr);
-          if (lane == 0) bm[w] = word;
-          const bool want = ok[b] && bin == thr;
-          const uint32_t mask = __ballot_sync(0xffffffffu, want);
-          if (mask) {
-            const int leader = __ffs(mask) - 1;
-            uint32_t base = 0;
-            if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
-            base = __shfl_sync(0xffffffffu, base, leader);
-            if (want) {
-              const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
-              const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
-              if (at < kSelCap) sm.cand[at] = (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - slot);
-              else sm.overflow = 1;
-            }
-          }
-        }
-      }
+    for (int64_t w = w_lo + warp; w < w_hi; w += kSelWarps) {
+      bool ok;
+      const int64_t slot = w * 32 + lane;
+      const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+      if (p == 0 && ok && isnan(f)) raise_err(a.err, CSA2_DEVERR_NAN);
+      const uint32_t key = key_of(f);
+      const uint32_t bin = key >> kSelBinShift;
+      const uint32_t word = __ballot_sync(0xffffffffu, ok && bin > thr);
+      if (lane == 0) bm_local[w - w_lo] = word;
+      const bool want = ok && bin == thr;
+      add_cands(__ballot_sync(0xffffffffu, want), want,
+                (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(slot)));
     }
+  }
+  cluster_sync();  // #1: every slice and candidate list complete
+
+  // ---- 3. the leader gathers the candidates and selects the ones still needed
+  if (rank == 0) {
+    uint32_t cnt[kSelCluster], off[kSelCluster], n = 0, ovf = 0;
+    for (uint32_t r = 0; r < kSelCluster; ++r) {
+      cnt[r] = r == 0 ? sm.ncand : ld_dsmem_u32(&sm.ncand, r);
+      ovf |= r == 0 ? sm.overflow : ld_dsmem_u32(&sm.overflow, r);
+      off[r] = n;
+      n += cnt[r];
+    }
+    const bool from_row = ovf != 0 || n > static_cast<uint32_t>(kSelCap);
+    if (!from_row) {
+      for (uint32_t r = 1; r < kSelCluster; ++r)
+        for (uint32_t i = tid; i < cnt[r]; i += kSelThreads) sm.cand[off[r] + i] = ld_dsmem_u64(&sm.cand[i], r);
+    }
+    __syncthreads();
     if (tid == 0) sm.rem = need;
     __syncthreads();
-  }
-
-  // ---- 3. exact select of the need-th largest low key in the bin: 8-bit
-  // digits over bits 50..3, then bits 2..0
-  const bool from_row = sm.overflow != 0;
-  const int n = static_cast<int>(min(sm.ncand, static_cast<uint32_t>(kSelCap)));
-  const bool all = !from_row && need == static_cast<uint32_t>(n);
-  if (need > 0 && !all) {
-    for (int d = 0; d < 7; ++d) {
-      const int sh = d < 6 ? 43 - 8 * d : 0;
-      const uint32_t dmask = d < 6 ? 0xFFu : 0x7u;
-      const uint64_t hi_mask = kLow & ~((1ull << (sh + (d < 6 ? 8 : 3))) - 1);
-      for (int i = tid; i < 256; i += kSelThreads) sm.dhist[i] = 0;
-      __syncthreads();
-      const uint64_t prefix = sm.prefix;
+    // exact select of the need-th largest low key in the bin: 8-bit digits over
+    // bits 50..3, then bits 2..0
+    const int nc = static_cast<int>(n);
+    const bool all = !from_row && need == n;
+    if (need > 0 && !all) {
+      for (int d = 0; d < 7; ++d) {
+        const int sh = d < 6 ? 43 - 8 * d : 0;
+        const uint32_t dmask = d < 6 ? 0xFFu : 0x7u;
+        const uint64_t hi_mask = kLow & ~((1ull << (sh + (d < 6 ? 8 : 3))) - 1);
+        for (int i = tid; i < 256; i += kSelThreads) sm.dhist[i] = 0;
+        __syncthreads();
+        const uint64_t prefix = sm.prefix;
+        if (!from_row) {
+          for (int i = tid; i < nc; i += kSelThreads) {
+            const uint64_t low = sm.cand[i] & kLow;
+            if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+          }
+        } else {
+          for (int64_t slot = tid; slot < ns; slot += kSelThreads) {
+            bool ok;
+            const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+            const uint32_t key = key_of(f);
+            if (!ok || (key >> kSelBinShift) != thr) continue;
+            const uint64_t low = low_of(key, static_cast<uint32_t>(slot));
+            if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) pick_digit(sm.dhist, sh, &sm.rem, &sm.prefix, &sm.done);
+        __syncthreads();
+        if (sm.done) break;
+      }
+    }
+    // mark the chosen keys of the bin (low >= the need-th largest) in their owners' slices
+    const uint64_t cut = sm.prefix;
+    auto mark = [&](uint32_t slot) {
+      const int64_t w = slot >> 5;
+      const uint32_t owner = static_cast<uint32_t>(w / span);
+      const uint32_t bit = 1u << (slot & 31);
+      if (bitmap_in_smem) or_dsmem(reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem)) + (w - owner * span), owner, bit);
+      else atomicOr(row_bitmap(bitmap_g, a.stride, row, p) + w, bit);
+    };
+    if (need > 0) {
       if (!from_row) {
-        for (int i = tid; i < n; i += kSelThreads) {
-          const uint64_t low = sm.cand[i] & kLow;
-          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+        for (int i = tid; i < nc; i += kSelThreads) {
+          const uint64_t K = sm.cand[i];
+          if (all || (K & kLow) >= cut) mark(0xFFFFFFFFu - static_cast<uint32_t>(K));
         }
       } else {
         for (int64_t slot = tid; slot < ns; slot += kSelThreads) {
@@ -477,60 +476,42 @@ __global__ void __launch_bounds__(kSelThreads, 1) k_select(TopkArgs a, const uin
           const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
           const uint32_t key = key_of(f);
           if (!ok || (key >> kSelBinShift) != thr) continue;
-          const uint64_t low = low_of(key, static_cast<uint32_t>(slot));
-          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+          if (low_of(key, static_cast<uint32_t>(slot)) >= cut) mark(static_cast<uint32_t>(slot));
         }
-      }
-      __syncthreads();
-      if (warp == 0) pick_digit(sm.dhist, sh, &sm.rem, &sm.prefix, &sm.done);
-      __syncthreads();
-      if (sm.done) break;
-    }
-  }
-  // mark the chosen keys of the bin: low >= the need-th largest
-  const uint64_t cut = sm.prefix;
-  if (need > 0) {
-    if (!from_row) {
-      for (int i = tid; i < n; i += kSelThreads) {
-        const uint64_t K = sm.cand[i];
-        if (all || (K & kLow) >= cut) {
-          const uint32_t slot = 0xFFFFFFFFu - static_cast<uint32_t>(K);
-          atomicOr(&bm[slot >> 5], 1u << (slot & 31));
-        }
-      }
-    } else {
-      for (int64_t slot = tid; slot < ns; slot += kSelThreads) {
-        bool ok;
-        const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
-        const uint32_t key = key_of(f);
-        if (!ok || (key >> kSelBinShift) != thr) continue;
-        if (low_of(key, static_cast<uint32_t>(slot)) >= cut) atomicOr(&bm[slot >> 5], 1u << (slot & 31));
       }
     }
   }
-  __syncthreads();
+  cluster_sync();  // #2: every chosen slot is marked
 
-  // ---- 4. ascending output: block scan of the bitmap's popcounts
-  const int64_t per = (nw + kSelThreads - 1) / kSelThreads;
-  const int64_t wb = tid * per, we = min(nw, wb + per);
-  uint32_t cnt = 0;
-  for (int64_t w = wb; w < we; ++w) cnt += __popc(bm[w]);
+  // ---- 4. ascending output: block scan of this slice's popcounts, offset by
+  // the counts of the lower-ranked slices
+  const int64_t nloc = w_hi - w_lo;
+  const int64_t per = (nloc + kSelThreads - 1) / kSelThreads;
+  const int64_t wb = min(nloc, tid * per), we = min(nloc, wb + per);
+  uint32_t c = 0;
+  for (int64_t w = wb; w < we; ++w) c += __popc(bm_local[w]);
   uint32_t tot;
-  uint32_t off = block_excl_scan(cnt, sm.warp_tot, &tot);
+  uint32_t off = block_excl_scan(c, sm.warp_tot, &tot);
+  if (tid == 0) sm.cnt = tot;
+  cluster_sync();  // #3: every slice's count published
+  for (uint32_t r = 0; r < rank; ++r) off += ld_dsmem_u32(&sm.cnt, r);
   int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
                         : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
   for (int64_t w = wb; w < we; ++w) {
-    uint32_t word = bm[w];
+    uint32_t word = bm_local[w];
     while (word) {
       const int b = __ffs(word) - 1;
       word &= word - 1;
-      if (off < kt) out[off] = slot_position(a, row, p, static_cast<uint32_t>(w * 32 + b));
+      if (off < kt) out[off] = slot_position(a, row, p, static_cast<uint32_t>((w_lo + w) * 32 + b));
       ++off;
     }
   }
-  const int kout = p == 0 ? a.k : a.out_pool_blocks;
-  for (int i = kt + tid; i < kout; i += kSelThreads) out[i] = -1;
-  if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
+  if (rank == kSelCluster - 1) {
+    const int kout = p == 0 ? a.k : a.out_pool_blocks;
+    for (int i = kt + tid; i < kout; i += kSelThreads) out[i] = -1;
+    if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
+  }
+  cluster_sync();  // #4: no CTA leaves while a peer may still read its shared memory
 }
 
 }  // namespace
@@ -570,15 +551,29 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
     aux = own;
   }
   const int nprob = (!a.pool && a.out_pool_blocks > 0) ? 2 : 1;
-  const int in_smem = w0 <= kSmemBitmapWords ? 1 : 0;
-  const int smem = static_cast<int>(sizeof(SelSmem) + (in_smem ? w0 * 4 : 0));
+  const int64_t slice = span_words(w0);
+  const int in_smem = slice <= kSmemBitmapWords ? 1 : 0;
+  const int smem = static_cast<int>(sizeof(SelSmem) + (in_smem ? slice * 4 : 0));
   static int attr = 0;
   if (smem > attr) {
     cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = smem;
   }
-  k_select<<<dim3(a.rows, nprob), kSelThreads, smem, s>>>(a, aux, aux_row, bitmap, in_smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSelCluster, a.rows, nprob);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute cl[1];
+  cl[0].id = cudaLaunchAttributeClusterDimension;
+  cl[0].val.clusterDim.x = kSelCluster;
+  cl[0].val.clusterDim.y = 1;
+  cl[0].val.clusterDim.z = 1;
+  cfg.attrs = cl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_select, a, aux, aux_row, bitmap, in_smem);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
