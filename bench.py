@@ -549,7 +549,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="full_decode", choices=["full_decode", "tiny_decode"])
+    ap.add_argument("--workload", default="full_decode", choices=["full_decode", "full_decode_small", "tiny_decode"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -172,6 +172,13 @@ def full_decode(device="cuda"):
                           index_heads=64, topk=512, swa_dtype=1, seed=1, device=device)
 
 
+def full_decode_small(device="cuda"):
+    """The Full-layer decode step at context 8,192: the attention and top-k launches
+    have the shapes of full_decode, the cache is 8x smaller (small profiler captures)."""
+    return DecodeWorkload("full_decode_b32_t8192", batch=32, context=8192, heads=64,
+                          index_heads=64, topk=512, swa_dtype=1, seed=1, device=device)
+
+
 def reindex_decode(device="cuda"):
     return DecodeWorkload("reindex_reuse3_b64_t262144", batch=64, context=262144, heads=64,
                           index_heads=64, topk=512, swa_dtype=1, seed=2,

@@ -15,9 +15,10 @@ def u16(t):
 
 
 def build_r1(orc, batch, n_tokens, swa_dtype, seed, chunks=None, in_bf16=False, cap=None,
-             theta=10000.0, rope=None):
+             theta=10000.0, rope=None, kv_scale=1.0):
     """Append n_tokens per sequence (in the given chunk sizes) on the GPU and in the
-    oracle.  Returns (gpu cache, [oracle caches], rope table, err word)."""
+    oracle; the latent rows are multiplied by kv_scale (a power of two).
+    Returns (gpu cache, [oracle caches], rope table, err word)."""
     cap = cap or n_tokens + 8
     c = csa2.Cache(batch, cap, ratio=1, swa_dtype=swa_dtype)
     rope = rope if rope is not None else csa2.rope_table(theta, cap + 8)
@@ -26,7 +27,7 @@ def build_r1(orc, batch, n_tokens, swa_dtype, seed, chunks=None, in_bf16=False, 
     oc = [orc.Cache(cap, swa_dtype=swa_dtype) for _ in range(batch)]
     t0 = 0
     for n in chunks:
-        kv = torch.stack([wl.token_rows(seed, wl.S_KV, b, t0, n, 576) for b in range(batch)])
+        kv = torch.stack([wl.token_rows(seed, wl.S_KV, b, t0, n, 576) for b in range(batch)]) * kv_scale
         ik = torch.stack([wl.token_rows(seed, wl.S_IK, b, t0, n, 128) for b in range(batch)])
         if in_bf16:
             kv, ik = kv.to(torch.bfloat16), ik.to(torch.bfloat16)

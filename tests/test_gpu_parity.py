@@ -248,8 +248,11 @@ def test_topk_nan_score_is_reported(orc):
 @pytest.mark.parametrize("B,T,H,k,swa_dtype,use_sink", [
     (3, 700, 64, 64, csa2.SWA_MXFP8, False),
     (3, 700, 64, 64, csa2.SWA_BF16, True),
-    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # enough rows: no split, no combine
+    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # two splits per row
+    (80, 200, 64, 48, csa2.SWA_BF16, False),   # enough rows: one split, two chunks, no merge
     (1, 90, 32, 128, csa2.SWA_MXFP8, False),   # window shorter than 128, idx padded with -1
+    (3, 1500, 128, 1024, csa2.SWA_BF16, True), # two head blocks, 8-CTA clusters, 2 chunks per split
+    (2, 300, 48, 200, csa2.SWA_MXFP8, False),  # a partial head block
 ])
 def test_sparse_attn_decode(orc, B, T, H, k, swa_dtype, use_sink):
     c, oc, _, err = build_r1(orc, B, T, swa_dtype, seed=41 + B)
@@ -281,6 +284,29 @@ def test_sparse_attn_decode(orc, B, T, H, k, swa_dtype, use_sink):
                             sink=sink.cuda() if sink is not None else None, err=err)
     torch.cuda.synchronize()
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+@pytest.mark.parametrize("swa_dtype", [csa2.SWA_BF16, csa2.SWA_MXFP8])
+def test_sparse_attn_decode_large_window_values(orc, swa_dtype):
+    """Latent rows scaled by 2^18 (the FP4 scales saturate, the window rows do not fit
+    fp16) and the query by 2^-18: the window entries take a power-of-two scale 2^-sigma
+    on the tensor-core path and the logits stay moderate."""
+    B, T, H, k = 2, 400, 64, 256
+    c, oc, _, err = build_r1(orc, B, T, swa_dtype, seed=71, kv_scale=2.0 ** 18)
+    _, _, q = _decode_inputs(B, 4, H, seed=72)
+    q = (q.float() * 2.0 ** -18).to(torch.bfloat16)
+    g = torch.Generator().manual_seed(73)
+    idx = torch.stack([torch.sort(torch.randperm(T - 1, generator=g)[:k]).values for _ in range(B)]).to(torch.int32)
+    q_pos = torch.full((B,), T - 1, dtype=torch.int64, device="cuda")
+    out = torch.empty((B, H, 512), device="cuda")
+    lse = torch.empty((B, H), device="cuda")
+    scale = 1 / math.sqrt(576)
+    csa2.sparse_attn_decode(c, q.cuda(), q_pos, idx.cuda(), out, lse, csa2.attn_workspace(B, H, k), scale, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for b in range(B):
+        ro, rl = orc.sparse_attn(oc[b], u16(q[b]), idx[b].numpy(), T - 1, scale)
+        attn_close(out[b].cpu().numpy(), lse[b].cpu().numpy(), ro, rl)
 
 
 def test_attn_index_error_is_reported(orc):
