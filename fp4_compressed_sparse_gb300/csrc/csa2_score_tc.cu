@@ -40,15 +40,27 @@
 namespace csa2 {
 namespace {
 
-constexpr int kStages = 8;
-constexpr int kAcc = 3;                 // TMEM accumulator buffers (tiles in flight in the epilogue)
-constexpr int kEpiWarps = 4 * kAcc;     // four warps (one per TMEM lane quarter) per accumulator
+// Every role that waits on an mbarrier waits on each of its phases in order:
+// a parity wait on a barrier two phases behind the waiter would return at
+// once.  So tile j goes to producer j % 2, to MMA issuer j % 2 and to
+// accumulator j % kAcc with kAcc a multiple of 2 (issuer i alone feeds the
+// accumulators i, i + 2, ...), and the stage count is even: each role then owns
+// a fixed subset of the stages and of the accumulators and visits their phases
+// consecutively.
 constexpr int kProducers = 2;            // copy-issuing warps (FULL mode), alternate tiles
 constexpr int kIssuers = 2;              // MMA-issuing warps, alternate tiles
+constexpr int kStages = 14;
+// TMEM accumulator buffers (tiles in flight in the epilogue): four while they
+// and the scale-factor columns fit the 512 TMEM columns, else two
+__host__ __device__ constexpr int acc_of(int np) { return 4 * np + 8 * 4 + 8 * 2 * kIssuers <= 512 ? 4 : 2; }
+constexpr int kAccMax = 4;
+static_assert(kStages % kProducers == 0 && kStages % kIssuers == 0, "each role must own whole stages");
 constexpr int kFirstEpiWarp = kProducers + kIssuers;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+// four epilogue warps (one per TMEM lane quarter) per accumulator
+__host__ __device__ constexpr int threads_of(int np) { return 32 * (kFirstEpiWarp + 4 * acc_of(np)); }
 constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
+constexpr int kRound = 64;               // accumulator columns read per TMEM load round in the epilogue
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
 
 // Per-row query record built by k_qprep: B codes (NP x 64 B, K-major no-swizzle:
@@ -121,8 +133,8 @@ struct __align__(1024) Smem {
   // line with them slow every barrier operation down
   __align__(128) uint64_t full[kStages];
   __align__(128) uint64_t empty[kStages];
-  __align__(128) uint64_t tfull[kAcc];
-  __align__(128) uint64_t tempty[kAcc];
+  __align__(128) uint64_t tfull[kAccMax];
+  __align__(128) uint64_t tempty[kAccMax];
   __align__(128) uint64_t bfull[2];
   __align__(128) uint64_t bempty[2];
   __align__(128) uint32_t tmem;
@@ -171,7 +183,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int max_tiles, int64_t total_items,
+__global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, int max_tiles, int64_t total_items,
                                                                 int64_t per_cta) {
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -181,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
   // items are (row, tile < max_tiles), row-major; a tile past the row's visible
   // length is empty and every role skips it the same way
   constexpr int np = NP;
+  constexpr int kAcc = acc_of(NP), kEpiWarps = 4 * kAcc;
+  static_assert(kAcc % kIssuers == 0, "each accumulator must be fed by one issuer");
   const int brec = qrec_bytes(np);
   const bool pool_mode = a.s.pool != nullptr;
   const int64_t seq_tiles = idx_tiles(a.s.cap);
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
     }
     for (int i = 0; i < kAcc; ++i) {
       tc::mbar_init(&sm.tfull[i], 1);
-      tc::mbar_init(&sm.tempty[i], 1);  // the group leader, after a named barrier of its 4 warps
+      tc::mbar_init(&sm.tempty[i], 4);  // the four warps of the accumulator's epilogue group
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sm.bfull[i], 1);
@@ -309,8 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
     if (lane == 0) sm.issued[pw] = mine;
   } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
     // ------------------------------------------------------------ MMA issuers (one thread each)
-    // issuer `who` takes the CTA's tiles j with j % kIssuers == who; each keeps its
-    // own copy of the row's query scale factors in TMEM
+    // issuer `who` takes the CTA's tiles j with j % kIssuers == who (accumulators
+    // and stages who, who + kIssuers, ...); each keeps its own copy of the row's
+    // query scale factors in TMEM
     const int who = warp - kProducers;
     int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
     const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
@@ -361,19 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
     const int parity = e >> 2;        // accumulator buffer this warp drains (tiles j % kAcc == parity)
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int m = 32 * quarter + lane;
-    // the group's first warp waits on the mbarriers; named barriers (ids 2.. and
-    // 2 + kAcc..) hand the result to the other three and collect them back
-    const bool leader = (e & 3) == 0;
-    const uint32_t bar_full = 2 + parity, bar_done = 2 + kAcc + parity;
     int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
     int64_t row_nslots = row_slots(a, row0);
     const int64_t aux_row = aux_row_bytes(a.s.stride);
     bool dead = false;
-    // the row's head weights: in registers up to 64 heads, else read from shared memory
-    constexpr bool kWReg = np <= 64;
-    float wreg[kWReg ? np : 1];
-    const float *wsm = nullptr;
-    int w_row = -1;
     for (int64_t it = i0; it < i1; ++it) {
       if (tile < nt) {
         if (row != prev_row) {
@@ -383,56 +389,52 @@ __global__ void __launch_bounds__(kThreads, 1) k_index_score_tc(TcArgs a, int ma
         }
         const bool last_of_row = tile + 1 >= nt || it + 1 >= i1;
         if (j % kAcc == parity && !dead) {
+          // each warp of the group waits for the accumulator itself and hands
+          // its lane quarter back on its own (tempty counts four arrivals)
           int ok = 1;
-          if (leader && lane == 0)
+          if (lane == 0)
             ok = wait1(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) &&
                  wait1(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err);
-          if (!bar_and(bar_full, 128, ok)) {
-            dead = true;  // the whole group: keep walking (the flush barriers below), no more work
+          if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            dead = true;
           } else {
             tc::tc_fence_after();
-            if (w_row != row) {
-              w_row = row;
-              wsm = reinterpret_cast<const float *>(sm.bslot[bs] + np * 64 + 512);
-              if constexpr (kWReg) {
-                const float4 *wv = reinterpret_cast<const float4 *>(wsm);
-#pragma unroll
-                for (int h = 0; h < np / 4; ++h) {
-                  const float4 v = wv[h];
-                  wreg[4 * h] = v.x;
-                  wreg[4 * h + 1] = v.y;
-                  wreg[4 * h + 2] = v.z;
-                  wreg[4 * h + 3] = v.w;
-                }
-              }
-            }
+            const float4 *wv = reinterpret_cast<const float4 *>(sm.bslot[bs] + np * 64 + 512);  // head weights
             const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
-            // 16-column chunks, the load of chunk c+1 in flight while chunk c is
-            // summed; the fma chain runs over the heads in order
-            constexpr int kNC = np / 16;
-            uint32_t ra[16], rb[16];
-            tc::tmem_ld_32x32b_x16(base, ra);
-            tc::tmem_ld_wait_x16(ra);
+            // up to kRound columns per round: every load of the round, then one
+            // wait; the fma chain runs over the heads in order
             float acc = 0.0f;
 #pragma unroll
-            for (int c = 0; c < kNC; ++c) {
-              uint32_t *cur = (c & 1) ? rb : ra;
-              uint32_t *nxt = (c & 1) ? ra : rb;
-              if (c + 1 < kNC) {
-                tc::tmem_ld_32x32b_x16(base + 16 * (c + 1), nxt);
-              } else {
-                // every TMEM read of the group has completed: hand the accumulator back
+            for (int h0 = 0; h0 < np; h0 += kRound) {
+              constexpr int kMaxC = (np < kRound ? np : kRound) / 16;
+              const int nc = (np - h0 < kRound ? np - h0 : kRound) / 16;
+              uint32_t r[kMaxC][16];
+#pragma unroll
+              for (int c = 0; c < kMaxC; ++c)
+                if (c < nc) tc::tmem_ld_32x32b_x16(base + h0 + 16 * c, r[c]);
+#pragma unroll
+              for (int c = 0; c < kMaxC; ++c)
+                if (c < nc) tc::tmem_ld_wait_x16(r[c]);
+              if (h0 + kRound >= np) {
+                // every TMEM read of this warp is complete: hand its quarter back
                 tc::tc_fence_before();
-                bar_sync(bar_done, 128);
-                if (leader && lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
               }
 #pragma unroll
-              for (int h = 0; h < 16; ++h) {
-                const float d = __uint_as_float(cur[h]);
-                const float wh = kWReg ? wreg[kWReg ? 16 * c + h : 0] : wsm[16 * c + h];
-                acc = __fmaf_rn(wh, d > 0.0f ? d : 0.0f, acc);
+              for (int c = 0; c < kMaxC; ++c) {
+                if (c >= nc) break;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float4 w4 = wv[(h0 + 16 * c) / 4 + q];
+                  const float wq[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const float d = __uint_as_float(r[c][4 * q + k]);
+                    acc = __fmaf_rn(wq[k], d > 0.0f ? d : 0.0f, acc);
+                  }
+                }
               }
-              if (c + 1 < kNC) tc::tmem_ld_wait_x16(nxt);
             }
             const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
             bool valid;
@@ -524,7 +526,7 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   a.s = s;
   a.np = ((s.heads + 15) / 16) * 16;
   a.qrec = static_cast<const uint8_t *>(ws);
-  const int cols = kAcc * a.np + 8 * kAcc + 8 * 2 * kIssuers;
+  const int cols = acc_of(a.np) * a.np + 8 * acc_of(a.np) + 8 * 2 * kIssuers;
   a.ncols = cols <= 128 ? 128 : (cols <= 256 ? 256 : 512);
   k_qprep<<<dim3(s.rows, a.np / 8), 256, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
   const int max_tiles = static_cast<int>(
@@ -561,7 +563,7 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   }
   const int64_t grid = total < num_sms ? total : num_sms;
   const int64_t per = (total + grid - 1) / grid;
-  fn<<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a, max_tiles, total, per);
+  fn<<<static_cast<unsigned>(grid), threads_of(a.np), smem, st>>>(a, max_tiles, total, per);
   return cudaGetLastError();
 }
 
