@@ -60,7 +60,7 @@ constexpr int kFirstEpiWarp = kProducers + kIssuers;
 __host__ __device__ constexpr int threads_of(int np) { return 32 * (kFirstEpiWarp + 4 * acc_of(np)); }
 constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
-constexpr int kRound = 64;               // accumulator columns read per TMEM load round in the epilogue
+constexpr int kRound = 32;               // accumulator columns read per TMEM load round in the epilogue
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
 
 // Per-row query record built by k_qprep: B codes (NP x 64 B, K-major no-swizzle:
@@ -239,9 +239,19 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
   // SFB: one copy per (issuer, B slot) at col_sfb + 8 * (2 * issuer + slot)
   const uint32_t col_sfa = kAcc * np, col_sfb = kAcc * np + 8 * kAcc;
 
-  // Every role walks the same (row, tile) sequence and skips the same empty
-  // tiles; a row's visible tile count is read once, when the walk enters it.
+  // Every role walks the rows of the CTA's item range in order and, in each
+  // row with visible tiles, visits its own tiles directly: tile j (counted over
+  // the visible tiles of the range) belongs to producer j % 2, issuer j % 2 and
+  // accumulator j % kAcc.
   const int tile_begin = static_cast<int>(i0 - static_cast<int64_t>(row0) * max_tiles);
+  // visible tiles [t0, t1) of row r inside the item range
+  auto row_span = [&](int r, int &t0, int &t1) {
+    t0 = r == row0 ? tile_begin : 0;
+    const int end_item = r == row_last ? static_cast<int>(i1 - static_cast<int64_t>(row_last) * max_tiles) : max_tiles;
+    t1 = min(end_item, tiles_of(r));
+  };
+  // the first tile t >= t0 of a row whose visible tiles start at count jrow with (jrow + t - t0) % mod == q
+  auto first_own = [](int t0, int jrow, int mod, int q) { return t0 + ((q - jrow % mod) % mod + mod) % mod; };
 
   if ((warp == 0 && (lane == 0 || pool_mode)) || (warp > 0 && warp < kProducers && lane == 0 && !pool_mode)) {
     // ------------------------------------------------------------ producers
@@ -249,34 +259,31 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
     // tile; POOL: warp 0 gathers every tile.  Producer 0 also loads each row's
     // query record into a B slot.
     const int pw = warp, nprod = pool_mode ? 1 : kProducers;
-    int prev_row = -1, bchanges = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0), mine = 0;
-    for (int64_t it = i0; it < i1; ++it) {
-      if (tile < nt) {
-        const int s = j % kStages;
-        bool ok = true;
-        if (row != prev_row) {
-          const int bs = bchanges & 1;
-          if (pw == 0) {
-            if (bchanges >= 2) {
-              ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
-                             : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
-              if (!ok) break;
-            }
-            if (lane == 0) {
-              tc::mbar_expect_tx(&sm.bfull[bs], brec);
-              bulk_g2s(tc::smem_addr(sm.bslot[bs]), a.qrec + static_cast<size_t>(row) * brec, brec, &sm.bfull[bs]);
-            }
-          }
-          prev_row = row;
-          ++bchanges;
+    int bchanges = 0, jrow = 0, mine = 0;
+    bool ok = true;
+    for (int row = row0; row <= row_last && ok; ++row) {
+      int t0, t1;
+      row_span(row, t0, t1);
+      if (t1 <= t0) continue;
+      const int bs = bchanges & 1;
+      if (pw == 0) {
+        if (bchanges >= 2) {
+          ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
+                         : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
+          if (!ok) break;
         }
-        if (j % nprod != pw) {
-          ++j;
-        } else {
+        if (lane == 0) {
+          tc::mbar_expect_tx(&sm.bfull[bs], brec);
+          bulk_g2s(tc::smem_addr(sm.bslot[bs]), a.qrec + static_cast<size_t>(row) * brec, brec, &sm.bfull[bs]);
+        }
+      }
+      ++bchanges;
+      const int seq = a.s.cache_seq < 0 ? row : a.s.cache_seq;
+      for (int tile = first_own(t0, jrow, nprod, pw); tile < t1; tile += nprod) {
+        const int j = jrow + (tile - t0), s = j % kStages;
         if (j >= kStages) ok = pool_mode ? wait_warp(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err)
                                          : wait1(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err);
         if (!ok) break;
-        const int seq = a.s.cache_seq < 0 ? row : a.s.cache_seq;
         uint8_t *dst = sm.stage[s];
         if (!pool_mode) {
           const size_t t = static_cast<size_t>(seq * seq_tiles + tile);
@@ -310,15 +317,9 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&sm.full[s]);
         }
-        ++j;
-        mine = j;
-        }
+        mine = j + 1;
       }
-      if (++tile == max_tiles) {
-        tile = 0;
-        ++row;
-        if (it + 1 < i1) nt = tiles_of(row);
-      }
+      jrow += t1 - t0;
     }
     if (lane == 0) sm.issued[pw] = mine;
   } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
@@ -327,48 +328,43 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
     // and stages who, who + kIssuers, ...); each keeps its own copy of the row's
     // query scale factors in TMEM
     const int who = warp - kProducers;
-    int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
+    int bchanges = 0, jrow = 0;
     const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
     bool dead = false;
-    for (int64_t it = i0; it < i1 && !dead; ++it) {
-      if (tile < nt) {
-        const int s = j % kStages, acc = j % kAcc;
-        if (row != prev_row) {
-          bs = bchanges & 1;
-          if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
-            dead = true;
-            break;
-          }
-          prev_row = row;
-          ++bchanges;
-          tc::tc_fence_after();
-          tc::tmem_cp_32x128b_x4(tmem + col_sfb + 8 * (2 * who + bs),
-                                 tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
-        }
-        if (j % kIssuers == who) {
-          if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) break;
-          if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) break;
-          tc::tc_fence_after();
-          const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
-          const uint32_t sfb = tmem + col_sfb + 8 * (2 * who + bs);
-          tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
-          const uint32_t d = tmem + acc * np;
-          tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
-                       tmem + col_sfa + 8 * acc, sfb, 0);
-          tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
-                       tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb, 1);
-          tc::mma_commit(&sm.empty[s]);
-          tc::mma_commit(&sm.tfull[acc]);
-        }
-        // the row's B slot is free once both issuers' MMAs of the row are done
-        if (tile + 1 >= nt || it + 1 >= i1) tc::mma_commit(&sm.bempty[bs]);
-        ++j;
+    for (int row = row0; row <= row_last && !dead; ++row) {
+      int t0, t1;
+      row_span(row, t0, t1);
+      if (t1 <= t0) continue;
+      const int bs = bchanges & 1;
+      if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
+        dead = true;
+        break;
       }
-      if (++tile == max_tiles) {
-        tile = 0;
-        ++row;
-        if (it + 1 < i1) nt = tiles_of(row);
+      ++bchanges;
+      tc::tc_fence_after();
+      const uint32_t sfb = tmem + col_sfb + 8 * (2 * who + bs);
+      tc::tmem_cp_32x128b_x4(sfb, tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
+      for (int tile = first_own(t0, jrow, kIssuers, who); tile < t1; tile += kIssuers) {
+        const int j = jrow + (tile - t0), s = j % kStages, acc = j % kAcc;
+        if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err) ||
+            (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err))) {
+          dead = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
+        tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
+        const uint32_t d = tmem + acc * np;
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
+                     tmem + col_sfa + 8 * acc, sfb, 0);
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
+                     tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb, 1);
+        tc::mma_commit(&sm.empty[s]);
+        tc::mma_commit(&sm.tfull[acc]);
       }
+      // the row's B slot is free once both issuers' MMAs of the row are done
+      if (!dead) tc::mma_commit(&sm.bempty[bs]);
+      jrow += t1 - t0;
     }
   } else if (warp >= kFirstEpiWarp) {
     // ------------------------------------------------------------ epilogue
@@ -376,19 +372,18 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
     const int parity = e >> 2;        // accumulator buffer this warp drains (tiles j % kAcc == parity)
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int m = 32 * quarter + lane;
-    int prev_row = -1, bchanges = 0, bs = 0, j = 0, row = row0, tile = tile_begin, nt = tiles_of(row0);
-    int64_t row_nslots = row_slots(a, row0);
     const int64_t aux_row = aux_row_bytes(a.s.stride);
+    int bchanges = 0, jrow = 0;
     bool dead = false;
-    for (int64_t it = i0; it < i1; ++it) {
-      if (tile < nt) {
-        if (row != prev_row) {
-          bs = bchanges & 1;
-          prev_row = row;
-          ++bchanges;
-        }
-        const bool last_of_row = tile + 1 >= nt || it + 1 >= i1;
-        if (j % kAcc == parity && !dead) {
+    for (int row = row0; row <= row_last; ++row) {
+      int t0, t1;
+      row_span(row, t0, t1);
+      if (t1 <= t0) continue;
+      const int bs = bchanges & 1;
+      ++bchanges;
+      const int64_t row_nslots = row_slots(a, row);
+      for (int tile = first_own(t0, jrow, kAcc, parity); tile < t1 && !dead; tile += kAcc) {
+        const int j = jrow + (tile - t0);
           // each warp of the group waits for the accumulator itself and hands
           // its lane quarter back on its own (tempty counts four arrivals)
           int ok = 1;
@@ -431,7 +426,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
 #pragma unroll
                   for (int k = 0; k < 4; ++k) {
                     const float d = __uint_as_float(r[c][4 * q + k]);
-                    acc = __fmaf_rn(wq[k], d > 0.0f ? d : 0.0f, acc);
+                    acc = __fmaf_rn(wq[k], fmaxf(d, 0.0f), acc);  // ReLU; NaN -> 0, -0 adds nothing
                   }
                 }
               }
@@ -467,9 +462,10 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
               }
             }
           }
-        }
-        if (last_of_row && lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
-        if (last_of_row && a.s.aux) {
+      }
+      jrow += t1 - t0;
+      if (lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
+      if (a.s.aux) {
           // every epilogue warp is done with this row: add the CTA's histograms
           // to the row's sideband and clear them
           asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
@@ -483,16 +479,6 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
           }
           asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
         }
-        ++j;
-      }
-      if (++tile == max_tiles) {
-        tile = 0;
-        ++row;
-        if (it + 1 < i1) {
-          nt = tiles_of(row);
-          row_nslots = row_slots(a, row);
-        }
-      }
     }
   }
 
