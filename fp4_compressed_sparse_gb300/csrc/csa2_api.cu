@@ -290,12 +290,6 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, con
     t.err = err_word;
     return cuda_status(csa2::launch_fill_aux(t, static_cast<uint8_t *>(score_aux), s), "csa2_index_score sideband");
   }
-  if (score_aux) {
-    // the histograms are accumulated by the kernel: start from zero
-    cudaError_t e = cudaMemset2DAsync(score_aux, csa2::aux_row_bytes(score_stride), 0, 2 * csa2::kSelBins * 4,
-                                      cache->batch, s);
-    if (e != cudaSuccess) return cuda_status(e, "csa2_index_score sideband clear");
-  }
   return cuda_status(csa2::launch_index_score_tc(a, ws, s), "csa2_index_score launch");
 }
 
@@ -528,8 +522,6 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     sa.stride = cache->capacity;
     sa.aux = wb + L.off_aux;
     sa.err = err_word;
-    e = cudaMemset2DAsync(sa.aux, csa2::aux_row_bytes(cache->capacity), 0, 2 * csa2::kSelBins * 4, nq, s);
-    if (e != cudaSuccess) return cuda_status(e, "prefill sideband clear");
     e = csa2::launch_index_score_tc(sa, wb + L.off_qrec, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill score");
     csa2::TopkArgs se{};

@@ -41,7 +41,7 @@ struct ScoreArgs {
   int pool_blocks, pool_bs;
   float *scores;              // [rows][stride]
   int64_t stride;
-  uint8_t *aux;               // [rows][aux_row_bytes(stride)] zeroed histograms, or nullptr
+  uint8_t *aux;               // [rows][aux_row_bytes(stride)] sideband (its histograms are cleared by the launch), or nullptr
   int32_t *err;
 };
 cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);  // CUDA cores (dp4a), no sideband

@@ -60,6 +60,7 @@ constexpr int kFirstEpiWarp = kProducers + kIssuers;
 __host__ __device__ constexpr int threads_of(int np) { return 32 * (kFirstEpiWarp + 4 * acc_of(np)); }
 constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
+constexpr int kTouchCap = 2048;          // touched bins listed per histogram (more: the flush scans them all)
 constexpr int kRound = 32;               // accumulator columns read per TMEM load round in the epilogue
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
 
@@ -69,8 +70,16 @@ __host__ __device__ __forceinline__ int qrec_bytes(int np) { return np * 64 + 51
 
 // grid (rows, np / 8), 256 threads: one warp per (row, head); lane l quantises
 // dims 4l..4l+3 (MX block l / 8; the block's amax is a max over its 8 lanes).
-__global__ void __launch_bounds__(256) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out) {
+// With a sideband the blocks of a row also clear its two histograms, which
+// the score kernel then accumulates.
+__global__ void __launch_bounds__(256) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out,
+                                               uint8_t *aux, int64_t aux_row) {
   const int r = blockIdx.x, lane = threadIdx.x & 31;
+  if (aux) {
+    uint4 *hz = reinterpret_cast<uint4 *>(aux + static_cast<size_t>(r) * aux_row);
+    constexpr int kVec = 2 * kSelBins * 4 / 16;
+    for (int i = blockIdx.y * 256 + threadIdx.x; i < kVec; i += gridDim.y * 256) hz[i] = make_uint4(0, 0, 0, 0);
+  }
   const int h = blockIdx.y * 8 + (threadIdx.x >> 5);
   uint8_t *rec = out + static_cast<size_t>(r) * qrec_bytes(np);
   uint8_t *sfb = rec + np * 64;
@@ -142,6 +151,8 @@ struct __align__(1024) Smem {
   int issued[kProducers];  // tiles whose copies each producer started (written once, at exit)
   __align__(128) int nt[kMaxRowsPerCta];  // visible tiles of the rows this CTA touches (row - row0)
   uint32_t hist[2][kSelBins];  // this CTA's share of the current row's sideband histograms
+  uint16_t touched[2][kTouchCap];  // the bins of hist[h] that went from 0 to 1 in the current row
+  int ntouched[2];
 };
 static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "score kernel shared memory above the per-CTA limit");
 
@@ -161,6 +172,14 @@ __device__ __forceinline__ bool wait_warp(Smem &sm, uint64_t *bar, uint32_t phas
 }
 
 __device__ __forceinline__ uint32_t sel_key(float f) { return isnan(f) ? 0u : orderable(f); }
+
+// Count one key in bin b of histogram h; a bin's first key also lists the bin.
+__device__ __forceinline__ void note_bin(Smem &sm, int h, uint32_t b) {
+  if (atomicAdd(&sm.hist[h][b], 1u) == 0u) {
+    const int k = atomicAdd(&sm.ntouched[h], 1);
+    if (k < kTouchCap) sm.touched[h][k] = static_cast<uint16_t>(b);
+  }
+}
 
 // Named barrier over `count` threads returning the AND of `v` across them.
 __device__ __forceinline__ int bar_and(uint32_t id, uint32_t count, int v) {
@@ -217,6 +236,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       tc::mbar_init(&sm.bempty[i], kIssuers + kEpiWarps);
     }
     sm.abort = 0;
+    sm.ntouched[0] = sm.ntouched[1] = 0;
     for (int i = 0; i < kProducers; ++i) sm.issued[i] = 0;
     tc::fence_mbar_init();
   }
@@ -384,101 +404,118 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       const int64_t row_nslots = row_slots(a, row);
       for (int tile = first_own(t0, jrow, kAcc, parity); tile < t1 && !dead; tile += kAcc) {
         const int j = jrow + (tile - t0);
-          // each warp of the group waits for the accumulator itself and hands
-          // its lane quarter back on its own (tempty counts four arrivals)
-          int ok = 1;
-          if (lane == 0)
-            ok = wait1(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) &&
-                 wait1(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            dead = true;
-          } else {
-            tc::tc_fence_after();
-            const float4 *wv = reinterpret_cast<const float4 *>(sm.bslot[bs] + np * 64 + 512);  // head weights
-            const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
-            // up to kRound columns per round: every load of the round, then one
-            // wait; the fma chain runs over the heads in order
-            float acc = 0.0f;
+        // each warp of the group waits for the accumulator itself and hands
+        // its lane quarter back on its own (tempty counts four arrivals)
+        int ok = 1;
+        if (lane == 0)
+          ok = wait1(sm, &sm.bfull[bs], ((bchanges - 1) >> 1) & 1, a.s.err) &&
+               wait1(sm, &sm.tfull[parity], (j / kAcc) & 1, a.s.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          dead = true;
+        } else {
+          tc::tc_fence_after();
+          const float4 *wv = reinterpret_cast<const float4 *>(sm.bslot[bs] + np * 64 + 512);  // head weights
+          const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
+          // up to kRound columns per round: every load of the round, then one
+          // wait; the fma chain runs over the heads in order
+          float acc = 0.0f;
 #pragma unroll
-            for (int h0 = 0; h0 < np; h0 += kRound) {
-              constexpr int kMaxC = (np < kRound ? np : kRound) / 16;
-              const int nc = (np - h0 < kRound ? np - h0 : kRound) / 16;
-              uint32_t r[kMaxC][16];
+          for (int h0 = 0; h0 < np; h0 += kRound) {
+            constexpr int kMaxC = (np < kRound ? np : kRound) / 16;
+            const int nc = (np - h0 < kRound ? np - h0 : kRound) / 16;
+            uint32_t r[kMaxC][16];
 #pragma unroll
-              for (int c = 0; c < kMaxC; ++c)
-                if (c < nc) tc::tmem_ld_32x32b_x16(base + h0 + 16 * c, r[c]);
+            for (int c = 0; c < kMaxC; ++c)
+              if (c < nc) tc::tmem_ld_32x32b_x16(base + h0 + 16 * c, r[c]);
 #pragma unroll
-              for (int c = 0; c < kMaxC; ++c)
-                if (c < nc) tc::tmem_ld_wait_x16(r[c]);
-              if (h0 + kRound >= np) {
-                // every TMEM read of this warp is complete: hand its quarter back
-                tc::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
-              }
-#pragma unroll
-              for (int c = 0; c < kMaxC; ++c) {
-                if (c >= nc) break;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const float4 w4 = wv[(h0 + 16 * c) / 4 + q];
-                  const float wq[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    const float d = __uint_as_float(r[c][4 * q + k]);
-                    acc = __fmaf_rn(wq[k], fmaxf(d, 0.0f), acc);  // ReLU; NaN -> 0, -0 adds nothing
-                  }
-                }
-              }
+            for (int c = 0; c < kMaxC; ++c)
+              if (c < nc) tc::tmem_ld_wait_x16(r[c]);
+            if (h0 + kRound >= np) {
+              // every TMEM read of this warp is complete: hand its quarter back
+              tc::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(&sm.tempty[parity]);
             }
-            const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
-            bool valid;
-            if (!pool_mode) {
-              valid = slot < row_nslots;
-            } else {
-              const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
-                                      ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
-                                      : -1;
-              const int64_t T = a.s.q_pos[row] / a.s.ratio;
-              const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
-              valid = pid >= 0 && p < T && p < a.s.cap;
-              if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
-            }
-            if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
-            if (a.s.aux) {
-              // sideband: score-key histogram; FULL rows also the max of each
-              // 8-position block (8 consecutive lanes) and its histogram
-              if (valid) atomicAdd(&sm.hist[0][sel_key(acc) >> kSelBinShift], 1u);
-              if (!pool_mode) {
-                float v = valid ? acc : -INFINITY;
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
-                v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-                if ((lane & 7) == 0 && valid) {
-                  float *bm = reinterpret_cast<float *>(a.s.aux + static_cast<size_t>(row) * aux_row + 2 * kSelBins * 4);
-                  bm[slot / 8] = v;
-                  atomicAdd(&sm.hist[1][sel_key(v) >> kSelBinShift], 1u);
+#pragma unroll
+            for (int c = 0; c < kMaxC; ++c) {
+              if (c >= nc) break;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 w4 = wv[(h0 + 16 * c) / 4 + q];
+                const float wq[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float d = __uint_as_float(r[c][4 * q + k]);
+                  acc = __fmaf_rn(wq[k], fmaxf(d, 0.0f), acc);  // ReLU; NaN -> 0, -0 adds nothing
                 }
               }
             }
           }
+          const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
+          bool valid;
+          if (!pool_mode) {
+            valid = slot < row_nslots;
+          } else {
+            const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
+                                    ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
+                                    : -1;
+            const int64_t T = a.s.q_pos[row] / a.s.ratio;
+            const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
+            valid = pid >= 0 && p < T && p < a.s.cap;
+            if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
+          }
+          if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
+          if (a.s.aux) {
+            // sideband: score-key histogram; FULL rows also the max of each
+            // 8-position block (8 consecutive lanes) and its histogram
+            if (valid) note_bin(sm, 0, sel_key(acc) >> kSelBinShift);
+            if (!pool_mode) {
+              float v = valid ? acc : -INFINITY;
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+              v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+              if ((lane & 7) == 0 && valid) {
+                float *bm = reinterpret_cast<float *>(a.s.aux + static_cast<size_t>(row) * aux_row + 2 * kSelBins * 4);
+                bm[slot / 8] = v;
+                note_bin(sm, 1, sel_key(v) >> kSelBinShift);
+              }
+            }
+          }
+        }
       }
       jrow += t1 - t0;
       if (lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
       if (a.s.aux) {
-          // every epilogue warp is done with this row: add the CTA's histograms
-          // to the row's sideband and clear them
-          asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
-          uint32_t *gh = reinterpret_cast<uint32_t *>(a.s.aux + static_cast<size_t>(row) * aux_row);
-          for (int i = threadIdx.x - 32 * kFirstEpiWarp; i < 2 * kSelBins; i += kEpiWarps * 32) {
-            const uint32_t c = (&sm.hist[0][0])[i];
-            if (c) {
-              atomicAdd(&gh[i], c);
-              (&sm.hist[0][0])[i] = 0;
+        // every epilogue warp is done with this row: add the CTA's histograms
+        // to the row's sideband and clear them (only the listed bins, unless
+        // more bins were touched than the list holds)
+        const int et = threadIdx.x - 32 * kFirstEpiWarp;
+        asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+        const int n0 = sm.ntouched[0], n1 = sm.ntouched[1];
+        asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+        if (et == 0) sm.ntouched[0] = sm.ntouched[1] = 0;
+        uint32_t *gh = reinterpret_cast<uint32_t *>(a.s.aux + static_cast<size_t>(row) * aux_row);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = h == 0 ? n0 : n1;
+          if (n <= kTouchCap) {
+            for (int i = et; i < n; i += kEpiWarps * 32) {
+              const uint32_t b = sm.touched[h][i];
+              atomicAdd(&gh[h * kSelBins + b], sm.hist[h][b]);
+              sm.hist[h][b] = 0;
+            }
+          } else {
+            for (int b = et; b < kSelBins; b += kEpiWarps * 32) {
+              const uint32_t c = sm.hist[h][b];
+              if (c) {
+                atomicAdd(&gh[h * kSelBins + b], c);
+                sm.hist[h][b] = 0;
+              }
             }
           }
-          asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
         }
+        asm volatile("bar.sync 1, %0;\n" ::"r"(kEpiWarps * 32) : "memory");
+      }
     }
   }
 
@@ -514,7 +551,8 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   a.qrec = static_cast<const uint8_t *>(ws);
   const int cols = acc_of(a.np) * a.np + 8 * acc_of(a.np) + 8 * 2 * kIssuers;
   a.ncols = cols <= 128 ? 128 : (cols <= 256 ? 256 : 512);
-  k_qprep<<<dim3(s.rows, a.np / 8), 256, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws));
+  k_qprep<<<dim3(s.rows, a.np / 8), 256, 0, st>>>(s.q_idx, s.w, s.heads, a.np, static_cast<uint8_t *>(ws), s.aux,
+                                                  static_cast<int64_t>(aux_row_bytes(s.stride)));
   const int max_tiles = static_cast<int>(
       s.pool ? (static_cast<int64_t>(s.pool_blocks) * s.pool_bs + kIdxTile - 1) / kIdxTile
              : idx_tiles(s.cap < s.stride ? s.cap : s.stride));
