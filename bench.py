@@ -49,9 +49,12 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def score_traffic():
+def score_traffic(workload):
     """dram read + write bytes per launch of the score kernel from the committed ncu
-    summary, or None when the kernel source has changed since that capture."""
+    summary of the B 32 x 65,536 decode workload, or None for another workload or
+    when the kernel source has changed since that capture."""
+    if workload != "full_decode_b32_t65536":
+        return None
     import hashlib
     here = os.path.dirname(os.path.abspath(__file__))
     prof = os.path.join(here, "profiles", "index_score_tc_full_decode_b32_t65536.md")
@@ -436,7 +439,7 @@ def run_ours(args):
                    "frac": round(kv_gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind},
         "roofline": {"kernel": "index_score (Full scan: query prep + tensor-core score + sideband)", "bound": "hbm",
                      "achieved": round(achieved, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": score_traffic(),
+                     "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": score_traffic(W.name),
                      "algorithmic_bytes_per_launch": score_bytes, "avg_launch_ms": round(score_avg, 5),
                      "peak_kind": hbm_kind},
         "step_breakdown_ms": {k: round(statistics.mean(v), 5) for k, v in parts.items()},
