@@ -215,7 +215,8 @@ struct SelSmem {
   uint32_t warp_tot[kSelWarps + 1];
   uint32_t dhist[256];
   uint64_t prefix;
-  uint32_t thr, above, total, ncand, overflow, rem, done, cnt;
+  uint32_t thr, above, total, ncand, overflow, rem, done;
+  uint32_t cnt_below;  // chosen slots in the lower-ranked slices (their CTAs add to it)
 };
 
 // Key of slot `slot` (valid only when *ok): reads of one warp step go to 32
@@ -304,6 +305,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
     for (int i = tid; i < kSelBins / 4; i += kSelThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
     if (tid == 0) {
       sm.ncand = 0;
+      sm.cnt_below = 0;
       sm.overflow = 0;
       sm.rem = 0;
       sm.done = 0;
@@ -492,9 +494,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
   for (int64_t w = wb; w < we; ++w) c += __popc(bm_local[w]);
   uint32_t tot;
   uint32_t off = block_excl_scan(c, sm.warp_tot, &tot);
-  if (tid == 0) sm.cnt = tot;
-  cluster_sync();  // #3: every slice's count published
-  for (uint32_t r = 0; r < rank; ++r) off += ld_dsmem_u32(&sm.cnt, r);
+  // every higher-ranked slice starts after this one: add this slice's count to
+  // theirs (cnt_below was cleared before barrier #1)
+  if (tid > 0 && tid < kSelCluster && static_cast<uint32_t>(tid) > rank)
+    asm volatile("red.shared::cluster.add.u32 [%0], %1;\n" ::"r"(dsmem_addr(&sm.cnt_below, tid)), "r"(tot) : "memory");
+  cluster_sync();  // #3: every slice's count added; no shared memory of a peer is touched after it
+  off += sm.cnt_below;
   int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
                         : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
   for (int64_t w = wb; w < we; ++w) {
@@ -511,7 +516,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
     for (int i = kt + tid; i < kout; i += kSelThreads) out[i] = -1;
     if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
   }
-  cluster_sync();  // #4: no CTA leaves while a peer may still read its shared memory
 }
 
 }  // namespace
