@@ -461,7 +461,10 @@ def run_ours(args):
 def run_e2e(bench, W, args, dev, flush):
     """Same metric through the public calls with host buffers: every step copies its
     inputs (new token, indexer query, head weights, query, positions) from pinned host
-    memory and reads the step's result (attention output + lse) back to the host."""
+    memory and reads the step's result (attention output + lse) back to the host.
+    Like the device-timed steps, each step (copies in, the public calls, copies out)
+    is launched as one CUDA graph, as a serving loop would; --no-graph launches the
+    calls one by one instead."""
     first = args.warmup + args.steps
     names = ("kv_new", "ik_new", "q_idx", "w", "q", "q_pos")
     host_in = [[getattr(bench, n)[first + s].cpu().pin_memory() for n in names]
@@ -473,16 +476,44 @@ def run_e2e(bench, W, args, dev, flush):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     for n, d in zip(names, dev_in):  # the step reads slot `first` of each input list
         getattr(bench, n)[first] = d
+    # the inputs of the score (indexer query, weights, positions) are copied on the
+    # main stream; the new token and the attention query on the side branch, where
+    # they overlap the score and the top-k (the attention waits for that branch)
+    side_names = ("kv_new", "ik_new", "q")
+
+    def one_step(s):
+        main = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(main)
+        bench.side.wait_event(fork)
+        for n, d, h in zip(names, dev_in, host_in[s]):
+            if n in side_names:
+                with torch.cuda.stream(bench.side):
+                    d.copy_(h, non_blocking=True)
+            else:
+                d.copy_(h, non_blocking=True)
+        bench.step(first)
+        out_h.copy_(bench.out, non_blocking=True)
+        lse_h.copy_(bench.lse, non_blocking=True)
+
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        for s in range(args.e2e_steps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                one_step(s)
+            graphs.append(g)
+        torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total = 0.0
     for s in range(args.e2e_steps):
         flush()
         start.record()
-        for d, h in zip(dev_in, host_in[s]):
-            d.copy_(h, non_blocking=True)
-        bench.step(first)
-        out_h.copy_(bench.out, non_blocking=True)
-        lse_h.copy_(bench.lse, non_blocking=True)
+        if graphs is not None:
+            graphs[s].replay()
+        else:
+            one_step(s)
         end.record()
         torch.cuda.synchronize()
         total += start.elapsed_time(end)
