@@ -75,6 +75,9 @@ __host__ __device__ __forceinline__ int qrec_bytes(int np) { return np * 64 + 51
 __global__ void __launch_bounds__(256) k_qprep(const uint16_t *q_idx, const float *w, int H, int np, uint8_t *out,
                                                uint8_t *aux, int64_t aux_row) {
   const int r = blockIdx.x, lane = threadIdx.x & 31;
+  // the scan may start its prologue and key-tile copies now; it waits for this
+  // grid before it reads a query record or adds to a histogram
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   if (aux) {
     uint4 *hz = reinterpret_cast<uint4 *>(aux + static_cast<size_t>(r) * aux_row);
     constexpr int kVec = 2 * kSelBins * 4 / 16;
@@ -287,6 +290,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       if (t1 <= t0) continue;
       const int bs = bchanges & 1;
       if (pw == 0) {
+        if (bchanges == 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the query prep is complete
         if (bchanges >= 2) {
           ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
                          : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
@@ -486,6 +490,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       jrow += t1 - t0;
       if (lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
       if (a.s.aux) {
+        if (bchanges == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the histograms are cleared
         // every epilogue warp is done with this row: add the CTA's histograms
         // to the row's sideband and clear them (only the listed bins, unless
         // more bins were touched than the list holds)
@@ -587,8 +592,17 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   }
   const int64_t grid = total < num_sms ? total : num_sms;
   const int64_t per = (total + grid - 1) / grid;
-  fn<<<static_cast<unsigned>(grid), threads_of(a.np), smem, st>>>(a, max_tiles, total, per);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(threads_of(a.np));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the query prep's tail
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, a, max_tiles, total, per);
 }
 
 }  // namespace csa2
