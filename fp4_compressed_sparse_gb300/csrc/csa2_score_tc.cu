@@ -204,7 +204,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                : "memory");
 }
 
-template <int NP>
+// kFullAux: the Full-layer scan with a sideband (no pool, aux present), fixed at
+// compile time so that its per-key path carries no mode tests
+template <int NP, bool kFullAux>
 __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, int max_tiles, int64_t total_items,
                                                                 int64_t per_cta) {
   extern __shared__ uint8_t smem_raw[];
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
   constexpr int kAcc = acc_of(NP), kEpiWarps = 4 * kAcc;
   static_assert(kAcc % kIssuers == 0, "each accumulator must be fed by one issuer");
   const int brec = qrec_bytes(np);
-  const bool pool_mode = a.s.pool != nullptr;
+  const bool pool_mode = kFullAux ? false : a.s.pool != nullptr;
+  const bool has_aux = kFullAux ? true : a.s.aux != nullptr;
   const int64_t seq_tiles = idx_tiles(a.s.cap);
 
   if (warp == 0) {
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
             if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
           }
           if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
-          if (a.s.aux) {
+          if (has_aux) {
             // sideband: score-key histogram; FULL rows also the max of each
             // 8-position block (8 consecutive lanes) and its histogram
             if (valid) note_bin(sm, 0, sel_key(acc) >> kSelBinShift);
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       }
       jrow += t1 - t0;
       if (lane == 0) tc::mbar_arrive(&sm.bempty[bs]);
-      if (a.s.aux) {
+      if (has_aux) {
         if (bchanges == 1) asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the histograms are cleared
         // every epilogue warp is done with this row: add the CTA's histograms
         // to the row's sideband and clear them (only the listed bins, unless
@@ -573,18 +576,21 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   const size_t smem = sizeof(Smem) + 1024;
   using KernelFn = void (*)(TcArgs, int, int64_t, int64_t);
   KernelFn fn = nullptr;
+  const bool full_aux = s.pool == nullptr && s.aux != nullptr;
+#define CSA2_SCORE_FN(N) (full_aux ? k_index_score_tc<N, true> : k_index_score_tc<N, false>)
   switch (a.np) {
-    case 16: fn = k_index_score_tc<16>; break;
-    case 32: fn = k_index_score_tc<32>; break;
-    case 48: fn = k_index_score_tc<48>; break;
-    case 64: fn = k_index_score_tc<64>; break;
-    case 80: fn = k_index_score_tc<80>; break;
-    case 96: fn = k_index_score_tc<96>; break;
-    case 112: fn = k_index_score_tc<112>; break;
-    default: fn = k_index_score_tc<128>; break;
+    case 16: fn = CSA2_SCORE_FN(16); break;
+    case 32: fn = CSA2_SCORE_FN(32); break;
+    case 48: fn = CSA2_SCORE_FN(48); break;
+    case 64: fn = CSA2_SCORE_FN(64); break;
+    case 80: fn = CSA2_SCORE_FN(80); break;
+    case 96: fn = CSA2_SCORE_FN(96); break;
+    case 112: fn = CSA2_SCORE_FN(112); break;
+    default: fn = CSA2_SCORE_FN(128); break;
   }
-  static bool attr[9] = {};
-  const int slot = a.np / 16;
+#undef CSA2_SCORE_FN
+  static bool attr[18] = {};
+  const int slot = a.np / 16 + (full_aux ? 9 : 0);
   if (!attr[slot]) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
