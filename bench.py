@@ -524,6 +524,243 @@ def run_e2e(bench, W, args, dev, flush):
             "steps": args.e2e_steps, "ms_per_step": round(total / args.e2e_steps, 4)}
 
 
+# ----------------------------------------------------------------------------- secondary workloads
+# The configurations besides the headline, timed the same way (one CUDA graph per
+# step, L2 flushed between steps, CUDA events on the launching stream).  Each prints
+# its own JSON line; the headline line above is the Full-layer decode.
+
+def group_step_bytes(W, T):
+    """Algorithmic HBM bytes of one decoder-group step (append excluded): per layer
+    what the method must move, summed over the group's layers."""
+    B, k, H, H_I = W.batch, W.topk, W.heads, W.index_heads
+    swa = 128 * (594 if W.swa_dtype == 1 else 1152)
+    attn = k * (324 + 4) + swa + H * 576 * 2 + H * 512 * 4      # per sequence and attention layer
+    qidx = H_I * 128 * 2 + 4 * H_I
+    per_seq = 0
+    for role in W.layers:
+        if role == "full":
+            per_seq += T * 68 + qidx + attn
+        elif role == "reindex":
+            per_seq += W.pool_blocks * W.pool_block_size * 68 + W.pool_blocks * 4 + qidx + attn
+        else:
+            per_seq += attn
+    return B * per_seq
+
+
+class GroupDecode:
+    """A decoder group at a decode step on one cache: append the step's token, then
+    each layer of W.layers in order -- "full": score every visible position, top-k and
+    the 2,048-block pool, attention; "reindex": score the positions of the pool, top-k,
+    attention; "reuse": attention with the last indexer layer's indices.  Every layer
+    has its own queries; the layers share the cache (a model's layers have caches of
+    the same shape, and the kernels read them the same way)."""
+
+    def __init__(self, W, n_steps, device):
+        from fp4_compressed_sparse_gb300 import csa2
+        from fp4_compressed_sparse_gb300 import workloads as wl
+        self.csa2, self.W = csa2, W
+        B, ctx, nl = W.batch, W.context, len(W.layers)
+        self.cap = ctx + n_steps + 8
+        self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
+        self.rope = csa2.rope_table(W.theta, self.cap + 8)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        chunk = max(256, min(wl.CHUNK, (1 << 29) // (B * 576 * 4)))  # bound each staging copy to ~512 MB
+        for t0 in range(0, ctx, chunk):
+            n = min(chunk, ctx - t0)
+            kv = torch.stack([W.kv(b, t0, n, device=device) for b in range(B)])
+            ik = torch.stack([W.ik(b, t0, n, device=device) for b in range(B)])
+            csa2.kv_append(self.cache, kv, ik, self.rope, err=self.err)
+            del kv, ik
+        torch.cuda.synchronize()
+        self.kv_new = [torch.stack([W.kv(b, ctx + s, 1, device=device) for b in range(B)]) for s in range(n_steps)]
+        self.ik_new = [torch.stack([W.ik(b, ctx + s, 1, device=device) for b in range(B)]) for s in range(n_steps)]
+        self.q_pos = [torch.full((B,), ctx + s, dtype=torch.int64, device=device) for s in range(n_steps)]
+        self.q_idx = [[W.q_idx(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
+        self.w = [[W.w(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
+        self.q = [[W.q(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
+        has_full = "full" in W.layers
+        # a group without a Full layer scores inside the prior pool (uniformly drawn blocks)
+        self.pool = (torch.empty((B, W.pool_blocks), dtype=torch.int32, device=device) if has_full
+                     else W.pool(device=device))
+        self.pool_cnt = torch.empty((B,), dtype=torch.int32, device=device)
+        pstride = W.pool_blocks * W.pool_block_size
+        self.scores = torch.empty((B, self.cap), device=device)
+        self.pscores = torch.empty((B, pstride), device=device)
+        self.aux = csa2.score_aux(B, self.cap)
+        self.paux = csa2.score_aux(B, pstride)
+        self.idx = torch.empty((B, W.topk), dtype=torch.int32, device=device)
+        self.out = torch.empty((B, W.heads, 512), device=device)
+        self.lse = torch.empty((B, W.heads), device=device)
+        self.ws_score = csa2.index_score_workspace(B, W.index_heads)
+        self.ws_topk = csa2.topk_workspace(B, self.cap, W.topk, W.pool_blocks)
+        self.ws_ptopk = csa2.topk_workspace(B, pstride, W.topk)
+        self.ws_attn = csa2.attn_workspace(B, W.heads, W.topk)
+        self.side = torch.cuda.Stream(device=device)
+
+    def step(self, s, marks=None):
+        """One step; with `marks` (a list of events) the parts run in order on one stream
+        with an event before each layer's indexer part, each attention and the end."""
+        c, W = self.csa2, self.W
+        main = torch.cuda.current_stream()
+        mark = (lambda: marks.pop(0).record()) if marks is not None else (lambda: None)
+        if marks is not None:
+            c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+        else:
+            fork, join = torch.cuda.Event(), torch.cuda.Event()
+            fork.record(main)
+            self.side.wait_event(fork)
+            with torch.cuda.stream(self.side):
+                c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+            join.record(self.side)
+        joined = marks is not None
+        for l, role in enumerate(W.layers):
+            mark()
+            if role == "full":
+                c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.scores, err=self.err,
+                              ws=self.ws_score, aux=self.aux)
+                c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
+                       pool_count=self.pool_cnt, err=self.err, aux=self.aux)
+            elif role == "reindex":
+                c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.pscores,
+                              pool=self.pool, err=self.err, ws=self.ws_score, aux=self.paux)
+                c.topk(self.pscores, 1, self.q_pos[s], W.topk, self.idx, self.ws_ptopk, pool=self.pool,
+                       err=self.err, aux=self.paux)
+            if not joined:
+                main.wait_event(join)  # the attention reads the new token's window slot
+                joined = True
+            mark()
+            c.sparse_attn_decode(self.cache, self.q[s][l], self.q_pos[s], self.idx, self.out, self.lse,
+                                 self.ws_attn, W.sm_scale, err=self.err)
+        mark()
+
+
+class PrefillBench:
+    """Encoder-style chunked prefill (ratio 2): one step = csa2_prefill_chunk of the
+    chunk's tokens against the prior entries.  The cache's token count, window ring
+    and compression buffer are put back before every step (outside the timed region),
+    so that every step appends the same chunk at the same positions."""
+
+    def __init__(self, W, device):
+        from fp4_compressed_sparse_gb300 import csa2
+        from fp4_compressed_sparse_gb300 import workloads as wl
+        self.csa2, self.W = csa2, W
+        self.cap = (W.prior + W.chunk) // 2 + 8
+        c = self.cache = csa2.Cache(1, self.cap, ratio=2, swa_dtype=W.swa_dtype)
+        self.rope = csa2.rope_table(W.theta, 2 * self.cap + 16)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ba, self.bb = W.bias(device=device)
+        for t0 in range(0, W.prior, wl.CHUNK):
+            rows = W.cmp_rows(t0, wl.CHUNK, device=device)
+            csa2.kv_append(c, rope_cs=self.rope, cmp=[r[None] for r in rows] + [self.ba, self.bb], err=self.err)
+        torch.cuda.synchronize()
+        self.saved = [t.clone() for t in (c.n_tokens, c.swa_codes, c.swa_scales, c.cmp_buf)]
+        self.rows = list(W.cmp_rows(W.prior, W.chunk, device=device))
+        self.q_idx, self.w, self.q = W.q_idx(device=device), W.w(device=device), W.q(device=device)
+        Q, k = W.chunk, W.topk
+        self.idx = torch.empty((Q, k), dtype=torch.int32, device=device)
+        self.out = torch.empty((Q, W.heads, 512), device=device)
+        self.lse = torch.empty((Q, W.heads), device=device)
+        self.ws = csa2.prefill_workspace(Q, self.cap, W.index_heads, W.heads, k)
+
+    def restore(self):
+        c = self.cache
+        for dst, src in zip((c.n_tokens, c.swa_codes, c.swa_scales, c.cmp_buf), self.saved):
+            dst.copy_(src)
+
+    def step(self, s):
+        W = self.W
+        self.csa2.prefill_chunk(self.cache, 0, self.rows + [self.ba, self.bb], self.rope, self.q_idx, self.w, self.q,
+                                W.topk, W.sm_scale, self.idx, self.out, self.lse, self.ws, err=self.err)
+
+
+def run_secondary(args):
+    from fp4_compressed_sparse_gb300 import build_lib, csa2
+    from fp4_compressed_sparse_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build_lib.build()
+    csa2.load()
+    W = getattr(wl, args.workload)(device="cuda")
+    prefill = args.workload == "prefill_chunk"
+    steps = args.steps
+    bench = PrefillBench(W, dev) if prefill else GroupDecode(W, args.warmup + steps, dev)
+    flush = L2Flush(dev)
+    prep = bench.restore if prefill else (lambda: None)
+    for s in range(args.warmup):
+        prep()
+        flush()
+        bench.step(s)
+    torch.cuda.synchronize()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} during warm-up")
+    graphs = []
+    for i in range(steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            bench.step(0 if prefill else args.warmup + i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    t_begin = time.perf_counter()
+    for i in range(steps):
+        prep()
+        flush()
+        ev[i][0].record()
+        graphs[i].replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    sampler.mark(t_begin, time.perf_counter())
+    clocks = sampler.stop()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} in the timed steps")
+    ms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    hbm, hbm_kind = peaks()
+    line = {"workload": W.name, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "data": "synthetic (seeded)", "clocks": clocks, "impl": "ours",
+            "l2": "flushed between timed steps", "launch": "one CUDA graph per step"}
+    if prefill:
+        Q = W.chunk
+        # FP4 indexer scoring: 2 * H_I * 128 per (query, visible entry); query i sees prior/2 + i//2 entries
+        flop = sum(2 * W.index_heads * 128 * (W.prior // 2 + i // 2) for i in range(Q))
+        fp4_peak = None
+        try:
+            fp4_peak = json.load(open(PEAKS_FILE))["bf16_tflops"] * 6.0
+        except Exception:
+            fp4_peak = 1900.0 * 6.0
+        rate = flop / (ms / 1e3) / 1e12
+        line.update({"metric": "prefill chunk: query tokens/s, and FP4 scoring TFLOP/s over the whole chunk",
+                     "value": round(Q / (ms / 1e3), 2), "unit": "tokens/s", "higher_is_better": True,
+                     "scoring_tflop": round(flop / 1e12, 3),
+                     "tensor": {"achieved_tflops_lower_bound": round(rate, 1), "fp4_peak_tflops": round(fp4_peak, 1),
+                                "peak_kind": "measured bf16 x 6 (nominal fp4 / bf16)",
+                                "frac_lower_bound": round(rate / fp4_peak, 4),
+                                "note": "the whole chunk's time (append, scoring, top-k, attention) divides the scoring FLOP"}})
+    else:
+        # per-layer breakdown: one more step, parts in order with events between
+        # (the cache is then one token longer, which changes nothing measurable)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(W.layers) + 1)]
+        ev_list = list(marks)
+        flush()
+        bench.step(args.warmup + steps - 1, marks=ev_list)
+        torch.cuda.synchronize()
+        parts = []
+        for l, role in enumerate(W.layers):
+            a, b, c2 = marks[2 * l], marks[2 * l + 1], marks[2 * l + 2]
+            parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
+                          "attention_ms": round(b.elapsed_time(c2), 4)})
+        line["layer_breakdown"] = parts
+        T = W.context + args.warmup + steps // 2
+        nbytes = group_step_bytes(W, T)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        line.update({"metric": "decoder-group tokens/s and algorithmic HBM GB/s (% of roofline)",
+                     "value": round(W.batch / (ms / 1e3), 2), "unit": "tokens/s", "higher_is_better": True,
+                     "layers": list(W.layers), "batch": W.batch, "context": W.context,
+                     "kv_hbm": {"algorithmic_bytes_per_step": nbytes, "gbs": round(gbs, 1),
+                                "frac": round(gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind}})
+    print(json.dumps(line), flush=True)
+
 # ----------------------------------------------------------------------------- oracle arm
 def cpu_baseline(W, args, sample_steps=1):
     """The CPU oracle (as it stands) on a bounded sample of the workload: sequence 0,
@@ -583,7 +820,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="full_decode", choices=["full_decode", "full_decode_small", "tiny_decode"])
+    ap.add_argument("--workload", default="full_decode",
+                    choices=["full_decode", "full_decode_small", "tiny_decode", "reindex_decode", "stack_1m",
+                             "prefill_chunk"],
+                    help="full_decode is the headline; reindex_decode, stack_1m and prefill_chunk print their own "
+                         "measurement line")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -594,6 +835,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload in ("reindex_decode", "stack_1m", "prefill_chunk"):
+        run_secondary(args)
     else:
         run_ours(args)
 

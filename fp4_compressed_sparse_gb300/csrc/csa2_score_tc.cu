@@ -60,6 +60,7 @@ constexpr int kFirstEpiWarp = kProducers + kIssuers;
 __host__ __device__ constexpr int threads_of(int np) { return 32 * (kFirstEpiWarp + 4 * acc_of(np)); }
 constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
+constexpr int kGatherDepth = 4;          // POOL: gathered tiles in flight per producer warp
 constexpr int kTouchCap = 2048;          // touched bins listed per histogram (more: the flush scans them all)
 constexpr int kRound = 32;               // accumulator columns read per TMEM load round in the epilogue
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
@@ -279,14 +280,22 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
   // the first tile t >= t0 of a row whose visible tiles start at count jrow with (jrow + t - t0) % mod == q
   auto first_own = [](int t0, int jrow, int mod, int q) { return t0 + ((q - jrow % mod) % mod + mod) % mod; };
 
-  if ((warp == 0 && (lane == 0 || pool_mode)) || (warp > 0 && warp < kProducers && lane == 0 && !pool_mode)) {
+  if (warp < kProducers && (lane == 0 || pool_mode)) {
     // ------------------------------------------------------------ producers
-    // FULL: lane 0 of warps 0..kProducers-1, alternate tiles, two bulk copies per
-    // tile; POOL: warp 0 gathers every tile.  Producer 0 also loads each row's
-    // query record into a B slot.
-    const int pw = warp, nprod = pool_mode ? 1 : kProducers;
+    // FULL: lane 0 of each producer warp, alternate tiles, two bulk copies per
+    // tile.  POOL: every lane of each producer warp, alternate tiles, gathering
+    // with cp.async; a warp keeps kGatherDepth tiles in flight and hands a tile
+    // over once its copies have landed.  Producer 0 also loads each row's query
+    // record into a B slot.
+    const int pw = warp, nprod = kProducers;
     int bchanges = 0, jrow = 0, mine = 0;
     bool ok = true;
+    int npend = 0, jlast = 0;  // POOL: own tiles in flight, the newest one's index
+    auto hand_over = [&](int st) {
+      tc::fence_proxy_async_smem();  // the gathered tile is read by the tensor cores
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.full[st]);
+    };
     for (int row = row0; row <= row_last && ok; ++row) {
       int t0, t1;
       row_span(row, t0, t1);
@@ -295,6 +304,12 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       if (pw == 0) {
         if (bchanges == 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the query prep is complete
         if (bchanges >= 2) {
+          if (pool_mode) {
+            // the slot is freed by the MMAs of two rows back, which may need tiles
+            // this warp still has in flight: hand every one of them over first
+            asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+            for (; npend > 0; --npend) hand_over((jlast - (npend - 1) * nprod) % kStages);
+          }
           ok = pool_mode ? wait_warp(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err)
                          : wait1(sm, &sm.bempty[bs], ((bchanges >> 1) - 1) & 1, a.s.err);
           if (!ok) break;
@@ -319,34 +334,52 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
           bulk_g2s(tc::smem_addr(dst + kIdxTileCodeBytes), a.s.idx_scales + t * kIdxTileScaleBytes,
                    kIdxTileScaleBytes, &sm.full[s]);
         } else {
-          // 16 pool blocks of 8 keys: lane l handles block l/2, chunks 2*(l%2)..+1
+          // 16 pool blocks of 8 keys: lane l gathers block l/2, code chunks 2*(l%2)..+1
+          // and 4 of its scale words; outside the pool or the cache the copy reads
+          // nothing and writes zeros
           const int jb = lane >> 1;
           const int pidx = tile * 16 + jb;
           const int32_t pid =
               pidx < a.s.pool_blocks ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + pidx] : -1;
           const int64_t p0 = static_cast<int64_t>(pid) * a.s.pool_bs;
           const bool okb = pid >= 0 && p0 + a.s.pool_bs <= seq_tiles * kIdxTile;
+          const uint32_t d0 = tc::smem_addr(dst);
+#pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * (lane & 1) + cc;
+#pragma unroll
             for (int i = 0; i < 8; ++i) {
-              uint4 v = make_uint4(0, 0, 0, 0);
-              if (okb) v = *reinterpret_cast<const uint4 *>(a.s.idx_codes + idx_code_off(seq * seq_tiles, p0 + i, c));
-              *reinterpret_cast<uint4 *>(dst + c * 2048 + (jb * 8 + i) * 16) = v;
+              const uint8_t *src = okb ? a.s.idx_codes + idx_code_off(seq * seq_tiles, p0 + i, c) : a.s.idx_codes;
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d0 + c * 2048 + (jb * 8 + i) * 16),
+                           "l"(src), "r"(okb ? 16 : 0)
+                           : "memory");
             }
           }
-          for (int i = (lane & 1) * 4; i < (lane & 1) * 4 + 4; ++i) {
-            const int m = jb * 8 + i;
-            uint32_t v = 0;
-            if (okb) v = *reinterpret_cast<const uint32_t *>(a.s.idx_scales + idx_scale_off(seq * seq_tiles, p0 + i));
-            *reinterpret_cast<uint32_t *>(dst + kIdxTileCodeBytes + 16 * (m % 32) + 4 * (m / 32)) = v;
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const int i = (lane & 1) * 4 + i4, m = jb * 8 + i;
+            const uint8_t *src = okb ? a.s.idx_scales + idx_scale_off(seq * seq_tiles, p0 + i) : a.s.idx_scales;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(
+                             d0 + kIdxTileCodeBytes + 16 * (m % 32) + 4 * (m / 32)),
+                         "l"(src), "r"(okb ? 4 : 0)
+                         : "memory");
           }
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&sm.full[s]);
+          asm volatile("cp.async.commit_group;\n" ::: "memory");
+          jlast = j;
+          if (++npend == kGatherDepth) {
+            // the oldest tile in flight has landed: hand it over
+            asm volatile("cp.async.wait_group %0;\n" ::"n"(kGatherDepth - 1) : "memory");
+            hand_over((jlast - (npend - 1) * nprod) % kStages);
+            --npend;
+          }
         }
         mine = j + 1;
       }
       jrow += t1 - t0;
+    }
+    if (pool_mode) {  // every gathered tile still in flight (also after a wait gave up)
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      for (; npend > 0; --npend) hand_over((jlast - (npend - 1) * nprod) % kStages);
     }
     if (lane == 0) sm.issued[pw] = mine;
   } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
