@@ -35,7 +35,7 @@ namespace {
 constexpr int kChunk = 4096;  // slots per sideband-fill CTA
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelCluster = 4;               // CTAs per (row, problem): one cluster shares the row
+constexpr int kSelClusterMax = 8;            // CTAs per (row, problem), one cluster sharing the row: 4 or 8
 constexpr int64_t kSmemBitmapWords = 32768;  // a CTA's bitmap slice stays in shared memory up to 128 KB
 
 __device__ __forceinline__ uint32_t key_of(float f) { return isnan(f) ? 0u : orderable(f); }
@@ -259,14 +259,14 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // bitmap words of one cluster CTA: a multiple of 4 (the vector pass takes 4 words per step)
-__host__ __device__ __forceinline__ int64_t span_words(int64_t nw) {
-  return ((nw + kSelCluster - 1) / kSelCluster + 3) / 4 * 4;
+__host__ __device__ __forceinline__ int64_t span_words(int64_t nw, int ncl) {
+  return ((nw + ncl - 1) / ncl + 3) / 4 * 4;
 }
 
-// grid (kSelCluster, rows, problems), cluster (kSelCluster, 1, 1), kSelThreads;
+// grid (ncl, rows, problems), cluster (ncl, 1, 1), kSelThreads;
 // dynamic smem: SelSmem + this CTA's bitmap slice (when it fits)
 __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uint8_t *aux, int64_t aux_row,
-                                                           uint32_t *bitmap_g, int bitmap_in_smem) {
+                                                           uint32_t *bitmap_g, int bitmap_in_smem, int ncl) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem &sm = *reinterpret_cast<SelSmem *>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
   const int64_t T = row_T(a, row);
   const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
   const int64_t nw = (ns + 31) / 32;
-  const int64_t span = span_words(nw);
+  const int64_t span = span_words(nw, ncl);
   const int64_t w_lo = min(nw, static_cast<int64_t>(rank) * span), w_hi = min(nw, w_lo + span);
   uint32_t *bm_local = bitmap_in_smem ? reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelSmem))
                                       : row_bitmap(bitmap_g, a.stride, row, p) + w_lo;
@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
 
   // ---- 3. the leader gathers the candidates and selects the ones still needed
   if (rank == 0) {
-    uint32_t cnt[kSelCluster], off[kSelCluster], n = 0, ovf = 0;
-    for (uint32_t r = 0; r < kSelCluster; ++r) {
+    uint32_t cnt[kSelClusterMax], off[kSelClusterMax], n = 0, ovf = 0;
+    for (uint32_t r = 0; r < static_cast<uint32_t>(ncl); ++r) {
       cnt[r] = r == 0 ? sm.ncand : ld_dsmem_u32(&sm.ncand, r);
       ovf |= r == 0 ? sm.overflow : ld_dsmem_u32(&sm.overflow, r);
       off[r] = n;
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
     }
     const bool from_row = ovf != 0 || n > static_cast<uint32_t>(kSelCap);
     if (!from_row) {
-      for (uint32_t r = 1; r < kSelCluster; ++r)
+      for (uint32_t r = 1; r < static_cast<uint32_t>(ncl); ++r)
         for (uint32_t i = tid; i < cnt[r]; i += kSelThreads) sm.cand[off[r] + i] = ld_dsmem_u64(&sm.cand[i], r);
     }
     __syncthreads();
@@ -496,7 +496,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
   uint32_t off = block_excl_scan(c, sm.warp_tot, &tot);
   // every higher-ranked slice starts after this one: add this slice's count to
   // theirs (cnt_below was cleared before barrier #1)
-  if (tid > 0 && tid < kSelCluster && static_cast<uint32_t>(tid) > rank)
+  if (tid > 0 && tid < ncl && static_cast<uint32_t>(tid) > rank)
     asm volatile("red.shared::cluster.add.u32 [%0], %1;\n" ::"r"(dsmem_addr(&sm.cnt_below, tid)), "r"(tot) : "memory");
   cluster_sync();  // #3: every slice's count added; no shared memory of a peer is touched after it
   off += sm.cnt_below;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
       ++off;
     }
   }
-  if (rank == kSelCluster - 1) {
+  if (rank == static_cast<uint32_t>(ncl) - 1) {
     const int kout = p == 0 ? a.k : a.out_pool_blocks;
     for (int i = kt + tid; i < kout; i += kSelThreads) out[i] = -1;
     if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
@@ -555,7 +555,10 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
     aux = own;
   }
   const int nprob = (!a.pool && a.out_pool_blocks > 0) ? 2 : 1;
-  const int64_t slice = span_words(w0);
+  // CTAs per (row, problem): 8 for long rows while the launch still fits one wave
+  // of two CTAs per SM, else 4
+  const int ncl = (a.rows * nprob * kSelClusterMax <= 2 * 152 && w0 >= 4096) ? kSelClusterMax : 4;
+  const int64_t slice = span_words(w0, ncl);
   const int in_smem = slice <= kSmemBitmapWords ? 1 : 0;
   const int smem = static_cast<int>(sizeof(SelSmem) + (in_smem ? slice * 4 : 0));
   static int attr = 0;
@@ -565,18 +568,18 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
     attr = smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kSelCluster, a.rows, nprob);
+  cfg.gridDim = dim3(ncl, a.rows, nprob);
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute cl[1];
   cl[0].id = cudaLaunchAttributeClusterDimension;
-  cl[0].val.clusterDim.x = kSelCluster;
+  cl[0].val.clusterDim.x = ncl;
   cl[0].val.clusterDim.y = 1;
   cl[0].val.clusterDim.z = 1;
   cfg.attrs = cl;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_select, a, aux, aux_row, bitmap, in_smem);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_select, a, aux, aux_row, bitmap, in_smem, ncl);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
