@@ -442,8 +442,14 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       const int bs = bchanges & 1;
       ++bchanges;
       const int64_t row_nslots = row_slots(a, row);
+      const int64_t row_T = pool_mode ? a.s.q_pos[row] / a.s.ratio : 0;  // POOL: visible positions
       for (int tile = first_own(t0, jrow, kAcc, parity); tile < t1 && !dead; tile += kAcc) {
         const int j = jrow + (tile - t0);
+        const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
+        // POOL: the key's pool block, requested before the wait for the accumulator
+        int32_t pid = -1;
+        if (pool_mode && slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs)
+          pid = __ldg(a.s.pool + static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs);
         // each warp of the group waits for the accumulator itself and hands
         // its lane quarter back on its own (tempty counts four arrivals)
         int ok = 1;
@@ -491,17 +497,12 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
               }
             }
           }
-          const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
           bool valid;
           if (!pool_mode) {
             valid = slot < row_nslots;
           } else {
-            const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
-                                    ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
-                                    : -1;
-            const int64_t T = a.s.q_pos[row] / a.s.ratio;
             const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
-            valid = pid >= 0 && p < T && p < a.s.cap;
+            valid = pid >= 0 && p < row_T && p < a.s.cap;
             if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
           }
           if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
