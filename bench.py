@@ -451,7 +451,7 @@ def run_ours(args):
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(W, args, sample_steps=1)
+        line["cpu_baseline"] = cpu_baseline(W, args)
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -762,16 +762,18 @@ def run_secondary(args):
     print(json.dumps(line), flush=True)
 
 # ----------------------------------------------------------------------------- oracle arm
-def cpu_baseline(W, args, sample_steps=1):
+def cpu_baseline(W, args, sample_steps=None, min_seconds=10.0, max_steps=1024):
     """The CPU oracle (as it stands) on a bounded sample of the workload: sequence 0,
-    `sample_steps` decode steps (append the token, Full-layer score over every visible
-    position, top-k, pool, attention), on the host cores."""
+    decode steps (append the token, Full-layer score over every visible position,
+    top-k, pool, attention) on the host cores, `sample_steps` of them, or when that is
+    None as many as fill `min_seconds` of oracle time (at most `max_steps`)."""
     import numpy as np
     from oracle import oracle as orc
 
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     orc.build()
-    cache = orc.Cache(W.context + sample_steps + 8, swa_dtype=W.swa_dtype)
+    cap = sample_steps if sample_steps is not None else max_steps
+    cache = orc.Cache(W.context + cap + 8, swa_dtype=W.swa_dtype)
     chunk = 8192
     for t0 in range(0, W.context, chunk):
         n = min(chunk, W.context - t0)
@@ -779,7 +781,10 @@ def cpu_baseline(W, args, sample_steps=1):
                       W.ik(0, t0, n, device=dev).cpu().numpy(), W.theta)
     u16 = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     t_total = 0.0
-    for s in range(sample_steps):
+    done = 0
+    for s in range(cap):
+        if sample_steps is None and t_total >= min_seconds:
+            break
         kv = W.kv(0, W.context + s, 1, device=dev).cpu().numpy()
         ik = W.ik(0, W.context + s, 1, device=dev).cpu().numpy()
         q_idx = u16(W.q_idx(s, 0, device=dev)[0])
@@ -789,9 +794,10 @@ def cpu_baseline(W, args, sample_steps=1):
         orc.append_r1(cache, kv, ik, W.theta)
         orc.full_layer(cache, q_idx, w, q, W.context + s, W.topk, W.sm_scale)
         t_total += time.perf_counter() - t0
-    return {"value": round(sample_steps / t_total, 4), "unit": UNIT, "cores": orc.num_threads(),
-            "kind": "oracle", "seconds": round(t_total, 3),
-            "sample": f"sequence 0 x {sample_steps} decode step(s) of {W.name}: append + Full-layer "
+        done += 1
+    return {"value": round(done / t_total, 4), "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(t_total, 3), "steps": done,
+            "sample": f"sequence 0 x {done} decode step(s) of {W.name}: append + Full-layer "
                       f"score over {W.context} positions x {W.index_heads} heads + top-{W.topk} + "
                       f"pool + attention ({W.heads} heads)"}
 
