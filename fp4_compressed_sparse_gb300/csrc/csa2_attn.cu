@@ -11,13 +11,15 @@
 // One CTA = (one split of a row's entry list, up to 64 heads).  Every head
 // shares the entries, so each entry is dequantised once per CTA:
 //   producer warps (4)  gather 32 entries at a time and dequantise them into a
-//                       two-stage fp16 ring: E2M1 x E4M3 through a byte -> half2
-//                       table (exact: at most 6 significant bits, >= 2^-10);
+//                       two-stage fp16 ring: E2M1 pairs by cvt.f16x2.e2m1x2, times
+//                       the E4M3 scale (exact: at most 6 significant bits, >= 2^-10);
 //                       window MXFP8 / bf16 entries, scaled by a power of two
 //                       2^-sigma_j only if they would not fit fp16
-//   consumer warps      S = Q K^T (mma.sync m16n8k16 f16, fp32 accumulate),
-//   (heads / 8)         online softmax in the log2 domain, O += P V with the
-//                       fp32 O tile in registers
+//   consumer warps      S = Q K^T (mma.sync m16n8k16 f16, fp32 accumulate; a
+//   (heads / 8)         warp takes 16 heads x the chunk's 32 entries over one half
+//                       of the 576 dims, the two halves summed by the softmax),
+//                       online softmax in the log2 domain, O += P V with the fp32
+//                       O tile in registers
 // The query is held as fp16 with a power-of-two scale per head (exact for bf16
 // values within 2^24 of the head's maximum).  Stage handover uses mbarriers
 // with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  The splits of a
@@ -36,7 +38,8 @@ namespace {
 constexpr int kE = 32;            // entries per chunk
 constexpr int kQS = kDqk + 8;     // fp16 row stride of Q and of the entry tiles (1168 B: conflict-free ldmatrix)
 constexpr int kPS = kE + 8;       // fp16 row stride of P (80 B)
-constexpr int kSS = kE + 4;       // fp32 row stride of the logits
+constexpr int kSS = kE + 8;       // fp32 row stride of the partial logits (conflict-free float2 stores)
+constexpr int kOS = kLat + 8;     // fp32 row stride of the partial O in the cluster merge
 constexpr int kProdThreads = 128; // four producer warps
 constexpr int kHeadBlock = 64;    // heads per CTA at most
 constexpr uint32_t kWaitIters = 200;
@@ -47,13 +50,12 @@ template <int HP>
 struct __align__(16) AttnSmem {
   __half q[HP][kQS];
   __half kv[2][kE][kQS];
-  float s[HP][kSS];
+  float s[2][HP][kSS]; // partial logits over dims 0..287 and 288..575
   __half p[HP][kPS];
   float qf[HP];        // logit factor of head h: 2^e_h * sm_scale * log2(e)
   float alpha[HP];     // this chunk's rescale of O
   float fin[HP][2];    // m, l per head after the last chunk
   float sig[2][kE];    // 2^sigma_j of entry j of a stage; 0 = empty entry
-  uint32_t lut[256];   // byte of two E2M1 codes -> half2 (low nibble in the low half)
   __align__(8) uint64_t full[2];
   __align__(8) uint64_t empty[2];
 };
@@ -86,6 +88,12 @@ __device__ __forceinline__ uint32_t hmul2u(uint32_t x, uint32_t y) {
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two_bytes) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(static_cast<uint16_t>(two_bytes)));
+  return r;
+}
+// two E2M1 codes (the low byte of `byte`; low nibble -> low half) to fp16, exactly
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(r) : "r"(byte));
   return r;
 }
 __device__ __forceinline__ uint32_t h2_splat(float v) {
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   const int total_chunks = (kpad + kWin) / kE;
   const int nchunks = split < total_chunks ? (total_chunks - split + n_splits - 1) / n_splits : 0;
 
-  // ---- set-up: barriers, dequant table
+  // ---- set-up: barriers
   if (tid == 0) {
     tc::mbar_init(&sm.full[0], kProdThreads);
     tc::mbar_init(&sm.full[1], kProdThreads);
@@ -213,11 +221,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     tc::mbar_init(&sm.empty[1], kCons);
     tc::fence_mbar_init();
   }
-  for (int i = tid; i < 256; i += blockDim.x) {
-    __half2 h = __floats2half2_rn(e2m1_value(i & 15), e2m1_value(i >> 4));
-    sm.lut[i] = *reinterpret_cast<uint32_t *>(&h);
-  }
-  __syncthreads();  // barriers and table ready
+  __syncthreads();  // barriers ready
 
   if (tid >= kCons) {
     // ================================================================ producers
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
             uint32_t o[8];
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-              o[b] = hmul2u(sm.lut[(raw.cw[i].x >> (8 * b)) & 0xFFu], s2);
-              o[4 + b] = hmul2u(sm.lut[(raw.cw[i].y >> (8 * b)) & 0xFFu], s2);
+              o[b] = hmul2u(e2m1x2_to_h2(raw.cw[i].x >> (8 * b)), s2);
+              o[4 + b] = hmul2u(e2m1x2_to_h2(raw.cw[i].y >> (8 * b)), s2);
             }
             dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -280,11 +284,13 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
             for (int g = 0; g < 18; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
             // values < 448 * 2^(sc-127): keep them below 2^16 with sigma >= 0
             const int sigma = min(15, max(0, static_cast<int>(mx) - 134));
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 9; ++i) {
               const int u = q4 + 4 * i;
               const uint4 cw = reinterpret_cast<const uint4 *>(cb)[u];
-              const int sc = static_cast<int>((sw[u >> 3] >> (8 * ((u >> 1) & 3))) & 0xFFu);
+              const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
+              const uint32_t swu = wi == 0 ? sw[0] : wi == 1 ? sw[1] : wi == 2 ? sw[2] : wi == 3 ? sw[3] : sw[4];
+              const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
               const int kx = sc - 127 - sigma;
               const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
               const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
           } else {
             const uint4 *cw = reinterpret_cast<const uint4 *>(cb);
             float amax = 0.0f;
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 9; ++i) {
               const int u = q4 + 4 * i;
               const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
             amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
             const int sigma = amax > 0.0f ? min(15, max(0, floor_log2f(amax) - 14)) : 0;
             const float inv = pow2f(-sigma);
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 9; ++i) {
               const int u = q4 + 4 * i;
               const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
@@ -417,55 +423,58 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   const int sh = tid >> 2, sq = tid & 3;  // softmax: head sh, entries 8 sq .. 8 sq + 7
   float m_run = -INFINITY, l_run = 0.0f;
   bool dead = false;
-  const int hg = warp >> 1, eh = warp & 1;  // QK: heads 16 hg.., entries 16 eh..
+  const int hg = warp >> 1, kh = warp & 1;  // QK: heads 16 hg.., dims 288 kh..
   const int d0 = warp * kDW;                // PV: dims d0 .. d0 + kDW - 1
 
   for (int c = 0; c < nchunks; ++c) {
     const int st = c & 1;
     if (!dead) dead = !wait_warp(&sm.full[st], (c >> 1) & 1, a.err);
     if (!dead) {
-      // ---- logits of heads 16hg.. x entries 16eh..
-      // four independent accumulator chains (2 entry tiles x even / odd k-steps)
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const uint32_t qa = smem_u32(&sm.q[16 * hg + (lane & 15)][(lane >> 4) * 8]);
-      const uint32_t kb = smem_u32(&sm.kv[st][16 * eh + (lane & 7) + ((lane >> 4) << 3)][((lane >> 3) & 1) * 8]);
+      // ---- partial logits of heads 16hg.. x the 32 entries over dims 288kh..
+      // (four independent accumulator chains, one per n8 tile of entries)
+      float acc[4][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint32_t qa = smem_u32(&sm.q[16 * hg + (lane & 15)][kh * (kDqk / 2) + (lane >> 4) * 8]);
+      const uint32_t kb = smem_u32(&sm.kv[st][(lane & 7) + ((lane >> 4) << 3)][kh * (kDqk / 2) + ((lane >> 3) & 1) * 8]);
 #pragma unroll 3
-      for (int kk = 0; kk < kDqk / 16; kk += 2) {
-        uint32_t af[4], b0, b1, b2, b3, ag[4], c0, c1, c2, c3;
+      for (int kk = 0; kk < kDqk / 32; ++kk) {
+        uint32_t af[4], b0, b1, b2, b3, c0, c1, c2, c3;
         ldsm_x4(qa + kk * 32, af[0], af[1], af[2], af[3]);
         ldsm_x4(kb + kk * 32, b0, b1, b2, b3);
-        ldsm_x4(qa + kk * 32 + 32, ag[0], ag[1], ag[2], ag[3]);
-        ldsm_x4(kb + kk * 32 + 32, c0, c1, c2, c3);
+        ldsm_x4(kb + 16 * kQS * 2 + kk * 32, c0, c1, c2, c3);
         mma_f16(acc[0], af, b0, b1);
         mma_f16(acc[1], af, b2, b3);
-        mma_f16(acc2[0], ag, c0, c1);
-        mma_f16(acc2[1], ag, c2, c3);
+        mma_f16(acc[2], af, c0, c1);
+        mma_f16(acc[3], af, c2, c3);
       }
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int h = 16 * hg + g + 8 * r;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int col = 16 * eh + 8 * nt + 2 * t + cc;
-            const float sg = sm.sig[st][col];
-            sm.s[h][col] = sg > 0.0f ? acc[nt][2 * r + cc] * sm.qf[h] * sg : -INFINITY;
-          }
-        }
+        for (int r = 0; r < 2; ++r)
+          *reinterpret_cast<float2 *>(&sm.s[kh][16 * hg + g + 8 * r][8 * nt + 2 * t]) =
+              make_float2(acc[nt][2 * r], acc[nt][2 * r + 1]);
     }
     bar_consumers(kCons);
     if (!dead) {
       // ---- online softmax, 4 threads per head
-      float z[8], mx = -INFINITY;
+      float z[8], sg[8], mx = -INFINITY;
+      const float qf = sm.qf[sh];
+#pragma unroll
+      for (int i = 0; i < 8; i += 4) {
+        const float4 s0 = *reinterpret_cast<const float4 *>(&sm.s[0][sh][8 * sq + i]);
+        const float4 s1 = *reinterpret_cast<const float4 *>(&sm.s[1][sh][8 * sq + i]);
+        const float4 g4 = *reinterpret_cast<const float4 *>(&sm.sig[st][8 * sq + i]);
+        z[i] = s0.x + s1.x;
+        z[i + 1] = s0.y + s1.y;
+        z[i + 2] = s0.z + s1.z;
+        z[i + 3] = s0.w + s1.w;
+        sg[i] = g4.x;
+        sg[i + 1] = g4.y;
+        sg[i + 2] = g4.z;
+        sg[i + 3] = g4.w;
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        z[i] = sm.s[sh][8 * sq + i];
+        z[i] = sg[i] > 0.0f ? z[i] * qf * sg[i] : -INFINITY;
         mx = fmaxf(mx, z[i]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
         const float p0 = m_new == -INFINITY ? 0.0f : exp2f(z[i] - m_new);
         const float p1 = m_new == -INFINITY ? 0.0f : exp2f(z[i + 1] - m_new);
         sum += p0 + p1;
-        __half2 h2 = __floats2half2_rn(p0 * sm.sig[st][8 * sq + i], p1 * sm.sig[st][8 * sq + i + 1]);
+        __half2 h2 = __floats2half2_rn(p0 * sg[i], p1 * sg[i + 1]);
         pw[i / 2] = *reinterpret_cast<uint32_t *>(&h2);
       }
       *reinterpret_cast<uint4 *>(&sm.p[sh][8 * sq]) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -565,8 +574,8 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   // unnormalised O (fp32) and (m, l) in its own shared memory, then CTA `split`
   // merges heads split, split + S, ... from its peers' shared memory
   // (flash-decoding LSE merge, then the sink)
-  float *osm = reinterpret_cast<float *>(&sm.q[0][0]);  // [HP][512]: the query and the ring are done with
-  static_assert(sizeof(float) * HP * kLat <= sizeof(sm.q) + sizeof(sm.kv), "partial O does not fit");
+  float *osm = reinterpret_cast<float *>(&sm.q[0][0]);  // [HP][kOS]: the query and the ring are done with
+  static_assert(sizeof(float) * HP * kOS <= sizeof(sm.q) + sizeof(sm.kv), "partial O does not fit");
 #pragma unroll
   for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
@@ -574,7 +583,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       const int hl = 16 * mt + g + 8 * r;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
-        *reinterpret_cast<float2 *>(osm + hl * kLat + d0 + 8 * nt + 2 * t) =
+        *reinterpret_cast<float2 *>(osm + hl * kOS + d0 + 8 * nt + 2 * t) =
             make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
     }
   if (!alive && sq == 0) {  // contribute nothing
@@ -611,7 +620,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     for (int sp = 0; sp < kMaxSplits; ++sp)
 #pragma unroll
       for (int c = 0; c < kLat / 128; ++c)
-        v[sp][c] = sp < n_splits ? ld_dsmem4(osm + hl * kLat + 128 * c + 4 * lane, sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[sp][c] = sp < n_splits ? ld_dsmem4(osm + hl * kOS + 128 * c + 4 * lane, sp) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < kLat / 128; ++c) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
