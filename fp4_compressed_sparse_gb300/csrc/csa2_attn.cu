@@ -23,10 +23,10 @@
 // The query is held as fp16 with a power-of-two scale per head (exact for bf16
 // values within 2^24 of the head's maximum).  Stage handover uses mbarriers
 // with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  The splits of a
-// row are one thread-block cluster: each keeps its unnormalised (O, m, l) in
-// shared memory and, after a cluster barrier, merges a slice of the heads from
-// its peers' shared memory (flash-decoding LSE merge, then the sink) -- no
-// global partials and no second kernel.
+// row are one thread-block cluster: each writes its unnormalised (O, m, l)
+// straight from registers to a workspace that stays in L2 and, after a cluster
+// barrier, merges a slice of the heads from its peers' partials (flash-decoding
+// LSE merge, then the sink) -- no second kernel.
 #include <cuda_fp16.h>
 
 #include "csa2_internal.cuh"
@@ -39,7 +39,6 @@ constexpr int kE = 32;            // entries per chunk
 constexpr int kQS = kDqk + 8;     // fp16 row stride of Q and of the entry tiles (1168 B: conflict-free ldmatrix)
 constexpr int kPS = kE + 8;       // fp16 row stride of P (80 B)
 constexpr int kSS = kE + 8;       // fp32 row stride of the partial logits (conflict-free float2 stores)
-constexpr int kOS = kLat + 8;     // fp32 row stride of the partial O in the cluster merge
 constexpr int kProdThreads = 128; // four producer warps
 constexpr int kHeadBlock = 64;    // heads per CTA at most
 constexpr uint32_t kWaitIters = 200;
@@ -106,24 +105,9 @@ constexpr int kMaxSplits = 8;  // splits of a row = one portable thread-block cl
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
-// a float / float4 at the same shared-memory offset in CTA `rank` of the cluster
-__device__ __forceinline__ float ld_dsmem(const float *p, uint32_t rank) {
-  uint32_t r;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(r) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem4(const float *p, uint32_t rank) {
-  uint32_t r;
-  float4 v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(r)
-               : "memory");
-  return v;
-}
+// a float2 / float4 written by another CTA of the cluster before a cluster barrier (L2, not L1)
+__device__ __forceinline__ float4 ld_cg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+__device__ __forceinline__ float2 ld_cg2(const float *p) { return __ldcg(reinterpret_cast<const float2 *>(p)); }
 
 __device__ __forceinline__ void bar_consumers(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
 // consumer barrier returning the AND of v over the consumer threads
@@ -193,8 +177,81 @@ __device__ __forceinline__ void load_fp4(const AttnArgs &a, int64_t src, int q4,
   r.rsc = a.rope_scales[src * 4 + q4];
 }
 
+// Partial results of one (row, head block, split) in the workspace: O [HP][512]
+// then (m, l) [HP][2], fp32.
 template <int HP>
-__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits) {
+__host__ __device__ constexpr size_t part_floats() { return static_cast<size_t>(HP) * (kLat + 2); }
+
+// The cluster merge of a row's splits, run by every consumer warp of every
+// split after the cluster barrier: split `split` merges heads split, split + S,
+// ... (S = n_splits <= kS) from the partials of all S splits.  A warp takes kH
+// of its heads at a time and requests every partial value of them -- the O rows
+// and the (m, l) pairs -- before it uses any.  Flash-decoding LSE merge, then
+// the sink.
+template <int kS, int kH, int HP>
+__device__ __forceinline__ void merge_heads(const AttnArgs &a, const float *part, int row, int hbase, int nh,
+                                            int split, int n_splits, int warp, int nwarps, int lane) {
+  const int stride = n_splits * nwarps;
+  for (int hl0 = split + n_splits * warp; hl0 < nh; hl0 += stride * kH) {
+    float4 v[kH][kS][kLat / 128];
+    float ms[kH], ls[kH];
+#pragma unroll
+    for (int j = 0; j < kH; ++j) {
+      const int hl = hl0 + stride * j;  // warp-uniform
+#pragma unroll
+      for (int sp = 0; sp < kS; ++sp)
+#pragma unroll
+        for (int c = 0; c < kLat / 128; ++c)
+          v[j][sp][c] = hl < nh && sp < n_splits
+                            ? ld_cg4(part + sp * part_floats<HP>() + static_cast<size_t>(hl) * kLat + 128 * c + 4 * lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      ms[j] = -INFINITY;
+      ls[j] = 0.0f;
+      if (hl < nh && lane < n_splits) {  // lane s < n_splits holds split s's (m, l)
+        const float2 ml = ld_cg2(part + lane * part_floats<HP>() + static_cast<size_t>(HP) * kLat + 2 * hl);
+        ms[j] = ml.x;
+        ls[j] = ml.y;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kH; ++j) {
+      const int hl = hl0 + stride * j;
+      if (hl >= nh) break;
+      const int h = hbase + hl;
+      float M = ms[j];
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+      const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
+      M = fmaxf(M, s2);
+      const float f = (M == -INFINITY || ms[j] == -INFINITY) ? 0.0f : exp2f(ms[j] - M);
+      float L = ls[j] * f;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+      if (a.sink && M != -INFINITY) L += exp2f(s2 - M);
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      float fs[kS];
+#pragma unroll
+      for (int sp = 0; sp < kS; ++sp) fs[sp] = __shfl_sync(0xffffffffu, f, sp) * inv;
+      float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat;
+#pragma unroll
+      for (int c = 0; c < kLat / 128; ++c) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sp = 0; sp < kS; ++sp) {
+          acc.x += v[j][sp][c].x * fs[sp];
+          acc.y += v[j][sp][c].y * fs[sp];
+          acc.z += v[j][sp][c].z * fs[sp];
+          acc.w += v[j][sp][c].w * fs[sp];
+        }
+        *reinterpret_cast<float4 *>(out + 128 * c + 4 * lane) = acc;
+      }
+      if (lane == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+template <int HP>
+__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits, float *part_ws) {
   constexpr int kCons = HP * 4;         // consumer threads: HP / 8 warps
   constexpr int kDW = 4096 / HP;        // output dims per consumer warp
   constexpr int kNT = kDW / 8;          // n8 tiles per consumer warp
@@ -355,10 +412,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
         if (c + 2 < nchunks) sel_next = sel_of(c + 2);
       }
     }
-    if (n_splits > 1) {  // the consumers' two cluster barriers, matched here
-      cluster_sync();
-      cluster_sync();
-    }
+    if (n_splits > 1) cluster_sync();  // the consumers' cluster barrier, matched here
     return;
   }
 
@@ -570,12 +624,12 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       }
     return;
   }
-  // ---- the row's splits form one thread-block cluster: each CTA leaves its
-  // unnormalised O (fp32) and (m, l) in its own shared memory, then CTA `split`
-  // merges heads split, split + S, ... from its peers' shared memory
-  // (flash-decoding LSE merge, then the sink)
-  float *osm = reinterpret_cast<float *>(&sm.q[0][0]);  // [HP][kOS]: the query and the ring are done with
-  static_assert(sizeof(float) * HP * kOS <= sizeof(sm.q) + sizeof(sm.kv), "partial O does not fit");
+  // ---- the row's splits form one thread-block cluster: each CTA writes its
+  // unnormalised O and (m, l) to its slot of the workspace, then after the
+  // cluster barrier CTA `split` merges heads split, split + S, ... from the
+  // slots of all S splits
+  float *part_row = part_ws + static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_splits * part_floats<HP>();
+  float *mine = part_row + split * part_floats<HP>();
 #pragma unroll
   for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
@@ -583,59 +637,17 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       const int hl = 16 * mt + g + 8 * r;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
-        *reinterpret_cast<float2 *>(osm + hl * kOS + d0 + 8 * nt + 2 * t) =
+        *reinterpret_cast<float2 *>(mine + hl * kLat + d0 + 8 * nt + 2 * t) =
             make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
     }
-  if (!alive && sq == 0) {  // contribute nothing
-    sm.fin[sh][0] = -INFINITY;
-    sm.fin[sh][1] = 0.0f;
-  }
-  cluster_sync();
-  for (int hl = split + n_splits * warp; hl < nh; hl += n_splits * (kCons / 32)) {
-    const int h = hbase + hl;
-    // lane s < n_splits holds split s's (m, l)
-    float ms = -INFINITY, ls = 0.0f;
-    if (lane < n_splits) {
-      ms = ld_dsmem(&sm.fin[hl][0], lane);
-      ls = ld_dsmem(&sm.fin[hl][1], lane);
-    }
-    float M = ms;
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-    const float s2 = a.sink ? a.sink[h] * kLog2e : -INFINITY;
-    M = fmaxf(M, s2);
-    const float f = (M == -INFINITY || ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-    float L = ls * f;
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-    if (a.sink && M != -INFINITY) L += exp2f(s2 - M);
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    float fs[kMaxSplits];
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp) fs[sp] = __shfl_sync(0xffffffffu, f, sp) * inv;
-    float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat;
-    // every peer load of the head first (independent), then the sums
-    float4 v[kMaxSplits][kLat / 128];
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp)
-#pragma unroll
-      for (int c = 0; c < kLat / 128; ++c)
-        v[sp][c] = sp < n_splits ? ld_dsmem4(osm + hl * kOS + 128 * c + 4 * lane, sp) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < kLat / 128; ++c) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int sp = 0; sp < kMaxSplits; ++sp) {
-        acc.x += v[sp][c].x * fs[sp];
-        acc.y += v[sp][c].y * fs[sp];
-        acc.z += v[sp][c].z * fs[sp];
-        acc.w += v[sp][c].w * fs[sp];
-      }
-      *reinterpret_cast<float4 *>(out + 128 * c + 4 * lane) = acc;
-    }
-    if (lane == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
-  }
-  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+  if (sq == 0)  // a CTA whose wait ran out contributes nothing
+    *reinterpret_cast<float2 *>(mine + HP * kLat + 2 * sh) =
+        alive ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.0f);
+  cluster_sync();  // release / acquire at cluster scope: the partials are visible to every CTA of the row
+  if (n_splits <= 4)
+    merge_heads<4, 2, HP>(a, part_row, row, hbase, nh, split, n_splits, warp, kCons / 32, lane);
+  else
+    merge_heads<kMaxSplits, 1, HP>(a, part_row, row, hbase, nh, split, n_splits, warp, kCons / 32, lane);
 }
 
 int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
@@ -653,7 +665,7 @@ int choose_splits(int rows, int heads, int k) {
 }
 
 template <int HP>
-cudaError_t launch_hp(const AttnArgs &a, int n_splits, cudaStream_t st) {
+cudaError_t launch_hp(const AttnArgs &a, int n_splits, float *part, cudaStream_t st) {
   static bool attr_set = false;
   const int smem = static_cast<int>(sizeof(AttnSmem<HP>));
   if (!attr_set) {
@@ -673,27 +685,36 @@ cudaError_t launch_hp(const AttnArgs &a, int n_splits, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_splits);
+  return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_splits, part);
 }
 
 }  // namespace
 
-// The splits merge through distributed shared memory: no workspace.
+// Workspace: the partial (O, m, l) of every split of every (row, head block)
+// when rows are split, sized for any call with at most `rows` rows (a prefill
+// block may be shorter than the block the workspace was sized for, and fewer
+// rows take more splits).
 size_t attn_workspace_bytes(int rows, int heads, int k) {
-  (void)rows;
-  (void)heads;
-  (void)k;
-  return 256;
+  size_t most = 0;
+  for (int r = 1; r <= rows && r <= 152; ++r) {
+    const int s = choose_splits(r, heads, k);
+    if (s > 1) most = std::max(most, static_cast<size_t>(r) * head_blocks(heads) * s);
+  }
+  return most * part_floats<kHeadBlock>() * sizeof(float) + 256;
 }
 
 cudaError_t launch_attn(const AttnArgs &a0, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (a0.rows <= 0) return cudaSuccess;
   const int n_splits = choose_splits(a0.rows, a0.heads, a0.k);
-  (void)ws;
-  (void)ws_bytes;
-  if (a0.heads <= 16) return launch_hp<16>(a0, n_splits, st);
-  if (a0.heads <= 32) return launch_hp<32>(a0, n_splits, st);
-  return launch_hp<64>(a0, n_splits, st);
+  if (n_splits > 1 &&
+      (ws == nullptr || ws_bytes < static_cast<size_t>(a0.rows) * head_blocks(a0.heads) * n_splits *
+                                       part_floats<kHeadBlock>() * sizeof(float) ||
+       reinterpret_cast<uintptr_t>(ws) % 16 != 0))
+    return cudaErrorInvalidValue;
+  float *part = static_cast<float *>(ws);
+  if (a0.heads <= 16) return launch_hp<16>(a0, n_splits, part, st);
+  if (a0.heads <= 32) return launch_hp<32>(a0, n_splits, part, st);
+  return launch_hp<64>(a0, n_splits, part, st);
 }
 
 }  // namespace csa2
