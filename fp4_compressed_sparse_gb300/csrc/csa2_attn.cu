@@ -417,54 +417,53 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   }
 
   // ================================================================== consumers
-  // the query: raw bf16 rows into sm.q (one round trip), then in place to fp16
-  // with a power-of-two scale per head: |q * 2^-e| < 2^15, exact for every bf16
-  // value >= amax * 2^-24
-  for (int i = tid; i < HP * (kDqk / 8); i += kCons) {
-    const int h = i / (kDqk / 8), c8 = i % (kDqk / 8);
-    __half *dq = &sm.q[h][8 * c8];
-    if (h < nh) {
-      const uint16_t *gq = a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk + 8 * c8;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dq)), "l"(gq) : "memory");
-    } else {
-      *reinterpret_cast<uint4 *>(dq) = make_uint4(0, 0, 0, 0);
+  // the query to fp16 in sm.q with a power-of-two scale per head: |q * 2^-e| <
+  // 2^15, exact for every bf16 value >= amax * 2^-24.  Warp w converts heads
+  // w, w + HP/8, ... (eight of them), lane l the bf16 pairs l, l + 32, ... of a
+  // head; every raw value of the warp's heads is requested from global memory
+  // before any is used (one round trip), and the eight heads' reductions run
+  // interleaved.
+  {
+    constexpr int kQW = 8;              // heads per consumer warp
+    constexpr int kQP = kDqk / 2 / 32;  // bf16 pairs per lane per head (9)
+    static_assert(kQW * (kCons / 32) == HP, "every head has one converting warp");
+    uint32_t raw[kQW][kQP];
+#pragma unroll
+    for (int j = 0; j < kQW; ++j) {
+      const int h = warp + (kCons / 32) * j;
+      const uint32_t *gq =
+          reinterpret_cast<const uint32_t *>(a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk);
+#pragma unroll
+      for (int i = 0; i < kQP; ++i) raw[j][i] = h < nh ? __ldg(gq + lane + 32 * i) : 0u;
     }
-  }
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
-  bar_consumers(kCons);
-  for (int h = warp; h < HP; h += kCons / 32) {
-    uint4 raw[3];
-    float amax = 0.0f;
+    float amax[kQW];
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int c8 = lane + 32 * i;
-      raw[i] = c8 < kDqk / 8 ? *reinterpret_cast<const uint4 *>(&sm.q[h][8 * c8]) : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+    for (int j = 0; j < kQW; ++j) {
+      amax[j] = 0.0f;
 #pragma unroll
-      for (int k2 = 0; k2 < 4; ++k2)
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k2] << 16)), fabsf(__uint_as_float(w[k2] & 0xFFFF0000u))));
+      for (int i = 0; i < kQP; ++i)
+        amax[j] = fmaxf(amax[j], fmaxf(fabsf(__uint_as_float(raw[j][i] << 16)),
+                                       fabsf(__uint_as_float(raw[j][i] & 0xFFFF0000u))));
     }
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int ex = amax > 0.0f ? floor_log2f(amax) - 14 : 0;
-    ex = max(ex, -110);
-    const float inv = pow2f(-ex);
+    for (int o = 1; o < 32; o <<= 1)
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-      const int c8 = lane + 32 * i;
-      if (c8 < kDqk / 8) {
-        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-        uint32_t hv[4];
+      for (int j = 0; j < kQW; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
 #pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[k2] << 16), inv),
-                                         __fmul_rn(__uint_as_float(w[k2] & 0xFFFF0000u), inv));
-          hv[k2] = *reinterpret_cast<uint32_t *>(&t2);
-        }
-        *reinterpret_cast<uint4 *>(&sm.q[h][8 * c8]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    for (int j = 0; j < kQW; ++j) {
+      const int h = warp + (kCons / 32) * j;
+      int ex = amax[j] > 0.0f ? floor_log2f(amax[j]) - 14 : 0;
+      ex = max(ex, -110);
+      const float inv = pow2f(-ex);
+      uint32_t *dq = reinterpret_cast<uint32_t *>(&sm.q[h][0]);
+#pragma unroll
+      for (int i = 0; i < kQP; ++i) {
+        __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(raw[j][i] << 16), inv),
+                                       __fmul_rn(__uint_as_float(raw[j][i] & 0xFFFF0000u), inv));
+        dq[lane + 32 * i] = *reinterpret_cast<uint32_t *>(&t2);
       }
+      if (lane == 0) sm.qf[h] = h < nh ? pow2f(ex) * a.sm_scale * kLog2e : 0.0f;
     }
-    if (lane == 0) sm.qf[h] = h < nh ? pow2f(ex) * a.sm_scale * kLog2e : 0.0f;
   }
   bar_consumers(kCons);
 
