@@ -284,6 +284,10 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     // ================================================================ producers
     const int pt = tid - kCons;
     const int e = pt >> 2, q4 = pt & 3;
+    // launched as a programmatic dependent of the selection: its indices are
+    // read only after that grid is complete (the consumers' query conversion
+    // does not wait)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t qmask = 0xFu << (lane & ~3);  // the four lanes of this entry
     const int32_t *idx_row = a.idx + static_cast<size_t>(row) * a.k;
     // software pipeline: once chunk c is handed over, the raw bytes of chunk
@@ -677,13 +681,15 @@ cudaError_t launch_hp(const AttnArgs &a, int n_splits, float *part, cudaStream_t
   cfg.blockDim = dim3(HP * 4 + kProdThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = n_splits;  // the row's splits: one cluster
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_splits, part);
 }
 
