@@ -306,9 +306,9 @@ class FullDecode:
 
     @staticmethod
     def kernel_launches():
-        # kv_append ratio 1, one token: 1 (it also advances n_tokens); index_score: q prep +
-        # score (the sideband clear is a memset); topk: 1 fused selector (top-k and pool);
-        # attention: 1 (splits merge inside; the arrival counters are cleared by a memset)
+        # kv_append ratio 1, one token: 1 (it also advances n_tokens); index_score: query
+        # prep (it also clears the sideband histograms) + score; topk: 1 fused selector
+        # (top-k and pool); attention: 1 (the splits of a row merge inside)
         return 1 + 2 + 1 + 1
 
 
