@@ -108,6 +108,26 @@ def test_index_score_full_and_topk_bitexact(orc, H_I):
         assert pcount[b].item() == cnt and pool[b].tolist() == pids.tolist()
 
 
+def test_index_score_many_short_rows_bitexact(orc):
+    """More rows than SMs over a short context (a CTA's item range spans several
+    rows, each with its own query record in the scan's operand slots), rows seeing
+    different numbers of positions."""
+    B, T, H_I = 200, 300, 64
+    c, oc, _, err = build_r1(orc, B, T, csa2.SWA_MXFP8, seed=23)
+    q_idx, w, _ = _decode_inputs(B, H_I, 16, seed=24)
+    pos = [T - 1 - (b % 50) * 3 for b in range(B)]
+    q_pos = torch.tensor(pos, dtype=torch.int64, device="cuda")
+    scores = torch.full((B, c.capacity), float("nan"), device="cuda")
+    csa2.index_score(c, q_idx.cuda(), w.cuda(), q_pos, scores, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for b in list(range(0, B, 7)) + [B - 1]:
+        ref, flags = orc.index_scores(oc[b], u16(q_idx[b]), w[b].numpy(), n_vis=pos[b])
+        assert flags == 0
+        got = scores[b, :pos[b]].cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"row {b}: {np.sum(got != ref)} scores differ"
+
+
 def test_index_score_block_scale_spread(orc):
     """Keys whose four 32-dim blocks differ in magnitude by up to 2^6 (and queries by
     up to 2^2): the block-scaled tensor-core dot must still equal the exact dot."""
