@@ -530,8 +530,8 @@ def run_e2e(bench, W, args, dev, flush):
 # its own JSON line; the headline line above is the Full-layer decode.
 
 def group_step_bytes(W, T):
-    """Algorithmic HBM bytes of one decoder-group step (append excluded): per layer
-    what the method must move, summed over the group's layers."""
+    """Algorithmic HBM bytes of one decoder-group step with T visible entries (append
+    excluded): per layer what the method must move, summed over the group's layers."""
     B, k, H, H_I = W.batch, W.topk, W.heads, W.index_heads
     swa = 128 * (594 if W.swa_dtype == 1 else 1152)
     attn = k * (324 + 4) + swa + H * 576 * 2 + H * 512 * 4      # per sequence and attention layer
@@ -549,37 +549,56 @@ def group_step_bytes(W, T):
 
 class GroupDecode:
     """A decoder group at a decode step on one cache: append the step's token, then
-    each layer of W.layers in order -- "full": score every visible position, top-k and
-    the 2,048-block pool, attention; "reindex": score the positions of the pool, top-k,
-    attention; "reuse": attention with the last indexer layer's indices.  Every layer
-    has its own queries; the layers share the cache (a model's layers have caches of
-    the same shape, and the kernels read them the same way)."""
+    each layer of W.layers in order -- "full": score every visible entry, top-k (and
+    the 2,048-block pool when a Reindex layer follows), attention; "reindex": score the
+    positions of the pool, top-k, attention; "reuse": attention with the last indexer
+    layer's indices.  Every layer has its own queries; the layers share the cache (a
+    model's layers have caches of the same shape, and the kernels read them the same
+    way).  With W.ratio == 2 the cache is encoder-style: two tokens per entry, the
+    step's token goes through the compression buffer."""
 
     def __init__(self, W, n_steps, device):
         from fp4_compressed_sparse_gb300 import csa2
         from fp4_compressed_sparse_gb300 import workloads as wl
         self.csa2, self.W = csa2, W
         B, ctx, nl = W.batch, W.context, len(W.layers)
-        self.cap = ctx + n_steps + 8
-        self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
-        self.rope = csa2.rope_table(W.theta, self.cap + 8)
+        self.cap = (ctx + n_steps) // W.ratio + 8
+        self.cache = csa2.Cache(B, self.cap, ratio=W.ratio, swa_dtype=W.swa_dtype)
+        self.rope = csa2.rope_table(W.theta, W.ratio * self.cap + 16)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
-        chunk = max(256, min(wl.CHUNK, (1 << 29) // (B * 576 * 4)))  # bound each staging copy to ~512 MB
+        # ratio 1: bound each staging copy to ~512 MB; ratio 2: whole generator chunks
+        # (four 704-wide streams; a partial chunk would redraw the whole chunk)
+        chunk = max(256, min(wl.CHUNK, (1 << 29) // (B * 576 * 4))) if W.ratio == 1 else wl.CHUNK
+        if W.ratio == 2:
+            self.ba, self.bb = W.bias(device=device)
         for t0 in range(0, ctx, chunk):
             n = min(chunk, ctx - t0)
-            kv = torch.stack([W.kv(b, t0, n, device=device) for b in range(B)])
-            ik = torch.stack([W.ik(b, t0, n, device=device) for b in range(B)])
-            csa2.kv_append(self.cache, kv, ik, self.rope, err=self.err)
-            del kv, ik
+            if W.ratio == 1:
+                kv = torch.stack([W.kv(b, t0, n, device=device) for b in range(B)])
+                ik = torch.stack([W.ik(b, t0, n, device=device) for b in range(B)])
+                csa2.kv_append(self.cache, kv, ik, self.rope, err=self.err)
+                del kv, ik
+            else:
+                rows = [torch.stack(x) for x in zip(*[W.cmp_rows(b, t0, n, device=device) for b in range(B)])]
+                csa2.kv_append(self.cache, rope_cs=self.rope, cmp=rows + [self.ba, self.bb], err=self.err)
+                del rows
         torch.cuda.synchronize()
-        self.kv_new = [torch.stack([W.kv(b, ctx + s, 1, device=device) for b in range(B)]) for s in range(n_steps)]
-        self.ik_new = [torch.stack([W.ik(b, ctx + s, 1, device=device) for b in range(B)]) for s in range(n_steps)]
+        if W.ratio == 1:
+            self.kv_new = [torch.stack([W.kv(b, ctx + s, 1, device=device) for b in range(B)])
+                           for s in range(n_steps)]
+            self.ik_new = [torch.stack([W.ik(b, ctx + s, 1, device=device) for b in range(B)])
+                           for s in range(n_steps)]
+        else:  # (C^a, C^b, Z^a, Z^b) [B, 1, 704] of the step's token
+            self.cmp_new = [[torch.stack(x) for x in zip(*[W.cmp_rows(b, ctx + s, 1, device=device)
+                                                           for b in range(B)])] for s in range(n_steps)]
         self.q_pos = [torch.full((B,), ctx + s, dtype=torch.int64, device=device) for s in range(n_steps)]
         self.q_idx = [[W.q_idx(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
         self.w = [[W.w(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
         self.q = [[W.q(s, l, device=device) for l in range(nl)] for s in range(n_steps)]
         has_full = "full" in W.layers
-        # a group without a Full layer scores inside the prior pool (uniformly drawn blocks)
+        # the Full layer builds the pool only for Reindex layers that follow; a group
+        # without a Full layer scores inside the prior pool (uniformly drawn blocks)
+        self.build_pool = has_full and "reindex" in W.layers
         self.pool = (torch.empty((B, W.pool_blocks), dtype=torch.int32, device=device) if has_full
                      else W.pool(device=device))
         self.pool_cnt = torch.empty((B,), dtype=torch.int32, device=device)
@@ -603,14 +622,21 @@ class GroupDecode:
         c, W = self.csa2, self.W
         main = torch.cuda.current_stream()
         mark = (lambda: marks.pop(0).record()) if marks is not None else (lambda: None)
+
+        def append():
+            if W.ratio == 1:
+                c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+            else:
+                c.kv_append(self.cache, rope_cs=self.rope, cmp=self.cmp_new[s] + [self.ba, self.bb], err=self.err)
+
         if marks is not None:
-            c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+            append()
         else:
             fork, join = torch.cuda.Event(), torch.cuda.Event()
             fork.record(main)
             self.side.wait_event(fork)
             with torch.cuda.stream(self.side):
-                c.kv_append(self.cache, self.kv_new[s], self.ik_new[s], self.rope, err=self.err)
+                append()
             join.record(self.side)
         joined = marks is not None
         for l, role in enumerate(W.layers):
@@ -618,12 +644,13 @@ class GroupDecode:
             if role == "full":
                 c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.scores, err=self.err,
                               ws=self.ws_score, aux=self.aux)
-                c.topk(self.scores, 1, self.q_pos[s], W.topk, self.idx, self.ws_topk, pool_out=self.pool,
-                       pool_count=self.pool_cnt, err=self.err, aux=self.aux)
+                c.topk(self.scores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_topk,
+                       pool_out=self.pool if self.build_pool else None,
+                       pool_count=self.pool_cnt if self.build_pool else None, err=self.err, aux=self.aux)
             elif role == "reindex":
                 c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.pscores,
                               pool=self.pool, err=self.err, ws=self.ws_score, aux=self.paux)
-                c.topk(self.pscores, 1, self.q_pos[s], W.topk, self.idx, self.ws_ptopk, pool=self.pool,
+                c.topk(self.pscores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_ptopk, pool=self.pool,
                        err=self.err, aux=self.paux)
             if not joined:
                 main.wait_event(join)  # the attention reads the new token's window slot
@@ -751,7 +778,7 @@ def run_secondary(args):
             parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
                           "attention_ms": round(b.elapsed_time(c2), 4)})
         line["layer_breakdown"] = parts
-        T = W.context + args.warmup + steps // 2
+        T = (W.context + args.warmup + steps // 2) // W.ratio  # visible entries at the middle step
         nbytes = group_step_bytes(W, T)
         gbs = nbytes / (ms / 1e3) / 1e9
         line.update({"metric": "decoder-group tokens/s and algorithmic HBM GB/s (% of roofline)",
@@ -828,8 +855,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full_decode",
                     choices=["full_decode", "full_decode_small", "tiny_decode", "reindex_decode", "stack_1m",
-                             "prefill_chunk"],
-                    help="full_decode is the headline; reindex_decode, stack_1m and prefill_chunk print their own "
+                             "encoder_decode", "prefill_chunk"],
+                    help="full_decode is the headline; reindex_decode, stack_1m, encoder_decode and prefill_chunk "
+                         "print their own "
                          "measurement line")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -841,7 +869,7 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("reindex_decode", "stack_1m", "prefill_chunk"):
+    elif args.workload in ("reindex_decode", "stack_1m", "encoder_decode", "prefill_chunk"):
         run_secondary(args)
     else:
         run_ours(args)

@@ -77,6 +77,7 @@ class DecodeWorkload:
     pool_block_size: int = 8
     layers: tuple = ("full",)  # sequence of "full" / "reindex" / "reuse"
     steps: int = 1
+    ratio: int = 1  # 2: encoder-style cache, two tokens per entry (compression inputs below)
     device: str = "cpu"
     extra: dict = field(default_factory=dict)
 
@@ -90,6 +91,16 @@ class DecodeWorkload:
 
     def ik(self, seq, start, n, device=None):
         return token_rows(self.seed, S_IK, seq, start, n, 128, device or self.device)
+
+    def cmp_rows(self, seq, start, n, device=None):
+        """Ratio 2: (C^a, C^b, Z^a, Z^b) rows [n, 704] of one sequence's tokens start..start+n-1."""
+        d = device or self.device
+        return tuple(token_rows(self.seed, s, seq, start, n, 704, d) for s in (S_CA, S_CB, S_ZA, S_ZB))
+
+    def bias(self, device=None):
+        """Ratio 2: B^a, B^b [2, 704].  READING: zero positional bias (the workload states none)."""
+        d = device or self.device
+        return (torch.zeros((2, 704), device=d), torch.zeros((2, 704), device=d))
 
     # ----------------------------------------------------------- per step / layer
     def q_idx(self, step, layer, device=None):
@@ -160,7 +171,7 @@ class PrefillWorkload:
                       device=device or self.device).to(torch.bfloat16)
 
 
-# The five workloads: shapes, sizes and distributions of the decode / prefill
+# The workloads: shapes, sizes and distributions of the decode / prefill
 # configurations this library is measured on.
 def tiny_decode(device="cpu"):
     return DecodeWorkload("tiny_decode_b1_t4096", batch=1, context=4096, heads=16, index_heads=4,
@@ -188,6 +199,15 @@ def reindex_decode(device="cuda"):
 def prefill_chunk(device="cuda"):
     return PrefillWorkload("prefill_q8192_prior131072_r2", prior=131072, chunk=8192, heads=64,
                            index_heads=64, topk=512, swa_dtype=1, seed=3, device=device)
+
+
+def encoder_decode(device="cuda"):
+    """An encoder group at decode: ratio-2 caches of 131,072 tokens (65,536 entries),
+    one token appended per step through the compression buffer, a Full layer and
+    five Reuse layers."""
+    return DecodeWorkload("encoder_full_reuse5_b32_t131072_r2", batch=32, context=131072, heads=64,
+                          index_heads=64, topk=512, swa_dtype=1, seed=5, ratio=2,
+                          layers=("full", "reuse", "reuse", "reuse", "reuse", "reuse"), device=device)
 
 
 def stack_1m(device="cuda"):

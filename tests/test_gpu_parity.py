@@ -375,6 +375,54 @@ def test_tiny_decode_step_end_to_end(orc):
     attn_close(out[0].cpu().numpy(), lse[0].cpu().numpy(), r_out, r_lse)
 
 
+def test_encoder_group_decode_steps(orc):
+    """Encoder-style group at decode (ratio 2): every step appends one token per
+    sequence through the compression buffer (an entry completes every second step,
+    the prior length is odd so the first step completes one), then a Full layer over
+    the visible entries (with the sideband, no pool) and two Reuse layers with their
+    own queries.  Cache bytes and indices exact, attention within tolerance."""
+    B, prior, steps, H_I, H, k, seed = 2, 601, 4, 4, 16, 32, 71
+    c, oc, rope, err, (ba, bb), _, _ = build_r2(orc, B, prior, csa2.SWA_MXFP8, seed=seed,
+                                               cap=(prior + steps) // 2 + 8)
+    scale = 1 / math.sqrt(576)
+    g = torch.Generator().manual_seed(72)
+    scores = torch.empty((B, c.capacity), device="cuda")
+    aux = csa2.score_aux(B, c.capacity)
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((B, H, 512), device="cuda")
+    lse = torch.empty((B, H), device="cuda")
+    ws_t = csa2.topk_workspace(B, c.capacity, k)
+    ws_a = csa2.attn_workspace(B, H, k)
+    for s in range(steps):
+        t = prior + s
+        rows = [torch.stack(x) for x in zip(*[cmp_rows(seed, b, t, 1) for b in range(B)])]
+        csa2.kv_append(c, rope_cs=rope, cmp=[r.cuda() for r in rows] + [ba.cuda(), bb.cuda()], err=err)
+        for b in range(B):
+            orc.append_r2(oc[b], *[r[b].numpy() for r in rows], ba.numpy(), bb.numpy(), 1e4)
+        q_pos = torch.full((B,), t, dtype=torch.int64, device="cuda")
+        q_idx = torch.randn((B, H_I, 128), generator=g).to(torch.bfloat16)
+        w = torch.rand((B, H_I), generator=g)
+        qs = [torch.randn((B, H, 576), generator=g).to(torch.bfloat16) for _ in range(3)]
+        csa2.index_score(c, q_idx.cuda(), w.cuda(), q_pos, scores, err=err, aux=aux)
+        csa2.topk(scores, 2, q_pos, k, idx, ws_t, err=err, aux=aux)
+        r_idx = []
+        for layer in range(3):
+            csa2.sparse_attn_decode(c, qs[layer].cuda(), q_pos, idx, out, lse, ws_a, scale, err=err)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0
+            for b in range(B):
+                if layer == 0:
+                    ri, _, _, ro, rl, _ = orc.full_layer(oc[b], u16(q_idx[b]), w[b].numpy(), u16(qs[0][b]), t, k,
+                                                         scale)
+                    assert idx[b].tolist() == ri.tolist(), f"step {s} sequence {b}"
+                    r_idx.append(ri)
+                else:
+                    ro, rl = orc.reuse_layer(oc[b], u16(qs[layer][b]), t, r_idx[b], scale)
+                attn_close(out[b].cpu().numpy(), lse[b].cpu().numpy(), ro, rl)
+    assert c.n_tokens.tolist() == [prior + steps] * B
+    assert_cache_equal(c, oc, (prior + steps) // 2)
+
+
 # ------------------------------------------------------------------ prefill (small)
 def test_prefill_chunk_small(orc):
     prior, Q, H_I, H, k = 300, 70, 4, 16, 32
