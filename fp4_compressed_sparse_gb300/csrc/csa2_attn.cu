@@ -262,10 +262,6 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   const int split = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kHeadBlock;
   const int nh = min(HP, a.heads - hbase);
   const int seq = a.cache_seq < 0 ? row : a.cache_seq;
-  const int64_t qpos = a.q_pos[row];
-  const int64_t T = qpos / a.ratio;
-  const int64_t ntok = a.n_tokens[seq];
-  const int64_t lin_base = a.lin_base ? *a.lin_base : INT64_MAX;
   const int kpad = (a.k + kE - 1) / kE * kE;
   const int total_chunks = (kpad + kWin) / kE;
   const int nchunks = split < total_chunks ? (total_chunks - split + n_splits - 1) / n_splits : 0;
@@ -278,16 +274,20 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     tc::mbar_init(&sm.empty[1], kCons);
     tc::fence_mbar_init();
   }
+  // launched as a programmatic dependent of the previous kernel: the block is
+  // resident and set up while that grid drains, and nothing in memory (query,
+  // positions, token counts, selection) is read before it is complete
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   __syncthreads();  // barriers ready
+  const int64_t qpos = a.q_pos[row];
+  const int64_t T = qpos / a.ratio;
+  const int64_t ntok = a.n_tokens[seq];
+  const int64_t lin_base = a.lin_base ? *a.lin_base : INT64_MAX;
 
   if (tid >= kCons) {
     // ================================================================ producers
     const int pt = tid - kCons;
     const int e = pt >> 2, q4 = pt & 3;
-    // launched as a programmatic dependent of the selection: its indices are
-    // read only after that grid is complete (the consumers' query conversion
-    // does not wait)
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint32_t qmask = 0xFu << (lane & ~3);  // the four lanes of this entry
     const int32_t *idx_row = a.idx + static_cast<size_t>(row) * a.k;
     // software pipeline: once chunk c is handed over, the raw bytes of chunk
