@@ -77,6 +77,22 @@ def dist_env():
     return rank, world, local
 
 
+def replica_seed(seed, rank):
+    """Weak scaling: every rank runs its own batch of independent sequences."""
+    return seed + 1000 * rank
+
+
+def aggregate_ranks(total_ms, batch, steps, world, device):
+    """Whole-job figures of a replicas-only run: the slowest rank's timed total (max
+    over ranks) and the tokens all ranks processed in it.  Returns (total_ms,
+    tokens per second)."""
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, batch * world * steps / (total_ms / 1e3)
+
+
 class ClockSampler:
     """SM clock, power and clock-event reasons sampled through NVML (the driver's
     libnvidia-ml, read-only queries) by a thread polling every ~2 ms, so that
@@ -327,7 +343,7 @@ def run_ours(args):
     csa2.load()
     W = getattr(wl, args.workload)(device="cuda")
     # weak scaling: every rank runs its own batch (independent sequences), seeds offset by rank
-    W.seed = W.seed + 1000 * rank
+    W.seed = replica_seed(W.seed, rank)
     n_steps = args.warmup + args.steps + args.e2e_steps
     bench = FullDecode(W, n_steps, dev)
     flush = L2Flush(dev)
@@ -373,14 +389,8 @@ def run_ours(args):
     if bench.err.item() != 0:
         raise RuntimeError(f"device error word {bench.err.item()} in the timed steps")
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate_ranks(sum(step_ms), W.batch, args.steps, world, dev)
     ms_per_step = total_ms / args.steps
-    tokens = W.batch * world * args.steps
-    value = tokens / (total_ms / 1e3)
 
     # second timed pass, same steps' inputs: each part as its own graph with
     # events between (score, top-k, attention do not change the cache), for the
