@@ -265,7 +265,9 @@ csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t
  *   out: fp32 [batch][n_heads][512] = sum_j p_j c_j; lse: fp32 [batch][n_heads]
  *   = M + log(denominator) (-inf when there is nothing to attend to).
  * n_heads: a multiple of 16, 16..128.  k: 1..2048.
- * ws: device workspace of csa2_attn_workspace_size() bytes (split partials).
+ * ws: device workspace of csa2_attn_workspace_size() bytes, 16-byte aligned:
+ *   the partial (O, m, l) of each split of a row, written and read within the
+ *   call; calls that may run concurrently need separate workspaces.
  * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
  */
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k);
