@@ -425,6 +425,16 @@ def test_ratio2_entry_count_and_visibility(orc):
     c2 = orc.Cache(64, ratio=2)
     orc.append_r2(c2, ca, cb, za, zb, ba, bb, 1e4)  # one append == two appends
     assert np.array_equal(c.lat_codes, c2.lat_codes) and np.array_equal(c.idx_codes, c2.idx_codes)
+    # one token per call, as a decode loop appends: the compression buffer carries the
+    # odd token and the previous entry's b rows across calls; every plane and the
+    # window ring end up as with one call
+    c3 = orc.Cache(64, ratio=2)
+    for j in range(n):
+        orc.append_r2(c3, ca[j:j + 1], cb[j:j + 1], za[j:j + 1], zb[j:j + 1], ba, bb, 1e4)
+    assert c3.n_tokens == 21 and c3.n_entries == 10
+    for name in ("lat_codes", "lat_scales", "rope_codes", "rope_scales", "idx_codes", "idx_scales", "swa_codes",
+                 "swa_scales"):
+        assert np.array_equal(getattr(c3, name), getattr(c2, name)), name
     # [P5] §2.3.1: query t sees entries s < floor(t/m)
     assert orc.visible(20, 2) == 10 and orc.visible(21, 2) == 10 and orc.visible(19, 2) == 9
     # 8,192 tokens -> 4,096 entries (2 tokens per entry)
