@@ -16,7 +16,7 @@ from . import build_lib
 OK = 0
 ERR_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RANGE",
              5: "ERR_UNSUPPORTED", 6: "ERR_CUDA", 7: "ERR_WORKSPACE"}
-DEVERR_CAPACITY, DEVERR_INDEX, DEVERR_NAN, DEVERR_ROPE, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+DEVERR_CAPACITY, DEVERR_INDEX, DEVERR_NAN, DEVERR_ROPE, DEVERR_TIMEOUT, DEVERR_INEXACT = 1, 2, 4, 8, 16, 32
 SWA_BF16, SWA_MXFP8 = 0, 1
 IN_F32, IN_BF16 = 0, 1
 D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128

@@ -4,7 +4,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
 
 #include "csa2_encode.cuh"
 #include "csa2_internal.cuh"
@@ -13,7 +16,12 @@ namespace {
 
 thread_local std::string g_detail;
 
-csa2_status fail(csa2_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+}  // namespace
+
+namespace csa2 {
+
+void set_error_detail(const char *msg) { g_detail = msg ? msg : ""; }
+
 csa2_status fail(csa2_status st, const char *fmt, ...) {
   char buf[512];
   va_list ap;
@@ -29,23 +37,61 @@ csa2_status cuda_status(cudaError_t e, const char *what) {
   return fail(CSA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+int g_sm_count[kMaxDevices] = {};
+std::map<std::pair<int, const void *>, int> g_smem_limit;  // (device, kernel) -> bytes set
+}  // namespace
 
-#define REQUIRE(cond, status, ...) \
-  do {                             \
-    if (!(cond)) return fail(status, __VA_ARGS__); \
-  } while (0)
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_sm_count[dev] > 0) return g_sm_count[dev];
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // a failed query is not sticky: clear it so the next launch reports its own status
+    return 1;
+  }
+  if (dev < kMaxDevices) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    g_sm_count[dev] = n;
+  }
+  return n;
+}
 
-#define REQUIRE_PTR(p)                                                   \
-  do {                                                                   \
-    if ((p) == nullptr) return fail(CSA2_ERR_NULL, "%s is NULL", #p);    \
-    if (!aligned16(p)) return fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
-  } while (0)
+cudaError_t ensure_smem_limit(const void *fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_pair(dev, fn);
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    auto it = g_smem_limit.find(key);
+    if (it != g_smem_limit.end() && it->second >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  int &have = g_smem_limit[key];
+  if (bytes > have) have = bytes;
+  return cudaSuccess;
+}
 
-#define REQUIRE_OPT_PTR(p)                                               \
-  do {                                                                   \
-    if ((p) != nullptr && !aligned16(p)) return fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
-  } while (0)
+}  // namespace csa2
+
+namespace {
+
+using csa2::aligned16;
+using csa2::cuda_status;
+using csa2::fail;
+
+#define REQUIRE CSA2_REQUIRE
+#define REQUIRE_PTR CSA2_REQUIRE_PTR
+#define REQUIRE_OPT_PTR CSA2_REQUIRE_OPT_PTR
 
 csa2_status check_cache(const csa2_cache *c) {
   REQUIRE(c != nullptr, CSA2_ERR_NULL, "cache is NULL");
@@ -89,10 +135,6 @@ csa2_cache seq_view(const csa2_cache &c, int seq) {
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
-
-namespace csa2 {
-void set_error_detail(const char *msg) { g_detail = msg ? msg : ""; }
-}  // namespace csa2
 
 // ===================================================================== prefill kernels
 namespace csa2 {
@@ -351,7 +393,7 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, const void *sco
 
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k) {
   if (batch <= 0 || n_heads <= 0 || k <= 0) return 256;
-  return csa2::attn_workspace_bytes(batch, n_heads, k);
+  return csa2::attn_workspace_bytes(batch, n_heads, csa2::attn_segments(k));
 }
 
 csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, int32_t n_heads, const int64_t *q_pos,
@@ -400,7 +442,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
   a.out = out;
   a.lse = lse;
   a.err = err_word;
-  return cuda_status(csa2::launch_attn(a, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)),
+  return cuda_status(csa2::launch_attn(a, csa2::attn_segments(k), ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream)),
                      "csa2_sparse_attn_decode launch");
 }
 
@@ -443,7 +485,7 @@ PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dt
   L.off_sel = o;
   o = align256(o + csa2::topk_workspace_bytes(qb, capacity, true));
   L.off_attn = o;
-  o = align256(o + csa2::attn_workspace_bytes(qb, n_heads, k));
+  o = align256(o + csa2::attn_workspace_bytes(qb, n_heads, 1));
   L.total = o;
   return L;
 }
@@ -566,7 +608,8 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     aa.out = out + static_cast<size_t>(q0) * n_heads * csa2::kLat;
     aa.lse = lse + static_cast<size_t>(q0) * n_heads;
     aa.err = err_word;
-    e = csa2::launch_attn(aa, wb + L.off_attn, L.total - L.off_attn, s);
+    // one segment per query: each query's attention is one pass over its entries
+    e = csa2::launch_attn(aa, 1, wb + L.off_attn, L.total - L.off_attn, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill attention");
   }
   return cuda_status(cudaGetLastError(), "csa2_prefill_chunk");

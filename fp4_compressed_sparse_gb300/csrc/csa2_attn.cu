@@ -8,7 +8,7 @@
 // (absorbed query: the logit is q_lat . c + q_rope . k_rope, the value is the
 // 512-dim latent c).
 //
-// One CTA = (one split of a row's entry list, up to 64 heads).  Every head
+// One CTA = (some segments of a row's entry list, up to 64 heads).  Every head
 // shares the entries, so each entry is dequantised once per CTA:
 //   producer warps (4)  gather 32 entries at a time and dequantise them into a
 //                       two-stage fp16 ring: E2M1 pairs by cvt.f16x2.e2m1x2, times
@@ -22,11 +22,20 @@
 //                       O tile in registers
 // The query is held as fp16 with a power-of-two scale per head (exact for bf16
 // values within 2^24 of the head's maximum).  Stage handover uses mbarriers
-// with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).  The splits of a
-// row are one thread-block cluster: each writes its unnormalised (O, m, l)
-// straight from registers to a workspace that stays in L2 and, after a cluster
-// barrier, merges a slice of the heads from its peers' partials (flash-decoding
-// LSE merge, then the sink) -- no second kernel.
+// with bounded waits (CSA2_DEVERR_TIMEOUT if one runs out).
+//
+// Batch-invariant schedule ([P5] §3.3: a token's output must not depend on the
+// batch it was computed in, so the accumulation order may not follow the
+// launch shape).  A row's entry list is cut into S segments, S fixed by k and
+// the window alone (chunk c of 32 entries belongs to segment c % S).  Each
+// segment gets its own online softmax and leaves an unnormalised partial
+// (O, m, l); the row's output merges the S partials in segment order
+// (flash-decoding LSE merge, then the sink).  Only the number G of CTAs a row
+// is spread over follows the batch (enough CTAs to fill the SMs): CTA g of the
+// row computes segments g, g + G, ... one after the other, writes their partials
+// to a workspace that stays in L2, and after a cluster barrier (the row's G CTAs
+// are one thread-block cluster) merges a slice of the heads -- the same
+// arithmetic in the same order for any G, so the bits do not change with it.
 #include <cuda_fp16.h>
 
 #include "csa2_internal.cuh"
@@ -44,6 +53,7 @@ constexpr int kHeadBlock = 64;    // heads per CTA at most
 constexpr uint32_t kWaitIters = 200;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxChunks = (CSA2_MAX_TOPK + kWin) / kE;  // chunks of the longest entry list (68)
 
 template <int HP>
 struct __align__(16) AttnSmem {
@@ -55,6 +65,9 @@ struct __align__(16) AttnSmem {
   float alpha[HP];     // this chunk's rescale of O
   float fin[HP][2];    // m, l per head after the last chunk
   float sig[2][kE];    // 2^sigma_j of entry j of a stage; 0 = empty entry
+  int16_t chunk_id[kMaxChunks];  // the CTA's chunks in processing order
+  int8_t seg_end[kMaxChunks];    // the segment a chunk ends, or -1
+  int nchunks;
   __align__(8) uint64_t full[2];
   __align__(8) uint64_t empty[2];
 };
@@ -99,7 +112,7 @@ __device__ __forceinline__ uint32_t h2_splat(float v) {
   __half2 h = __float2half2_rn(v);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-constexpr int kMaxSplits = 8;  // splits of a row = one portable thread-block cluster
+constexpr int kMaxSeg = 8;  // segments of a row; also the most CTAs per row (one portable cluster)
 
 // every non-exited thread of the cluster
 __device__ __forceinline__ void cluster_sync() {
@@ -133,8 +146,8 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, int32_
 
 // The row's entry list: the k selected cache entries padded with empties to
 // kpad = ceil(k / 32) * 32, then the 128 window tokens; chunk c = entries
-// 32c .. 32c + 31.  Split s of S takes chunks s, s + S, s + 2S, ... so every
-// split gets its share of the window.
+// 32c .. 32c + 31.  Segment s of S holds chunks s, s + S, s + 2S, ... so every
+// segment gets its share of the window.
 // Kind of entry j: 0 empty, 1 cache entry, 2 window ring slot, 3 window row
 // of the call.  `sel` is the raw index of a selected entry (read ahead).
 __device__ __forceinline__ int entry_kind(const AttnArgs &a, int seq, int j, int kpad, int32_t sel, int64_t qpos,
@@ -177,22 +190,22 @@ __device__ __forceinline__ void load_fp4(const AttnArgs &a, int64_t src, int q4,
   r.rsc = a.rope_scales[src * 4 + q4];
 }
 
-// Partial results of one (row, head block, split) in the workspace: O [HP][512]
-// then (m, l) [HP][2], fp32.
+// Partial results of one (row, head block, segment) in the workspace: O
+// [HP][512] then (m, l) [HP][2], fp32.
 template <int HP>
 __host__ __device__ constexpr size_t part_floats() { return static_cast<size_t>(HP) * (kLat + 2); }
 
-// The cluster merge of a row's splits, run by every consumer warp of every
-// split after the cluster barrier: split `split` merges heads split, split + S,
-// ... (S = n_splits <= kS) from the partials of all S splits.  A warp takes kH
-// of its heads at a time and requests every partial value of them -- the O rows
-// and the (m, l) pairs -- before it uses any.  Flash-decoding LSE merge, then
-// the sink.
+// The merge of a row's segments, run by every consumer warp of every CTA of
+// the row after the cluster barrier: CTA `cta` of G merges heads cta, cta + G,
+// ... from the partials of all n_seg segments (n_seg <= kS), always in segment
+// order.  A warp takes kH of its heads at a time and requests every partial
+// value of them -- the O rows and the (m, l) pairs -- before it uses any.
+// Flash-decoding LSE merge, then the sink.
 template <int kS, int kH, int HP>
 __device__ __forceinline__ void merge_heads(const AttnArgs &a, const float *part, int row, int hbase, int nh,
-                                            int split, int n_splits, int warp, int nwarps, int lane) {
-  const int stride = n_splits * nwarps;
-  for (int hl0 = split + n_splits * warp; hl0 < nh; hl0 += stride * kH) {
+                                            int cta, int n_cta, int n_seg, int warp, int nwarps, int lane) {
+  const int stride = n_cta * nwarps;
+  for (int hl0 = cta + n_cta * warp; hl0 < nh; hl0 += stride * kH) {
     float4 v[kH][kS][kLat / 128];
     float ms[kH], ls[kH];
 #pragma unroll
@@ -202,12 +215,12 @@ __device__ __forceinline__ void merge_heads(const AttnArgs &a, const float *part
       for (int sp = 0; sp < kS; ++sp)
 #pragma unroll
         for (int c = 0; c < kLat / 128; ++c)
-          v[j][sp][c] = hl < nh && sp < n_splits
+          v[j][sp][c] = hl < nh && sp < n_seg
                             ? ld_cg4(part + sp * part_floats<HP>() + static_cast<size_t>(hl) * kLat + 128 * c + 4 * lane)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
       ms[j] = -INFINITY;
       ls[j] = 0.0f;
-      if (hl < nh && lane < n_splits) {  // lane s < n_splits holds split s's (m, l)
+      if (hl < nh && lane < n_seg) {  // lane s < n_seg holds segment s's (m, l)
         const float2 ml = ld_cg2(part + lane * part_floats<HP>() + static_cast<size_t>(HP) * kLat + 2 * hl);
         ms[j] = ml.x;
         ls[j] = ml.y;
@@ -251,7 +264,7 @@ __device__ __forceinline__ void merge_heads(const AttnArgs &a, const float *part
 }
 
 template <int HP>
-__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_splits, float *part_ws) {
+__global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, int n_cta, int n_seg, float *part_ws) {
   constexpr int kCons = HP * 4;         // consumer threads: HP / 8 warps
   constexpr int kDW = 4096 / HP;        // output dims per consumer warp
   constexpr int kNT = kDW / 8;          // n8 tiles per consumer warp
@@ -259,26 +272,37 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttnSmem<HP> &sm = *reinterpret_cast<AttnSmem<HP> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kHeadBlock;
+  const int cta = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kHeadBlock;
   const int nh = min(HP, a.heads - hbase);
   const int seq = a.cache_seq < 0 ? row : a.cache_seq;
   const int kpad = (a.k + kE - 1) / kE * kE;
   const int total_chunks = (kpad + kWin) / kE;
-  const int nchunks = split < total_chunks ? (total_chunks - split + n_splits - 1) / n_splits : 0;
 
-  // ---- set-up: barriers
+  // ---- set-up: barriers, and this CTA's chunks: segments cta, cta + G, ...,
+  // each segment's chunks in ascending order
   if (tid == 0) {
     tc::mbar_init(&sm.full[0], kProdThreads);
     tc::mbar_init(&sm.full[1], kProdThreads);
     tc::mbar_init(&sm.empty[0], kCons);
     tc::mbar_init(&sm.empty[1], kCons);
     tc::fence_mbar_init();
+    int n = 0;
+    for (int sg = cta; sg < n_seg; sg += n_cta) {
+      for (int ch = sg; ch < total_chunks && n < kMaxChunks; ch += n_seg) {
+        sm.chunk_id[n] = static_cast<int16_t>(ch);
+        sm.seg_end[n] = -1;
+        ++n;
+      }
+      if (n > 0) sm.seg_end[n - 1] = static_cast<int8_t>(sg);
+    }
+    sm.nchunks = n;
   }
   // launched as a programmatic dependent of the previous kernel: the block is
   // resident and set up while that grid drains, and nothing in memory (query,
   // positions, token counts, selection) is read before it is complete
   asm volatile("griddepcontrol.wait;\n" ::: "memory");
-  __syncthreads();  // barriers ready
+  __syncthreads();  // barriers and the chunk list ready
+  const int nchunks = sm.nchunks;
   const int64_t qpos = a.q_pos[row];
   const int64_t T = qpos / a.ratio;
   const int64_t ntok = a.n_tokens[seq];
@@ -294,7 +318,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     // c+1 and the indices of chunk c+2 are requested; they land while this
     // producer waits for a free stage
     auto sel_of = [&](int i) -> int32_t {  // selected index of entry e of local chunk i, or -1
-      const int j = (split + n_splits * i) * kE + e;
+      const int j = sm.chunk_id[i] * kE + e;
       return j < a.k ? idx_row[j] : -1;
     };
     int64_t src = 0;
@@ -302,7 +326,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     Fp4Raw raw;
     int32_t sel_next = -1;
     if (nchunks > 0) {
-      kind = entry_kind(a, seq, split * kE + e, kpad, sel_of(0), qpos, T, ntok, lin_base, src);
+      kind = entry_kind(a, seq, sm.chunk_id[0] * kE + e, kpad, sel_of(0), qpos, T, ntok, lin_base, src);
       if (kind == 1) load_fp4(a, src, q4, raw);
       if (nchunks > 1) sel_next = sel_of(1);
     }
@@ -410,13 +434,12 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       }
       tc::mbar_arrive(&sm.full[st]);
       if (c + 1 < nchunks) {
-        kind = entry_kind(a, seq, (split + n_splits * (c + 1)) * kE + e, kpad, sel_next, qpos, T, ntok, lin_base,
-                          src);
+        kind = entry_kind(a, seq, sm.chunk_id[c + 1] * kE + e, kpad, sel_next, qpos, T, ntok, lin_base, src);
         if (kind == 1) load_fp4(a, src, q4, raw);
         if (c + 2 < nchunks) sel_next = sel_of(c + 2);
       }
     }
-    if (n_splits > 1) cluster_sync();  // the consumers' cluster barrier, matched here
+    if (n_seg > 1) cluster_sync();  // the consumers' cluster barrier, matched here
     return;
   }
 
@@ -537,7 +560,9 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_new = fmaxf(m_run, mx);
-      const float alpha = m_new == -INFINITY ? 1.0f : exp2f(m_run - m_new);
+      // a segment's first chunk (m_run = -inf) rescales O by 0: it drops the
+      // previous segment's O, already written out (O is 0 before the first one)
+      const float alpha = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new);
       float sum = 0.0f;
       uint32_t pw[4];
 #pragma unroll
@@ -590,9 +615,46 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       }
     }
     tc::mbar_arrive(&sm.empty[st]);
+    const int seg = sm.seg_end[c];
+    if (n_seg > 1 && seg >= 0) {
+      // ---- the segment ends: its unnormalised O and (m, l) go to its slot of
+      // the workspace, and the next segment starts from nothing (with m = -inf
+      // its first chunk rescales O by 0).  A wait that ran out in any consumer
+      // warp voids the segment (the error bit is raised).
+      const int alive = bar_consumers_and(kCons, dead ? 0 : 1);
+      float *mine = part_ws + (static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg + seg) * part_floats<HP>();
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int hl = 16 * mt + g + 8 * r;
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt)
+            *reinterpret_cast<float2 *>(mine + hl * kLat + d0 + 8 * nt + 2 * t) =
+                make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
+        }
+      if (sq == 0)
+        *reinterpret_cast<float2 *>(mine + HP * kLat + 2 * sh) =
+            alive ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.0f);
+      m_run = -INFINITY;
+      l_run = 0.0f;
+    }
   }
 
-  // ---- epilogue
+  if (n_seg > 1) {
+    // ---- every segment's partial is in the workspace: after the cluster
+    // barrier (release / acquire at cluster scope) CTA `cta` merges heads cta,
+    // cta + G, ... over all segments
+    cluster_sync();
+    const float *part_row = part_ws + static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg * part_floats<HP>();
+    if (n_seg <= 4)
+      merge_heads<4, 2, HP>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kCons / 32, lane);
+    else
+      merge_heads<kMaxSeg, 1, HP>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kCons / 32, lane);
+    return;
+  }
+
+  // ---- one segment: normalise in registers
   if (sq == 0) {
     sm.fin[sh][0] = m_run;
     sm.fin[sh][1] = l_run;
@@ -600,126 +662,96 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   // a wait that ran out in any consumer warp: the CTA's result is void (the
   // error bit is raised); it still takes part in every barrier below
   const int alive = bar_consumers_and(kCons, dead ? 0 : 1);
-  if (n_splits == 1) {
-    if (!alive) return;
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int hl = 16 * mt + g + 8 * r;
-        if (hl >= nh) continue;
-        const int h = hbase + hl;
-        float m = sm.fin[hl][0], l = sm.fin[hl][1], f = 1.0f;
-        if (a.sink) {
-          const float s2 = a.sink[h] * kLog2e;
-          const float mf = fmaxf(m, s2);
-          f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
-          l = l * f + exp2f(s2 - mf);
-          m = mf;
-        }
-        const float inv = l > 0.0f ? f / l : 0.0f;
-        float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat + d0;
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-          *reinterpret_cast<float2 *>(out + 8 * nt + 2 * t) =
-              make_float2(o[mt][nt][2 * r] * inv, o[mt][nt][2 * r + 1] * inv);
-        if (warp == 0 && t == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      }
-    return;
-  }
-  // ---- the row's splits form one thread-block cluster: each CTA writes its
-  // unnormalised O and (m, l) to its slot of the workspace, then after the
-  // cluster barrier CTA `split` merges heads split, split + S, ... from the
-  // slots of all S splits
-  float *part_row = part_ws + static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_splits * part_floats<HP>();
-  float *mine = part_row + split * part_floats<HP>();
+  if (!alive) return;
 #pragma unroll
   for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int hl = 16 * mt + g + 8 * r;
+      if (hl >= nh) continue;
+      const int h = hbase + hl;
+      float m = sm.fin[hl][0], l = sm.fin[hl][1], f = 1.0f;
+      if (a.sink) {
+        const float s2 = a.sink[h] * kLog2e;
+        const float mf = fmaxf(m, s2);
+        f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
+        l = l * f + exp2f(s2 - mf);
+        m = mf;
+      }
+      const float inv = l > 0.0f ? f / l : 0.0f;
+      float *out = a.out + (static_cast<size_t>(row) * a.heads + h) * kLat + d0;
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt)
-        *reinterpret_cast<float2 *>(mine + hl * kLat + d0 + 8 * nt + 2 * t) =
-            make_float2(o[mt][nt][2 * r], o[mt][nt][2 * r + 1]);
+        *reinterpret_cast<float2 *>(out + 8 * nt + 2 * t) =
+            make_float2(o[mt][nt][2 * r] * inv, o[mt][nt][2 * r + 1] * inv);
+      if (warp == 0 && t == 0) a.lse[static_cast<size_t>(row) * a.heads + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
-  if (sq == 0)  // a CTA whose wait ran out contributes nothing
-    *reinterpret_cast<float2 *>(mine + HP * kLat + 2 * sh) =
-        alive ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.0f);
-  cluster_sync();  // release / acquire at cluster scope: the partials are visible to every CTA of the row
-  if (n_splits <= 4)
-    merge_heads<4, 2, HP>(a, part_row, row, hbase, nh, split, n_splits, warp, kCons / 32, lane);
-  else
-    merge_heads<kMaxSplits, 1, HP>(a, part_row, row, hbase, nh, split, n_splits, warp, kCons / 32, lane);
 }
 
 int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
 
-// Entry splits per (row, head block): fill the 152 SMs once (one CTA per SM),
-// at least one 32-entry chunk per split, at most one portable cluster (8).
-int choose_splits(int rows, int heads, int k) {
+// CTAs per row (one cluster): enough to fill the SMs once (one CTA per SM),
+// at most one per segment.  Only the speed depends on this choice.
+int choose_ctas(int rows, int heads, int n_seg) {
   const int ctas = rows * head_blocks(heads);
-  int s = 152 / ctas;
-  const int max_s = ((k + kE - 1) / kE * kE + kWin) / kE;
-  if (s > max_s) s = max_s;
-  if (s > kMaxSplits) s = kMaxSplits;
-  if (s < 1) s = 1;
-  return s;
+  int g = device_sm_count() / ctas;
+  if (g > n_seg) g = n_seg;
+  if (g < 1) g = 1;
+  return g;
 }
 
 template <int HP>
-cudaError_t launch_hp(const AttnArgs &a, int n_splits, float *part, cudaStream_t st) {
-  static bool attr_set = false;
+cudaError_t launch_hp(const AttnArgs &a, int n_cta, int n_seg, float *part, cudaStream_t st) {
   const int smem = static_cast<int>(sizeof(AttnSmem<HP>));
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_attn<HP>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_splits, a.rows, head_blocks(a.heads));
+  cfg.gridDim = dim3(n_cta, a.rows, head_blocks(a.heads));
   cfg.blockDim = dim3(HP * 4 + kProdThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = n_splits;  // the row's splits: one cluster
+  attr[0].val.clusterDim.x = n_cta;  // the row's CTAs: one cluster
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_splits, part);
+  return cudaLaunchKernelEx(&cfg, k_attn<HP>, a, n_cta, n_seg, part);
 }
 
 }  // namespace
 
-// Workspace: the partial (O, m, l) of every split of every (row, head block)
-// when rows are split, sized for any call with at most `rows` rows (a prefill
-// block may be shorter than the block the workspace was sized for, and fewer
-// rows take more splits).
-size_t attn_workspace_bytes(int rows, int heads, int k) {
-  size_t most = 0;
-  for (int r = 1; r <= rows && r <= 152; ++r) {
-    const int s = choose_splits(r, heads, k);
-    if (s > 1) most = std::max(most, static_cast<size_t>(r) * head_blocks(heads) * s);
-  }
-  return most * part_floats<kHeadBlock>() * sizeof(float) + 256;
+// Segments of a decode row's entry list: fixed by k and the window alone (never
+// by the batch), at most one portable cluster of CTAs' worth (8), at least one
+// chunk each.
+int attn_segments(int k) {
+  const int chunks = ((k + kE - 1) / kE * kE + kWin) / kE;
+  return chunks < kMaxSeg ? chunks : kMaxSeg;
 }
 
-cudaError_t launch_attn(const AttnArgs &a0, void *ws, size_t ws_bytes, cudaStream_t st) {
+// Workspace: the partial (O, m, l) of every segment of every (row, head block)
+// when a row has more than one segment.
+size_t attn_workspace_bytes(int rows, int heads, int n_seg) {
+  if (n_seg <= 1) return 256;
+  return static_cast<size_t>(rows) * head_blocks(heads) * n_seg * part_floats<kHeadBlock>() * sizeof(float) + 256;
+}
+
+cudaError_t launch_attn(const AttnArgs &a0, int n_seg, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (a0.rows <= 0) return cudaSuccess;
-  const int n_splits = choose_splits(a0.rows, a0.heads, a0.k);
-  if (n_splits > 1 &&
-      (ws == nullptr || ws_bytes < static_cast<size_t>(a0.rows) * head_blocks(a0.heads) * n_splits *
+  if (n_seg < 1 || n_seg > kMaxSeg) return cudaErrorInvalidValue;
+  const int n_cta = choose_ctas(a0.rows, a0.heads, n_seg);
+  if (n_seg > 1 &&
+      (ws == nullptr || ws_bytes < static_cast<size_t>(a0.rows) * head_blocks(a0.heads) * n_seg *
                                        part_floats<kHeadBlock>() * sizeof(float) ||
        reinterpret_cast<uintptr_t>(ws) % 16 != 0))
     return cudaErrorInvalidValue;
   float *part = static_cast<float *>(ws);
-  if (a0.heads <= 16) return launch_hp<16>(a0, n_splits, part, st);
-  if (a0.heads <= 32) return launch_hp<32>(a0, n_splits, part, st);
-  return launch_hp<64>(a0, n_splits, part, st);
+  if (a0.heads <= 16) return launch_hp<16>(a0, n_cta, n_seg, part, st);
+  if (a0.heads <= 32) return launch_hp<32>(a0, n_cta, n_seg, part, st);
+  return launch_hp<64>(a0, n_cta, n_seg, part, st);
 }
 
 }  // namespace csa2

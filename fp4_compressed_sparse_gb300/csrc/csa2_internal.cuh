@@ -5,8 +5,37 @@
 
 namespace csa2 {
 
+// ------------------------------------------------------------------ host helpers (csa2_api.cu)
 // thread-local text returned by csa2_last_error_detail()
 void set_error_detail(const char *msg);
+// records a printf-style detail for csa2_last_error_detail() and returns st
+csa2_status fail(csa2_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+// CSA2_OK for cudaSuccess, else CSA2_ERR_CUDA with "what: <CUDA error text>" as the detail
+csa2_status cuda_status(cudaError_t e, const char *what);
+// SM count of the current device (queried once per device)
+int device_sm_count();
+// Raises fn's dynamic shared-memory limit to at least `bytes` on the current
+// device (the attribute is per device: set once per (device, kernel)).
+cudaError_t ensure_smem_limit(const void *fn, int bytes);
+
+__host__ __forceinline__ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define CSA2_REQUIRE(cond, status, ...)                  \
+  do {                                                   \
+    if (!(cond)) return ::csa2::fail(status, __VA_ARGS__); \
+  } while (0)
+
+#define CSA2_REQUIRE_PTR(p)                                                                 \
+  do {                                                                                      \
+    if ((p) == nullptr) return ::csa2::fail(CSA2_ERR_NULL, "%s is NULL", #p);               \
+    if (!::csa2::aligned16(p)) return ::csa2::fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+#define CSA2_REQUIRE_OPT_PTR(p)                                                             \
+  do {                                                                                      \
+    if ((p) != nullptr && !::csa2::aligned16(p))                                            \
+      return ::csa2::fail(CSA2_ERR_ALIGN, "%s is not 16-byte aligned", #p);                 \
+  } while (0)
 
 cudaError_t launch_kv_append(const csa2_cache &c, const void *kv, const void *ik, int in_dtype,
                              const csa2_compress_in *cmp, const float *rope_cs, int64_t rope_len, int n_new,
@@ -92,7 +121,10 @@ struct AttnArgs {
   float *out, *lse;
   int32_t *err;
 };
-size_t attn_workspace_bytes(int rows, int heads, int k);
-cudaError_t launch_attn(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t s);
+// Segments of a decode row (a function of k alone: the batch-invariant
+// accumulation order); a row's output is the ordered merge of its segments.
+int attn_segments(int k);
+size_t attn_workspace_bytes(int rows, int heads, int n_seg);
+cudaError_t launch_attn(const AttnArgs &a, int n_seg, void *ws, size_t ws_bytes, cudaStream_t s);
 
 }  // namespace csa2

@@ -11,7 +11,9 @@
 // products of doubled E2M1 codes (dp4a), per 32-wide block, scaled by
 // 2^(eq+ek-2).  The four block terms and the fp32 sum are exact whenever the
 // block exponents of the pair span <= 9 binades, so d_h equals the fp32 value of
-// the exact dot; the head reduction is the fixed-order chain
+// the exact dot; a visible key whose pair with some head exceeds that span
+// raises CSA2_DEVERR_INEXACT (blocks with scale code 0 take no part, as in the
+// tensor-core path).  The head reduction is the fixed-order chain
 // acc = fma(w_h, max(d_h, +0), acc).
 #include "csa2_internal.cuh"
 
@@ -19,6 +21,34 @@ namespace csa2 {
 namespace {
 
 constexpr int kThreads = 128;  // one key per thread
+constexpr int kMaxExactSpan = 9;
+
+// max - min of the nonzero E8M0 codes packed in w (0 if fewer than two)
+__device__ __forceinline__ int span4(uint32_t w) {
+  int mx = 0, mn = 255;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = static_cast<int>((w >> (8 * j)) & 0xFFu);
+    if (c) {
+      mx = max(mx, c);
+      mn = min(mn, c);
+    }
+  }
+  return mx >= mn ? mx - mn : 0;
+}
+// span of e_q,j + e_k,j over the blocks where both codes are nonzero
+__device__ __forceinline__ int pair_span4(uint32_t wq, uint32_t wk) {
+  int mx = 0, mn = 1024;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int cq = static_cast<int>((wq >> (8 * j)) & 0xFFu), ck = static_cast<int>((wk >> (8 * j)) & 0xFFu);
+    if (cq && ck) {
+      mx = max(mx, cq + ck);
+      mn = min(mn, cq + ck);
+    }
+  }
+  return mx >= mn ? mx - mn : 0;
+}
 
 __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
   extern __shared__ uint32_t smem[];
@@ -26,6 +56,7 @@ __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
   uint32_t *s_q = smem;                                          // [H][32] int8x4 words (2*E2M1 of q)
   float *s_qf = reinterpret_cast<float *>(s_q + H * 32);          // [H][4] 2^(eq-1)
   float *s_w = s_qf + H * 4;                                      // [H]
+  uint32_t *s_qc = reinterpret_cast<uint32_t *>(s_w + H);         // [H] the four block scale codes
 
   const int r = blockIdx.y;
   const int64_t T = a.q_pos[r] / a.ratio;  // visible entries
@@ -51,6 +82,7 @@ __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
       s_q[h * 32 + blk * 8 + 2 * i + 1] = e2m1x4_twice_i8(w4[i] >> 16);
     }
     s_qf[h * 4 + blk] = pow2f(static_cast<int>(sc) - 128);
+    reinterpret_cast<uint8_t *>(s_qc + h)[blk] = static_cast<uint8_t>(sc);
   }
   for (int h = threadIdx.x; h < H; h += kThreads) s_w[h] = a.w[static_cast<size_t>(r) * H + h];
   __syncthreads();
@@ -85,6 +117,18 @@ __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) kf[blk] = pow2f(static_cast<int>((ksc >> (8 * blk)) & 0xFFu) - 128);
 
+  // exactness bound: the sum of the query's and the key's spans bounds every
+  // pair's; only when it fails is each head checked
+  {
+    int qmax = 0;
+    for (int h = 0; h < H; ++h) qmax = max(qmax, span4(s_qc[h]));
+    if (qmax + span4(ksc) > kMaxExactSpan) {
+      bool bad = false;
+      for (int h = 0; h < H && !bad; ++h) bad = pair_span4(s_qc[h], ksc) > kMaxExactSpan;
+      if (bad) raise_err(a.err, CSA2_DEVERR_INEXACT);
+    }
+  }
+
   float acc = 0.0f;
   for (int h = 0; h < H; ++h) {
     float t[4];
@@ -109,7 +153,7 @@ cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s) {
   const int64_t nslots = a.pool ? static_cast<int64_t>(a.pool_blocks) * a.pool_bs : a.stride;
   if (nslots <= 0 || a.rows <= 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((nslots + kThreads - 1) / kThreads), a.rows);
-  const size_t smem = static_cast<size_t>(a.heads) * (32 * 4 + 4 * 4 + 4);
+  const size_t smem = static_cast<size_t>(a.heads) * (32 * 4 + 4 * 4 + 4 + 4);
   k_index_score_dp4a<<<grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

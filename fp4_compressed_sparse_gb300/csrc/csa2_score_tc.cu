@@ -15,23 +15,38 @@
 // thread of a key reads its N accumulators and runs the fixed-order chain
 // acc = fma(w_h, max(d_h, +0), acc).
 //
-// Persistent CTA per SM, warp-specialised:
-//   warps 0, 1  producers, alternate tiles (a single thread issuing every bulk
-//               copy caps the stream well below HBM speed): bulk copies of
-//               the key tiles (8 KB codes + 512 B scales, already stored in the
-//               MMA operand layout) into an 8-stage ring; Reindex (POOL) tiles
-//               are gathered by warp 0 alone; warp 0 also puts each row's
-//               query operand into one of two B slots
-//   warps 2, 3  MMA issuers, alternate tiles (one thread issuing every tcgen05
-//               op of the CTA could not keep up): scale factors to TMEM
-//               (tcgen05.cp), two MMAs, commits that free the stage and hand
-//               the accumulator over
-//   warps 4..15 epilogue: three TMEM accumulators, four warps each (one per
-//               32-lane quarter); tile j of the CTA goes to accumulator j % 3.
-//               With a sideband buffer the epilogue also histograms the score
-//               keys (and, in FULL mode, the 8-position block maxima) in shared
-//               memory and adds them to the row's global histogram once the
-//               CTA is done with the row, so top-k needs no pass of its own.
+// Exactness: a block sum is an integer below 2^13, and with 4 blocks the dot is
+// an integer multiple of its smallest block's unit below 2^(15 + span), where
+// span = max - min of the pair's block exponents e_q,j + e_k,j.  With span <= 9
+// it fits the 24-bit fp32 significand, so the tensor core's fp32 result is the
+// exact dot, rounded once (the value the oracle defines).  The MMA-issuing warps
+// check every tile against that bound from the scale bytes in shared memory
+// (blocks whose scale code is 0 -- all-zero blocks -- take no part) and raise
+// CSA2_DEVERR_INEXACT if some (head, visible key) pair exceeds it.
+//
+// Persistent CTA per SM, warp-specialised (tile j of a CTA, counted over the
+// tiles of its item range, goes to producer j % 2, issuer j % 2 and
+// accumulator j % kAcc):
+//   warps 0, 1  producers (a single thread issuing every bulk copy caps the
+//               stream well below HBM speed).  FULL: lane 0 of each warp issues
+//               two bulk copies per tile (8 KB codes + 512 B scales, already
+//               stored in the MMA operand layout) into a 14-stage ring.  POOL
+//               (Reindex): all 32 lanes of both warps gather the tile's 16 pool
+//               blocks with zero-filling cp.async, four tiles in flight per warp.
+//               Warp 0 also loads each row's query record into one of two B
+//               slots.
+//   warps 2, 3  MMA issuers: lane 0 copies the scale factors to TMEM
+//               (tcgen05.cp), issues the two MMAs and the commits that free the
+//               stage and hand the accumulator over; the whole warp checks the
+//               exactness bound on the tile's scale bytes.
+//   the rest    epilogue: four warps (one per 32-lane TMEM quarter) per
+//               accumulator, four accumulators (two when 4 x N columns do not
+//               fit TMEM beside the scale factors).  A thread owns one key: it
+//               reads the key's N accumulator columns and runs the fixed-order
+//               chain.  With a sideband buffer the epilogue also histograms the
+//               score keys (and, in FULL mode, the 8-position block maxima) in
+//               shared memory and adds them to the row's global histogram once
+//               the CTA is done with the row, so top-k needs no pass of its own.
 // Every mbarrier wait is bounded; a wait that runs out raises
 // CSA2_DEVERR_TIMEOUT, sets a CTA abort flag and the CTA drains and exits.
 #include "csa2_internal.cuh"
@@ -173,6 +188,48 @@ __device__ __forceinline__ bool wait_warp(Smem &sm, uint64_t *bar, uint32_t phas
   int ok = 0;
   if ((threadIdx.x & 31) == 0) ok = wait1(sm, bar, phase, err) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Bounded wait by lane 0 for the whole warp; once it succeeds every lane
+// observes the completed phase itself (its acquire of the copied data).  The
+// phase cannot move on meanwhile: the waiter has not released the buffer yet.
+__device__ __forceinline__ bool wait_all(Smem &sm, uint64_t *bar, uint32_t phase, int32_t *err) {
+  if (!wait_warp(sm, bar, phase, err)) return false;
+  tc::mbar_wait_bounded(bar, phase, kWaitIters);
+  return true;
+}
+
+// Exactness bound of the block-scaled dot (see the file header).
+constexpr int kMaxExactSpan = 9;
+// max - min of the nonzero E8M0 codes of the four blocks packed in w (0 if fewer than two)
+__device__ __forceinline__ int code_span(uint32_t w) {
+  int mx = 0, mn = 255;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = static_cast<int>((w >> (8 * j)) & 0xFFu);
+    if (c) {
+      mx = max(mx, c);
+      mn = min(mn, c);
+    }
+  }
+  return mx >= mn ? mx - mn : 0;
+}
+// span of the exponents e_q,j + e_k,j over the blocks where both codes are nonzero
+__device__ __forceinline__ int pair_span(uint32_t wq, uint32_t wk) {
+  int mx = 0, mn = 1024;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int cq = static_cast<int>((wq >> (8 * j)) & 0xFFu), ck = static_cast<int>((wk >> (8 * j)) & 0xFFu);
+    if (cq && ck) {
+      mx = max(mx, cq + ck);
+      mn = min(mn, cq + ck);
+    }
+  }
+  return mx >= mn ? mx - mn : 0;
+}
+// the four block scale codes of query head h in a record's scale-factor atom
+__device__ __forceinline__ uint32_t sfb_word(const uint8_t *sf, int h) {
+  return *reinterpret_cast<const uint32_t *>(sf + 16 * (h % 32) + 4 * (h / 32));
 }
 
 __device__ __forceinline__ uint32_t sel_key(float f) { return isnan(f) ? 0u : orderable(f); }
@@ -382,48 +439,102 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       for (; npend > 0; --npend) hand_over((jlast - (npend - 1) * nprod) % kStages);
     }
     if (lane == 0) sm.issued[pw] = mine;
-  } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
-    // ------------------------------------------------------------ MMA issuers (one thread each)
+  } else if (warp >= kProducers && warp < kProducers + kIssuers) {
+    // ------------------------------------------------------------ MMA issuers (one warp each)
     // issuer `who` takes the CTA's tiles j with j % kIssuers == who (accumulators
     // and stages who, who + kIssuers, ...); each keeps its own copy of the row's
-    // query scale factors in TMEM
+    // query scale factors in TMEM.  Lane 0 issues every tcgen05 op; the whole
+    // warp checks the exactness bound.
     const int who = warp - kProducers;
     int bchanges = 0, jrow = 0;
     const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
-    bool dead = false;
+    bool dead = false, flagged = false;
     for (int row = row0; row <= row_last && !dead; ++row) {
       int t0, t1;
       row_span(row, t0, t1);
       if (t1 <= t0) continue;
       const int bs = bchanges & 1;
-      if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
+      if (!wait_all(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
         dead = true;
         break;
       }
       ++bchanges;
-      tc::tc_fence_after();
       const uint32_t sfb = tmem + col_sfb + 8 * (2 * who + bs);
-      tc::tmem_cp_32x128b_x4(sfb, tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
+      if (lane == 0) {
+        tc::tc_fence_after();
+        tc::tmem_cp_32x128b_x4(sfb, tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
+      }
+      // widest block-exponent span over the row's query heads (padding heads are zero)
+      const uint8_t *qsf = sm.bslot[bs] + np * 64;
+      int qspan = 0;
+      for (int h = lane; h < np; h += 32) qspan = max(qspan, code_span(sfb_word(qsf, h)));
+      qspan = __reduce_max_sync(0xffffffffu, qspan);
+      const int64_t nslots = row_slots(a, row);
       for (int tile = first_own(t0, jrow, kIssuers, who); tile < t1; tile += kIssuers) {
         const int j = jrow + (tile - t0), s = j % kStages, acc = j % kAcc;
-        if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err) ||
-            (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err))) {
+        if (!wait_all(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) {
           dead = true;
           break;
         }
-        tc::tc_fence_after();
-        const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
-        tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
-        const uint32_t d = tmem + acc * np;
-        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
-                     tmem + col_sfa + 8 * acc, sfb, 0);
-        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
-                     tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb, 1);
-        tc::mma_commit(&sm.empty[s]);
-        tc::mma_commit(&sm.tfull[acc]);
+        // this lane's keys m = lane + 32 i: word i holds their four block scale codes
+        const uint4 kw = *reinterpret_cast<const uint4 *>(sm.stage[s] + kIdxTileCodeBytes + 16 * lane);
+        const uint32_t kwi[4] = {kw.x, kw.y, kw.z, kw.w};
+        int kspan = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (pool_mode || static_cast<int64_t>(tile) * kIdxTile + lane + 32 * i < nslots)
+            kspan = max(kspan, code_span(kwi[i]));
+        kspan = __reduce_max_sync(0xffffffffu, kspan);  // the scale bytes are in registers: the stage may go
+        if (lane == 0) {
+          if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) {
+            dead = true;
+          } else {
+            tc::tc_fence_after();
+            const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
+            tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc,
+                                   tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
+            const uint32_t d = tmem + acc * np;
+            tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
+                         tmem + col_sfa + 8 * acc, sfb, 0);
+            tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
+                         tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb,
+                         1);
+            tc::mma_commit(&sm.empty[s]);
+            tc::mma_commit(&sm.tfull[acc]);
+          }
+        }
+        if (__shfl_sync(0xffffffffu, dead ? 1 : 0, 0)) {
+          dead = true;
+          break;
+        }
+        if (!flagged && qspan + kspan > kMaxExactSpan) {
+          // rare: the per-tile bound fails; check every (head, visible key) pair
+          int bad = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + lane + 32 * i;
+            bool valid;
+            if (!pool_mode) {
+              valid = slot < nslots;
+            } else {
+              const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
+                                      ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
+                                      : -1;
+              const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
+              valid = pid >= 0 && p < a.s.q_pos[row] / a.s.ratio && p < a.s.cap;
+            }
+            if (!valid || code_span(kwi[i]) + qspan <= kMaxExactSpan) continue;
+#pragma unroll 1
+            for (int h = 0; h < np && !bad; ++h) bad = pair_span(sfb_word(qsf, h), kwi[i]) > kMaxExactSpan;
+          }
+          if (__any_sync(0xffffffffu, bad)) {
+            if (lane == 0) raise_err(a.s.err, CSA2_DEVERR_INEXACT);
+            flagged = true;
+          }
+        }
       }
       // the row's B slot is free once both issuers' MMAs of the row are done
-      if (!dead) tc::mma_commit(&sm.bempty[bs]);
+      if (!dead && lane == 0) tc::mma_commit(&sm.bempty[bs]);
       jrow += t1 - t0;
     }
   } else if (warp >= kFirstEpiWarp) {
@@ -600,13 +711,7 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
              : idx_tiles(s.cap < s.stride ? s.cap : s.stride));
   const int64_t total = static_cast<int64_t>(s.rows) * max_tiles;
   if (total <= 0) return cudaGetLastError();
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (num_sms <= 0) num_sms = 148;
-  }
+  const int num_sms = device_sm_count();
   const size_t smem = sizeof(Smem) + 1024;
   using KernelFn = void (*)(TcArgs, int, int64_t, int64_t);
   KernelFn fn = nullptr;
@@ -623,13 +728,8 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
     default: fn = CSA2_SCORE_FN(128); break;
   }
 #undef CSA2_SCORE_FN
-  static bool attr[18] = {};
-  const int slot = a.np / 16 + (full_aux ? 9 : 0);
-  if (!attr[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr[slot] = true;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(fn), static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   const int64_t grid = total < num_sms ? total : num_sms;
   const int64_t per = (total + grid - 1) / grid;
   cudaLaunchConfig_t cfg = {};

@@ -11,20 +11,24 @@
 // every mode); -0 == +0, NaN ranks lowest.  Every K is distinct, so the chosen
 // set never depends on scheduling.
 //
-// One 1024-thread CTA per (row, problem) -- problem 0 is the top-k over the
-// row's slots, problem 1 the top blocks by block maximum (FULL rows building a
-// pool) -- and everything in shared memory:
-//   1. the row's 13-bit key histogram (the score kernel's sideband) gives the
-//      threshold bin, where the count from the top reaches k, and how many
-//      keys lie strictly above it;
-//   2. one pass over the row (just written, so mostly from L2): a slot whose
-//      key lies above the threshold bin is chosen outright and marked in a
-//      bitmap (one warp ballot per 32 slots writes one word); keys in the
-//      threshold bin go to a candidate list (at most kSelCap);
-//   3. an exact radix select over the candidates' low 51 key bits marks the
-//      ones still needed (after an overflow of the list it runs over the row);
-//   4. a block scan of the bitmap writes the chosen positions in ascending
-//      order, -1 padded.
+// One thread-block cluster of 4 or 8 CTAs (512 threads each) per (row, problem)
+// -- problem 0 is the top-k over the row's slots, problem 1 the top blocks by
+// block maximum (FULL rows building a pool).  Each CTA of the cluster owns a
+// contiguous slice of the row's bitmap words, in shared memory (in the
+// workspace when a slice exceeds 128 KB):
+//   1. every CTA reads the row's 13-bit key histogram (the score kernel's
+//      sideband) and finds the threshold bin, where the count from the top
+//      reaches k, and how many keys lie strictly above it;
+//   2. one pass over its slice of the row (just written, so mostly from L2): a
+//      slot whose key lies above the threshold bin is chosen outright and marked
+//      in the slice's bitmap (one warp ballot per 32 slots writes one word);
+//      keys in the threshold bin go to the CTA's candidate list;
+//   3. after a cluster barrier the leader CTA gathers every candidate list
+//      through distributed shared memory, runs an exact radix select over the
+//      candidates' low 51 key bits and marks the ones still needed in their
+//      owners' slices (after an overflow of the lists it runs over the row);
+//   4. each CTA scans its slice's popcounts, offsets them by the lower slices'
+//      counts and writes the chosen positions in ascending order, -1 padded.
 // Slots run in ascending position order in every mode, so the bitmap order is
 // the output order and no sort is needed.
 #include "csa2_internal.cuh"
@@ -557,16 +561,12 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
   const int nprob = (!a.pool && a.out_pool_blocks > 0) ? 2 : 1;
   // CTAs per (row, problem): 8 for long rows while the launch still fits one wave
   // of two CTAs per SM, else 4
-  const int ncl = (a.rows * nprob * kSelClusterMax <= 2 * 152 && w0 >= 4096) ? kSelClusterMax : 4;
+  const int ncl = (a.rows * nprob * kSelClusterMax <= 2 * device_sm_count() && w0 >= 4096) ? kSelClusterMax : 4;
   const int64_t slice = span_words(w0, ncl);
   const int in_smem = slice <= kSmemBitmapWords ? 1 : 0;
   const int smem = static_cast<int>(sizeof(SelSmem) + (in_smem ? slice * 4 : 0));
-  static int attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = smem;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_select), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncl, a.rows, nprob);
   cfg.blockDim = dim3(kSelThreads);
@@ -579,7 +579,7 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
   cl[0].val.clusterDim.z = 1;
   cfg.attrs = cl;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_select, a, aux, aux_row, bitmap, in_smem, ncl);
+  e = cudaLaunchKernelEx(&cfg, k_select, a, aux, aux_row, bitmap, in_smem, ncl);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

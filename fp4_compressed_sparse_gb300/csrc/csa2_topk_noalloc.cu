@@ -16,6 +16,13 @@
 // The histograms are cleared at the start of every call and the selection
 // state is written before it is read; nothing in the array needs a known value
 // on entry.
+//
+// Host code must not hand g_topk_scratch itself to a kernel: on the host that
+// name is a stand-in, not a device address.  The first call on each device,
+// with that device current, asks the runtime for the array's device address
+// (cudaGetSymbolAddress) and keeps it for the rest of the process; the address
+// belongs to the device's current context, so a cudaDeviceReset after that
+// first call is not supported.
 #include <cstdio>
 #include <mutex>
 
@@ -31,8 +38,7 @@ static __device__ __align__(256) uint8_t g_topk_scratch[kNoAllocScratchBytes];
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_topk_scratch on the current device (looked up once per
-// device; the name alone is a host-side stand-in and must not be passed to a kernel).
+// Device address of g_topk_scratch on the current device (looked up once per device).
 cudaError_t scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -49,8 +55,6 @@ cudaError_t scratch_address(void **out) {
   return cudaSuccess;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
@@ -58,42 +62,38 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stri
                                          int32_t pool_block_size, int32_t k, int32_t *idx_out,
                                          int32_t out_pool_blocks, int32_t *pool_out, int32_t *pool_count,
                                          int32_t *err_word, csa2_stream_t stream) {
-  if (!scores || !q_pos || !idx_out) return CSA2_ERR_NULL;
-  if (!aligned16(scores) || !aligned16(q_pos) || !aligned16(idx_out)) return CSA2_ERR_ALIGN;
-  if (batch < 1 || batch > 65535 || score_stride < 1) return CSA2_ERR_SHAPE;
-  if (ratio != 1 && ratio != 2) return CSA2_ERR_RANGE;
-  if (k < 1 || k > CSA2_MAX_TOPK) return CSA2_ERR_RANGE;
-  if (pool_block_size < 1 || pool_block_size > 64) return CSA2_ERR_SHAPE;
+  CSA2_REQUIRE_PTR(scores);
+  CSA2_REQUIRE_PTR(q_pos);
+  CSA2_REQUIRE_PTR(idx_out);
+  CSA2_REQUIRE(batch >= 1 && batch <= 65535, CSA2_ERR_SHAPE, "batch %d outside 1..65535", batch);
+  CSA2_REQUIRE(score_stride >= 1, CSA2_ERR_SHAPE, "score_stride %lld < 1", static_cast<long long>(score_stride));
+  CSA2_REQUIRE(ratio == 1 || ratio == 2, CSA2_ERR_RANGE, "ratio %d (must be 1 or 2)", ratio);
+  CSA2_REQUIRE(k >= 1 && k <= CSA2_MAX_TOPK, CSA2_ERR_RANGE, "k %d outside 1..2048", k);
+  CSA2_REQUIRE(pool_block_size >= 1 && pool_block_size <= 64, CSA2_ERR_SHAPE, "pool_block_size %d outside 1..64",
+               pool_block_size);
   if (pool) {
-    if (!aligned16(pool)) return CSA2_ERR_ALIGN;
-    if (pool_blocks < 1 || score_stride < static_cast<int64_t>(pool_blocks) * pool_block_size)
-      return CSA2_ERR_SHAPE;
-    if (pool_out) return CSA2_ERR_RANGE;
+    CSA2_REQUIRE_PTR(pool);
+    CSA2_REQUIRE(pool_blocks >= 1, CSA2_ERR_SHAPE, "pool_blocks %d < 1", pool_blocks);
+    CSA2_REQUIRE(score_stride >= static_cast<int64_t>(pool_blocks) * pool_block_size, CSA2_ERR_SHAPE,
+                 "score_stride %lld < pool_blocks*pool_block_size", static_cast<long long>(score_stride));
+    CSA2_REQUIRE(pool_out == nullptr, CSA2_ERR_RANGE, "a pool can only be built in FULL mode");
   }
   if (pool_out) {
-    if (!pool_count) return CSA2_ERR_NULL;
-    if (!aligned16(pool_out) || !aligned16(pool_count)) return CSA2_ERR_ALIGN;
-    if (out_pool_blocks < 1 || out_pool_blocks > CSA2_MAX_TOPK) return CSA2_ERR_RANGE;
-    if (pool_block_size != 8) return CSA2_ERR_UNSUPPORTED;
+    CSA2_REQUIRE_PTR(pool_out);
+    CSA2_REQUIRE_PTR(pool_count);
+    CSA2_REQUIRE(out_pool_blocks >= 1 && out_pool_blocks <= CSA2_MAX_TOPK, CSA2_ERR_RANGE,
+                 "out_pool_blocks %d outside 1..2048", out_pool_blocks);
+    CSA2_REQUIRE(pool_block_size == 8, CSA2_ERR_UNSUPPORTED, "the candidate pool is built from 8-position blocks");
   }
   // the same scratch layout csa2_topk uses for its caller workspace
   const size_t need = csa2::topk_workspace_bytes(batch, score_stride, false);
-  if (need > kNoAllocScratchBytes) {
-    char msg[256];
-    snprintf(msg, sizeof(msg),
-             "csa2_topk_noalloc: batch %d x score_stride %lld needs %zu bytes of scratch; the built-in "
-             "array holds %zu (use csa2_topk with a caller workspace)",
-             batch, static_cast<long long>(score_stride), need, kNoAllocScratchBytes);
-    csa2::set_error_detail(msg);
-    return CSA2_ERR_WORKSPACE;
-  }
+  CSA2_REQUIRE(need <= kNoAllocScratchBytes, CSA2_ERR_WORKSPACE,
+               "csa2_topk_noalloc: batch %d x score_stride %lld needs %zu bytes of scratch; the built-in array "
+               "holds %zu (use csa2_topk with a caller workspace)",
+               batch, static_cast<long long>(score_stride), need, kNoAllocScratchBytes);
   void *ws = nullptr;
-  const cudaError_t ce = scratch_address(&ws);
-  if (ce != cudaSuccess) {
-    csa2::set_error_detail(cudaGetErrorString(ce));
-    return CSA2_ERR_CUDA;
-  }
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const csa2_status st = csa2::cuda_status(scratch_address(&ws), "csa2_topk_noalloc scratch address");
+  if (st != CSA2_OK) return st;
   csa2::TopkArgs a{};
   a.rows = batch;
   a.scores = scores;
@@ -110,6 +110,6 @@ extern "C" csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stri
   a.pool_out = pool_out;
   a.pool_count = pool_count;
   a.err = err_word;
-  if (csa2::launch_topk(a, ws, s) != cudaSuccess) return CSA2_ERR_CUDA;
-  return CSA2_OK;
+  return csa2::cuda_status(csa2::launch_topk(a, ws, reinterpret_cast<cudaStream_t>(stream)),
+                           "csa2_topk_noalloc launch");
 }

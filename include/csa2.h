@@ -57,6 +57,7 @@ typedef enum csa2_status {
 #define CSA2_DEVERR_NAN 4u      /* a NaN index score (it ranks lowest)                */
 #define CSA2_DEVERR_ROPE 8u     /* a position outside the RoPE table (nothing written) */
 #define CSA2_DEVERR_TIMEOUT 16u /* a bounded device wait gave up (outputs unspecified)  */
+#define CSA2_DEVERR_INEXACT 32u /* an index score may not be the exact dot (see csa2_index_score) */
 
 /* sliding-window storage */
 #define CSA2_SWA_BF16 0  /* 576 bf16 values, 1,152 B per token                         */
@@ -172,8 +173,11 @@ csa2_status csa2_kv_append(const csa2_cache *cache, const void *kv, const void *
  *   q_idx: bf16 [batch][n_heads_idx][128]; w: fp32 [batch][n_heads_idx];
  *   q_pos: int64 [batch] query positions; entry s is visible iff
  *          s < floor(q_pos / ratio) ([P5] §2.3.1).
- *   d_h is the dot of the dequantised vectors (exact when the block exponents of
- *   a (query, key) pair span at most 9 binades, as for N(0,1) data);
+ *   d_h is the dot of the dequantised vectors, rounded once to fp32.  That holds
+ *   when the block exponents e_q,j + e_k,j of a (head, key) pair span at most 9
+ *   binades over the blocks whose two scale codes are nonzero (always the case
+ *   for N(0,1)-like data); a visible key whose pair with some head spans more
+ *   raises the INEXACT bit (its scores are then unspecified in the last bits);
  *   score = fma chain over heads in order: acc = fma(w_h, max(d_h, +0), acc).
  * FULL (pool == NULL): scores[b][s] for every visible s (others untouched).
  * POOL (Reindex, [P1] "512개를 고르기 위해 ..."): pool [batch][pool_blocks] int32
@@ -265,9 +269,16 @@ csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t
  *   out: fp32 [batch][n_heads][512] = sum_j p_j c_j; lse: fp32 [batch][n_heads]
  *   = M + log(denominator) (-inf when there is nothing to attend to).
  * n_heads: a multiple of 16, 16..128.  k: 1..2048.
+ * Batch invariance ([P5] §3.3): a row's result is bit-identical whatever the
+ *   batch it is computed in.  Its 32-entry chunks (the k selected entries, then
+ *   the window) are dealt to S = min(8, chunks) segments, S a function of k
+ *   alone; each segment runs its own online softmax and the row merges the S
+ *   partials in segment order.  Only the number of CTAs sharing a row follows
+ *   the batch and the GPU's SM count.
  * ws: device workspace of csa2_attn_workspace_size() bytes, 16-byte aligned:
- *   the partial (O, m, l) of each split of a row, written and read within the
- *   call; calls that may run concurrently need separate workspaces.
+ *   the partial (O, m, l) of each segment of a row (S x 131 KB per row and
+ *   64-head block), written and read within the call; calls that may run
+ *   concurrently need separate workspaces.
  * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
  */
 size_t csa2_attn_workspace_size(int32_t batch, int32_t n_heads, int32_t k);
@@ -288,6 +299,10 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
  *   w fp32 [Q][n_heads_idx]; q bf16 [Q][n_heads][576];
  *   idx_out int32 [Q][k]; out fp32 [Q][n_heads][512]; lse fp32 [Q][n_heads].
  * ws: device workspace of csa2_prefill_workspace_size() bytes.
+ * Each query's attention is one pass over its entries (one segment), so its
+ * bits do not depend on the chunk's size either; they may differ in the last
+ * bits from a decode step at the same position (csa2_sparse_attn_decode merges
+ * S segments), within the attention tolerance.
  * Ratio-1 caches return CSA2_ERR_UNSUPPORTED.
  */
 size_t csa2_prefill_workspace_size(int32_t Q, int32_t capacity, int32_t n_heads_idx,

@@ -256,6 +256,16 @@ void orc_encode_entry(const float *v, const float *ik, const float *cs, uint8_t 
   for (int b = 0; b < ORC_DI / 32; ++b) orc_mxfp4_quant32(ik + 32 * b, idx_codes + 16 * b, idx_scales + b);
 }
 
+/* The indexer-key records alone of n entries (the idx planes of
+ * orc_encode_entry, entry by entry): ik [n][128] -> idx_codes [n][64],
+ * idx_scales [n][4].  Entries are independent, so rows run in parallel. */
+void orc_encode_keys(int64_t n, const float *ik, uint8_t *idx_codes, uint8_t *idx_scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t e = 0; e < n; ++e)
+    for (int b = 0; b < ORC_DI / 32; ++b)
+      orc_mxfp4_quant32(ik + e * ORC_DI + 32 * b, idx_codes + e * 64 + 16 * b, idx_scales + e * 4 + b);
+}
+
 /* One sliding-window slot from a token vector v[576] (rope dims not yet
  * rotated): rotate, then store 8-bit (MXFP8: 576 codes + 18 scales) or bf16. */
 void orc_encode_swa(const float *v, const float *cs, int swa_mxfp8, uint8_t *codes /*576 or 1152 B*/,

@@ -92,6 +92,7 @@ def _declare(L):
         "orc_rope_apply": (None, [vp, vp]),
         "orc_encode_entry": (None, [vp] * 9),
         "orc_encode_swa": (None, [vp, vp, i32, vp, vp]),
+        "orc_encode_keys": (None, [i64, vp, vp, vp]),
         "orc_compress": (None, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "orc_quant_q_index": (None, [i32, vp, vp, vp]),
         "orc_index_score_rows": (i32, [i64, vp, vp, vp, i32, vp, vp, vp]),
@@ -256,6 +257,27 @@ def encode_entry(v576, ik128, cs):
     out = [np.zeros(n, np.uint8) for n in (256, 32, 32, 4, 64, 4)]
     lib().orc_encode_entry(_p(v), _p(ik), _p(_f32(cs)), *[_p(o) for o in out])
     return out
+
+
+class KeyCache:
+    """Indexer-key records only (what the index score reads): idx_codes [n,64],
+    idx_scales [n,4] of n consecutive entries."""
+
+    def __init__(self, n: int):
+        self.idx_codes = np.zeros((n, 64), np.uint8)
+        self.idx_scales = np.zeros((n, 4), np.uint8)
+
+
+def encode_keys(cache, start: int, ik):
+    """MXFP4 records of the indexer keys ik [n,128] into entries start.. of a
+    KeyCache or Cache (the idx planes of encode_entry, [P5] §2.3.4)."""
+    ik = _f32(ik)
+    n = ik.shape[0]
+    codes = np.zeros((n, 64), np.uint8)
+    scales = np.zeros((n, 4), np.uint8)
+    lib().orc_encode_keys(n, _p(ik), _p(codes), _p(scales))
+    cache.idx_codes[start:start + n] = codes
+    cache.idx_scales[start:start + n] = scales
 
 
 def encode_swa(v576, cs, swa_dtype):

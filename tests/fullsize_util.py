@@ -1,10 +1,11 @@
 """Helpers for the parity tests at the workloads' full sizes.
 
 The CUDA side builds its caches through the C ABI in the same chunking as
-bench.py.  The oracle never sees a full cache: for every check it encodes, from
-the same seeded rows, only the entries that check needs (a "compact" oracle
-cache whose slot j holds position positions[j]), so no oracle input comes from
-the CUDA path and the oracle's work stays small at 64 K - 1 M contexts.
+bench.py.  The oracle encodes, from the same seeded rows, the indexer keys of
+every visible position of a checked sequence (the score's only cache input)
+and the latent records only where a check needs them (a "compact" oracle cache
+whose slot j holds position positions[j]), so no oracle input comes from the
+CUDA path.
 """
 import numpy as np
 import torch
@@ -98,21 +99,11 @@ def assert_entries_equal(c, seq, comp):
                               f"{comp.positions[bad[:3, 0]].tolist()}"
 
 
-def topk_ref(scores, k, positions=None):
-    """Exact top-k of fp32 scores by (score desc, position asc), ascending, -1 padded
-    (the selection rule; -0 == +0)."""
-    s = np.asarray(scores, np.float32).astype(np.float64)
-    pos = np.arange(s.shape[0]) if positions is None else np.asarray(positions, np.int64)
-    order = np.lexsort((pos, -s))[:k]
-    out = np.sort(pos[order])
-    return np.concatenate([out, -np.ones(k - out.shape[0], np.int64)]).astype(np.int32)
-
-
-def pool_ref(scores, T, max_blocks=2048, bs=8):
-    s = np.asarray(scores[:T], np.float32)
-    nb = (T + bs - 1) // bs
-    pad = np.full(nb * bs, -np.inf, np.float32)
-    pad[:T] = s
-    bmax = pad.reshape(nb, bs).max(axis=1)
-    ids = topk_ref(bmax, max_blocks)
-    return ids, min(nb, max_blocks)
+def oracle_keys(orc, W, seq, T):
+    """The oracle's indexer-key records of positions 0..T-1 of one sequence,
+    encoded from the workload's seeded key rows chunk by chunk."""
+    kc = orc.KeyCache(T)
+    for t0 in range(0, T, CHUNK):
+        n = min(CHUNK, T - t0)
+        orc.encode_keys(kc, t0, W.ik(seq, t0, n, device=W.device).cpu().numpy())
+    return kc

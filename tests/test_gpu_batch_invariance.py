@@ -1,0 +1,69 @@
+"""Batch invariance of the decode step ([P5] §3.3 "Batch Invariance": a token's
+output must be bitwise the same whatever the batch it is computed in).
+
+One sequence's decode step -- index scores, top-k and candidate pool, sparse
+attention -- is run inside batches of 1, 32, 76 and 160 sequences, which spread
+a row over 8, 4, 2 and 1 CTAs on a 152-SM GPU.  Its scores, selection, output
+and lse must be bit-identical across the batches.
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_sparse_gb300 import csa2
+from fp4_compressed_sparse_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+SEED, T, H, H_I, K = 91, 1200, 64, 64, 512
+TARGET = 5  # the sequence followed through every batch
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from fp4_compressed_sparse_gb300 import build_lib
+    build_lib.build()
+    csa2.load()
+
+
+def _step(batch, row):
+    """Sequence TARGET at row `row` of a batch whose other rows are other sequences."""
+    seqs = [TARGET if b == row else 1000 + b for b in range(batch)]
+    cap = T + 8
+    c = csa2.Cache(batch, cap, ratio=1)
+    rope = csa2.rope_table(1e4, cap + 8)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv = torch.stack([wl.token_rows(SEED, wl.S_KV, s, 0, T, 576, device="cuda") for s in seqs])
+    ik = torch.stack([wl.token_rows(SEED, wl.S_IK, s, 0, T, 128, device="cuda") for s in seqs])
+    csa2.kv_append(c, kv, ik, rope, err=err)
+    q_idx = torch.stack([wl.normal((H_I, 128), SEED, wl.S_QIDX, s, device="cuda") for s in seqs]).to(torch.bfloat16)
+    w = torch.stack([wl.uniform((H_I,), SEED, wl.S_W, s, device="cuda") for s in seqs])
+    q = torch.stack([wl.normal((H, 576), SEED, wl.S_Q, s, device="cuda") for s in seqs]).to(torch.bfloat16)
+    sink = wl.normal((H,), SEED, wl.S_SINK, 0, device="cuda")
+    q_pos = torch.full((batch,), T - 1, dtype=torch.int64, device="cuda")
+    scores = torch.empty((batch, cap), device="cuda")
+    aux = csa2.score_aux(batch, cap)
+    idx = torch.empty((batch, K), dtype=torch.int32, device="cuda")
+    pool = torch.empty((batch, 64), dtype=torch.int32, device="cuda")
+    pcnt = torch.empty((batch,), dtype=torch.int32, device="cuda")
+    out = torch.empty((batch, H, 512), device="cuda")
+    lse = torch.empty((batch, H), device="cuda")
+    csa2.index_score(c, q_idx, w, q_pos, scores, err=err, aux=aux)
+    csa2.topk(scores, 1, q_pos, K, idx, csa2.topk_workspace(batch, cap, K, 64), pool_out=pool, pool_count=pcnt,
+              err=err, aux=aux)
+    csa2.sparse_attn_decode(c, q, q_pos, idx, out, lse, csa2.attn_workspace(batch, H, K), 1 / 24.0, sink=sink,
+                            err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return [t[row].cpu() for t in (scores[:, :T - 1], idx, pool, out, lse)]
+
+
+def test_decode_step_is_batch_invariant():
+    ref = _step(1, 0)
+    assert (ref[1] >= 0).all()
+    for batch, row in ((32, 17), (76, 40), (160, 159)):
+        got = _step(batch, row)
+        for name, a, b in zip(("scores", "idx", "pool", "out", "lse"), ref, got):
+            assert torch.equal(a.view(torch.int32) if a.is_floating_point() else a,
+                               b.view(torch.int32) if b.is_floating_point() else b), \
+                f"batch {batch}: {name} differs from batch 1"

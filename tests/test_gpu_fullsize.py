@@ -1,15 +1,13 @@
 """Parity at the workloads' full sizes, in the launch shapes bench.py times.
 
-The oracle cannot score 32 x 65,536 (or 8 x 1,048,576) positions in seconds, so
-each test checks sampled outputs the oracle computes one by one, and properties
-that hold at any size:
-  - cache records (codes, scales) bit-exact at sampled positions and at every
-    selected position;
-  - scores bit-exact at sampled positions and at every selected position;
-  - the top-k list and the candidate pool equal the exact selection over the
-    whole score row (a host sort of the row the GPU scored);
-  - attention outputs within 2e-3 normwise of the oracle's fp64 attention over
-    the selected entries and the window.
+Every index score of the checked rows is compared with the oracle: the oracle
+encodes the indexer key of every visible position from the same seeded rows
+(the MXFP4 key records alone, which is all the score reads), scores the whole
+row, and its own top-k and candidate pool are the references for the GPU's
+selection.  The oracle never reads a GPU result.  Latent records are checked
+at sampled positions and at every selected one, and attention outputs within
+2e-3 normwise of the oracle's fp64 attention over the oracle-selected entries
+and the window.
 """
 import numpy as np
 import pytest
@@ -18,7 +16,7 @@ import torch
 from fp4_compressed_sparse_gb300 import csa2
 from fp4_compressed_sparse_gb300 import workloads as wl
 from gpu_util import attn_close, u16
-from fullsize_util import (Compact, assert_entries_equal, build_gpu_r1, pool_ref, topk_ref,
+from fullsize_util import (CHUNK, Compact, assert_entries_equal, build_gpu_r1, oracle_keys,
                            window_records)
 
 pytestmark = pytest.mark.gpu
@@ -32,23 +30,31 @@ def _sample(rng, T, extra):
 
 
 def _check_full_layer(orc, W, c, seq, q_pos, q_idx, w, q, scores, idx, pool, pool_cnt, out, lse, rng):
+    """Whole-row check of one Full layer of sequence `seq`: key records and scores
+    of every visible position bit-exact, top-k and pool equal to the oracle's
+    selection over its own scores, attention within 2e-3."""
     T = q_pos  # ratio 1: entries 0 .. q_pos-1 are visible
-    g_scores = scores[seq, :T].cpu().numpy()
-    g_idx = idx[seq].cpu().numpy()
-    comp = Compact(orc, W, seq, _sample(rng, T, g_idx))
-    assert_entries_equal(c, seq, comp)
-    ref, flags = orc.index_scores(comp.cache, u16(q_idx[seq]), w[seq].cpu().numpy(),
-                                  n_vis=comp.positions.shape[0])
+    kc = oracle_keys(orc, W, seq, T)
+    ic, isc = c.idx_entries()
+    assert np.array_equal(ic[seq, :T].cpu().numpy(), kc.idx_codes), f"seq {seq}: key codes"
+    assert np.array_equal(isc[seq, :T].cpu().numpy(), kc.idx_scales), f"seq {seq}: key scales"
+    ref, flags = orc.index_scores(kc, u16(q_idx[seq]), w[seq].cpu().numpy(), n_vis=T)
     assert flags == 0
-    got = g_scores[comp.positions]
-    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), \
-        f"seq {seq}: {int(np.sum(got != ref))} sampled scores differ"
-    assert g_idx.tolist() == topk_ref(g_scores, g_idx.shape[0]).tolist(), f"seq {seq}: top-k"
+    got = scores[seq, :T].cpu().numpy()
+    bad = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+    assert bad.size == 0, f"seq {seq}: {bad.size} of {T} scores differ, first at {bad[:4].tolist()}"
+    k = idx.shape[1]
+    r_idx = orc.topk(ref, k)
+    g_idx = idx[seq].cpu().numpy()
+    assert g_idx.tolist() == r_idx.tolist(), f"seq {seq}: top-k"
     if pool is not None:
-        pids, cnt = pool_ref(g_scores, T, pool.shape[1])
-        assert int(pool_cnt[seq].item()) == cnt and pool[seq].cpu().numpy().tolist() == pids.tolist()
+        pids, cnt = orc.pool(ref, T, 8, pool.shape[1])
+        assert int(pool_cnt[seq].item()) == cnt, f"seq {seq}: pool count"
+        assert pool[seq].cpu().numpy().tolist() == pids.tolist(), f"seq {seq}: pool"
+    comp = Compact(orc, W, seq, _sample(rng, T, r_idx))
+    assert_entries_equal(c, seq, comp)
     wc, wsc = window_records(orc, W, seq, q_pos, q_pos + 1)
-    ro, rl = orc.sparse_attn(comp.cache, u16(q[seq]), comp.remap(g_idx), q_pos, W.sm_scale,
+    ro, rl = orc.sparse_attn(comp.cache, u16(q[seq]), comp.remap(r_idx), q_pos, W.sm_scale,
                              swa_codes=wc, swa_scales=wsc)
     attn_close(out[seq].cpu().numpy(), lse[seq].cpu().numpy(), ro, rl)
 
@@ -166,7 +172,9 @@ def test_stack_b8_t1048576_one_step(orc):
 def test_prefill_q8192_prior131072(orc):
     """Encoder-style chunked prefill: 8,192 query tokens against 131,072 prior tokens
     packed 2 per entry (65,536 entries), 64 indexer heads, top-512, 64 heads, MXFP8
-    window.  Queries 0, 1, 4095 and 8191 are checked against a full oracle scan."""
+    window.  The cache is compared whole; the first and last query of every score
+    block and of every 512-query span (49 queries) are checked against full
+    oracle scans."""
     W = wl.prefill_chunk(device="cuda")
     cap = (W.prior + W.chunk) // 2 + 8
     c = csa2.Cache(1, cap, ratio=2, swa_dtype=W.swa_dtype)
@@ -217,7 +225,17 @@ def test_prefill_q8192_prior131072(orc):
     for name, g in (("lat_codes", c.lat_codes), ("lat_scales", c.lat_scales), ("rope_codes", c.rope_codes),
                     ("rope_scales", c.rope_scales), ("idx_codes", ic), ("idx_scales", isc)):
         assert np.array_equal(g[0, :n_entries].cpu().numpy(), getattr(o, name)), f"prefill cache {name}"
-    for i in (0, 1, 4095, 8191):
+    # the chunk is scored in blocks of queries whose fp32 score rows fill 256 MB:
+    # the first and last query of every such block, of every 512-query span, and
+    # the middle of the chunk
+    qb = max(1, min(Q, 4096, (256 << 20) // (cap * 4)))
+    qs = {1, Q // 2 - 1, Q // 2}
+    for span in (qb, 512):
+        for q0 in range(0, Q, span):
+            qs.update((q0, min(Q, q0 + span) - 1))
+    qs = sorted(qs)
+    assert len(qs) >= 16
+    for i in qs:
         t = W.prior + i
         sc, flags = orc.index_scores(o, u16(q_idx[i]), w[i].cpu().numpy(), n_vis=t // 2)
         assert flags == 0

@@ -266,12 +266,12 @@ def test_topk_nan_score_is_reported(orc):
 
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("B,T,H,k,swa_dtype,use_sink", [
-    (3, 700, 64, 64, csa2.SWA_MXFP8, False),
+    (3, 700, 64, 64, csa2.SWA_MXFP8, False),   # 6 segments, one per CTA
     (3, 700, 64, 64, csa2.SWA_BF16, True),
-    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # two splits per row
-    (80, 200, 64, 48, csa2.SWA_BF16, False),   # enough rows: one split, two chunks, no merge
+    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # 6 segments over 4 CTAs per row
+    (80, 200, 64, 48, csa2.SWA_BF16, False),   # one CTA per row computes all 6 segments
     (1, 90, 32, 128, csa2.SWA_MXFP8, False),   # window shorter than 128, idx padded with -1
-    (3, 1500, 128, 1024, csa2.SWA_BF16, True), # two head blocks, 8-CTA clusters, 2 chunks per split
+    (3, 1500, 128, 1024, csa2.SWA_BF16, True), # two head blocks, 8-CTA clusters, 5 chunks per segment
     (2, 300, 48, 200, csa2.SWA_MXFP8, False),  # a partial head block
 ])
 def test_sparse_attn_decode(orc, B, T, H, k, swa_dtype, use_sink):

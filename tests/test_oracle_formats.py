@@ -205,3 +205,38 @@ def test_mxfp8_identity_and_scale(orc):
     x2 = x * np.float32(2.0 ** -6)
     codes2, sc2 = orc.mxfp8_quant32(x2)
     assert sc2 == 121 and list(codes2) == list(codes)
+
+
+def test_encode_swa_matches_torch_route(orc):
+    """The window slot ([P1] "890 bytes/token": window KV kept in 8 bits; reading:
+    MXFP8, one E8M0 exponent per 32 values, e = floor(log2 amax) - 8) rebuilt by an
+    independent route: the row's RoPE dims rotated, each 32-value block scaled by
+    2^-e and cast by torch's float8_e4m3fn (clamped to +-448, the satfinite rule),
+    the exponent read with numpy's frexp; bf16 slots by torch's bfloat16 cast."""
+    rng = np.random.default_rng(31)
+    for trial in range(40):
+        v = (rng.standard_normal(576) * 2.0 ** rng.integers(-12, 12)).astype(np.float32)
+        if trial % 5 == 0:
+            v[rng.integers(0, 576, 40)] = 0.0
+        if trial == 3:
+            v[64:96] = 0.0  # an all-zero block: scale code 0, zero codes
+        pos = int(rng.integers(0, 200000))
+        cs = orc.rope_cs(1e4, pos)
+        rot = v.copy()
+        rot[512:] = orc.rope_apply(v[512:], cs)
+        codes, scales = orc.encode_swa(v, cs, 1)
+        for b in range(18):
+            blk = rot[32 * b:32 * b + 32].astype(np.float64)
+            amax = np.max(np.abs(blk))
+            if amax == 0.0:
+                assert scales[b] == 0 and not codes[32 * b:32 * b + 32].any()
+                continue
+            e = int(np.frexp(amax)[1]) - 1 - 8
+            e = max(-127, min(127, e))
+            assert scales[b] == e + 127, (trial, b)
+            scaled = np.clip(np.ldexp(blk, -e), -448.0, 448.0)
+            ref = torch.from_numpy(scaled.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(codes[32 * b:32 * b + 32], ref), (trial, b)
+        hb, _ = orc.encode_swa(v, cs, 0)
+        ref_bf16 = torch.from_numpy(rot).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(hb.view(np.uint16), ref_bf16), trial

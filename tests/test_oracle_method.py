@@ -109,30 +109,45 @@ def test_accounting_matches_pages(orc):
 
 
 def test_layer_roles_reproduce_890(orc):
+    """Role masks over the layer table: a layer with compression ratio 0 keeps
+    only its window; among the others the KV-source ids hold a global cache
+    (Full), the further index-source ids only re-score (Reindex) and the rest
+    reuse.  The global bytes per token sum the Full layers' records divided by
+    their ratios."""
     g = _gold("layer_roles.txt")
-    L = int(g["num_hidden_layers"][0][0])
-    kv = {int(x) for x in g["kv_source_layer_ids"][0]}
-    ix = {int(x) for x in g["index_source_layer_ids"][0]}
-    cr = []
-    for run in g["compress_ratios_runs"][0]:
-        v, n = run.split("x")
-        cr += [int(v)] * int(n)
-    kinds = {}
-    total = 0.0
+    n_layers = int(g["num_hidden_layers"][0][0])
+    ratios = np.concatenate([np.full(int(n), int(v)) for v, n in
+                             (run.split("x") for run in g["compress_ratios_runs"][0])])
+    ids = np.arange(n_layers)
+    compressed = ratios[:n_layers] > 0
+    full = compressed & np.isin(ids, [int(x) for x in g["kv_source_layer_ids"][0]])
+    reindex = compressed & ~full & np.isin(ids, [int(x) for x in g["index_source_layer_ids"][0]])
+    reuse = compressed & ~full & ~reindex
     c = orc.Cache(4)
-    rec = (c.lat_codes.shape[1] + c.lat_scales.shape[1] + c.idx_codes.shape[1]
-           + c.idx_scales.shape[1])
-    for i in range(L):
-        k = ("swa-only" if cr[i] == 0 else "full" if i in kv else "reindex" if i in ix
-             else "reuse")
-        kinds.setdefault(k, []).append(i)
-        if k == "full":
-            total += rec / cr[i]
-    exp = {e[0]: e[1] for e in g["expect"]}
-    for k in ("swa-only", "full", "reindex", "reuse"):
-        assert len(kinds[k]) == int(exp[k])
-    assert len(cr) == int(exp["compress_ratios_entries"])
-    assert total == float(exp["global_bytes_per_token"])
+    record = sum(a.shape[1] for a in (c.lat_codes, c.lat_scales, c.idx_codes, c.idx_scales))
+    per_token = float(np.sum(record / ratios[:n_layers][full]))
+    want = {e[0]: e[1] for e in g["expect"]}
+    counts = {"swa-only": int(np.sum(~compressed)), "full": int(full.sum()), "reindex": int(reindex.sum()),
+              "reuse": int(reuse.sum())}
+    assert counts == {k: int(want[k]) for k in counts}
+    assert ratios.shape[0] == int(want["compress_ratios_entries"])
+    assert per_token == float(want["global_bytes_per_token"])
+
+
+def test_encode_keys_equals_entry_records(orc):
+    """The key-only encoder gives the indexer planes of the full entry encoder."""
+    rng = np.random.default_rng(41)
+    n = 300
+    kv = rng.standard_normal((n, 576)).astype(np.float32)
+    ik = (rng.standard_normal((n, 128)) * 2.0 ** rng.integers(-20, 20, (n, 1))).astype(np.float32)
+    ik[5] = 0.0
+    full = orc.Cache(n)
+    orc.append_r1(full, kv, ik, 1e4)
+    keys = orc.KeyCache(n + 7)
+    orc.encode_keys(keys, 7, ik)
+    assert np.array_equal(keys.idx_codes[7:], full.idx_codes[:n])
+    assert np.array_equal(keys.idx_scales[7:], full.idx_scales[:n])
+    assert not keys.idx_codes[:7].any()
 
 
 # ------------------------------------------------------------ RoPE (C9)
