@@ -49,7 +49,7 @@ constexpr int kQS = kDqk + 8;     // fp16 row stride of Q and of the entry tiles
 constexpr int kPS = kE + 8;       // fp16 row stride of P (80 B)
 constexpr int kSS = kE + 8;       // fp32 row stride of the partial logits (conflict-free float2 stores)
 constexpr int kProdThreads = 128; // four producer warps
-constexpr int kHeadBlock = 64;    // heads per CTA at most
+constexpr int kHeadBlock = 64;    // heads per CTA at most (16 or 32 when small batches need more CTAs)
 constexpr uint32_t kWaitIters = 200;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -112,7 +112,8 @@ __device__ __forceinline__ uint32_t h2_splat(float v) {
   __half2 h = __float2half2_rn(v);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-constexpr int kMaxSeg = 8;  // segments of a row; also the most CTAs per row (one portable cluster)
+constexpr int kMaxSeg = 8;  // segments of a row at most; also the most CTAs per row (one portable cluster)
+constexpr int kSegments = 4;  // segments of a decode row (fewer when its entry list has fewer chunks)
 
 // every non-exited thread of the cluster
 __device__ __forceinline__ void cluster_sync() {
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
   extern __shared__ __align__(128) uint8_t smem_raw[];
   AttnSmem<HP> &sm = *reinterpret_cast<AttnSmem<HP> *>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cta = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kHeadBlock;
+  const int cta = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * HP;
   const int nh = min(HP, a.heads - hbase);
   const int seq = a.cache_seq < 0 ? row : a.cache_seq;
   const int kpad = (a.k + kE - 1) / kE * kE;
@@ -688,16 +689,26 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     }
 }
 
-int head_blocks(int heads) { return (heads + kHeadBlock - 1) / kHeadBlock; }
+int head_blocks(int heads, int hp) { return (heads + hp - 1) / hp; }
 
-// CTAs per row (one cluster): enough to fill the SMs once (one CTA per SM),
-// at most one per segment.  Only the speed depends on this choice.
-int choose_ctas(int rows, int heads, int n_seg) {
-  const int ctas = rows * head_blocks(heads);
-  int g = device_sm_count() / ctas;
-  if (g > n_seg) g = n_seg;
-  if (g < 1) g = 1;
-  return g;
+// Launch shape: G CTAs per (row, head block), one cluster, and hp heads per CTA.
+// The segments of a row are fixed; G only spreads them, and a head's arithmetic
+// does not depend on the head block it is in, so neither choice changes a bit.
+// G grows first (up to one CTA per segment) while the grid fits one wave of one
+// CTA per SM; then, for small batches, the heads are split into blocks of 32 or
+// 16 (each CTA then dequantises the row's entries for fewer heads).
+struct AttnShape {
+  int n_cta, hp;
+};
+AttnShape choose_shape(int rows, int heads, int n_seg) {
+  const int sms = device_sm_count();
+  AttnShape sh{1, heads <= 16 ? 16 : heads <= 32 ? 32 : kHeadBlock};
+  const int ctas = rows * head_blocks(heads, sh.hp);
+  sh.n_cta = sms / ctas;
+  if (sh.n_cta > n_seg) sh.n_cta = n_seg;
+  if (sh.n_cta < 1) sh.n_cta = 1;
+  while (sh.hp > 16 && sh.n_cta == n_seg && rows * sh.n_cta * head_blocks(heads, sh.hp / 2) <= sms) sh.hp /= 2;
+  return sh;
 }
 
 template <int HP>
@@ -706,13 +717,13 @@ cudaError_t launch_hp(const AttnArgs &a, int n_cta, int n_seg, float *part, cuda
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_attn<HP>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_cta, a.rows, head_blocks(a.heads));
+  cfg.gridDim = dim3(n_cta, a.rows, head_blocks(a.heads, HP));
   cfg.blockDim = dim3(HP * 4 + kProdThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = n_cta;  // the row's CTAs: one cluster
+  attr[0].val.clusterDim.x = n_cta;  // the row's CTAs of one head block: one cluster
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -725,33 +736,33 @@ cudaError_t launch_hp(const AttnArgs &a, int n_cta, int n_seg, float *part, cuda
 }  // namespace
 
 // Segments of a decode row's entry list: fixed by k and the window alone (never
-// by the batch), at most one portable cluster of CTAs' worth (8), at least one
-// chunk each.
+// by the batch), four, or fewer when the list has fewer 32-entry chunks.
 int attn_segments(int k) {
   const int chunks = ((k + kE - 1) / kE * kE + kWin) / kE;
-  return chunks < kMaxSeg ? chunks : kMaxSeg;
+  return chunks < kSegments ? chunks : kSegments;
 }
 
-// Workspace: the partial (O, m, l) of every segment of every (row, head block)
-// when a row has more than one segment.
+// Workspace: the partial (O, m, l) of every segment of every (row, head) when a
+// row has more than one segment (sized for 64-head blocks, the largest: a
+// smaller block never needs more).
 size_t attn_workspace_bytes(int rows, int heads, int n_seg) {
   if (n_seg <= 1) return 256;
-  return static_cast<size_t>(rows) * head_blocks(heads) * n_seg * part_floats<kHeadBlock>() * sizeof(float) + 256;
+  return static_cast<size_t>(rows) * head_blocks(heads, kHeadBlock) * n_seg * part_floats<kHeadBlock>() *
+             sizeof(float) +
+         256;
 }
 
 cudaError_t launch_attn(const AttnArgs &a0, int n_seg, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (a0.rows <= 0) return cudaSuccess;
   if (n_seg < 1 || n_seg > kMaxSeg) return cudaErrorInvalidValue;
-  const int n_cta = choose_ctas(a0.rows, a0.heads, n_seg);
-  if (n_seg > 1 &&
-      (ws == nullptr || ws_bytes < static_cast<size_t>(a0.rows) * head_blocks(a0.heads) * n_seg *
-                                       part_floats<kHeadBlock>() * sizeof(float) ||
-       reinterpret_cast<uintptr_t>(ws) % 16 != 0))
+  const AttnShape sh = choose_shape(a0.rows, a0.heads, n_seg);
+  if (n_seg > 1 && (ws == nullptr || ws_bytes + 256 < attn_workspace_bytes(a0.rows, a0.heads, n_seg) ||
+                    reinterpret_cast<uintptr_t>(ws) % 16 != 0))
     return cudaErrorInvalidValue;
   float *part = static_cast<float *>(ws);
-  if (a0.heads <= 16) return launch_hp<16>(a0, n_cta, n_seg, part, st);
-  if (a0.heads <= 32) return launch_hp<32>(a0, n_cta, n_seg, part, st);
-  return launch_hp<64>(a0, n_cta, n_seg, part, st);
+  if (sh.hp == 16) return launch_hp<16>(a0, sh.n_cta, n_seg, part, st);
+  if (sh.hp == 32) return launch_hp<32>(a0, sh.n_cta, n_seg, part, st);
+  return launch_hp<64>(a0, sh.n_cta, n_seg, part, st);
 }
 
 }  // namespace csa2

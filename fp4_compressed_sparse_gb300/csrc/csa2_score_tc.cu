@@ -19,10 +19,11 @@
 // an integer multiple of its smallest block's unit below 2^(15 + span), where
 // span = max - min of the pair's block exponents e_q,j + e_k,j.  With span <= 9
 // it fits the 24-bit fp32 significand, so the tensor core's fp32 result is the
-// exact dot, rounded once (the value the oracle defines).  The MMA-issuing warps
-// check every tile against that bound from the scale bytes in shared memory
-// (blocks whose scale code is 0 -- all-zero blocks -- take no part) and raise
-// CSA2_DEVERR_INEXACT if some (head, visible key) pair exceeds it.
+// exact dot, rounded once (the value the oracle defines).  The epilogue checks
+// every visible key against that bound (blocks whose scale code is 0 -- all-zero
+// blocks -- take no part) and raises CSA2_DEVERR_INEXACT if some (head, key)
+// pair exceeds it: the key's own code spread plus the row's widest query spread
+// bounds all its pairs, and only when that sum exceeds 9 is each head checked.
 //
 // Persistent CTA per SM, warp-specialised (tile j of a CTA, counted over the
 // tiles of its item range, goes to producer j % 2, issuer j % 2 and
@@ -35,10 +36,9 @@
 //               blocks with zero-filling cp.async, four tiles in flight per warp.
 //               Warp 0 also loads each row's query record into one of two B
 //               slots.
-//   warps 2, 3  MMA issuers: lane 0 copies the scale factors to TMEM
-//               (tcgen05.cp), issues the two MMAs and the commits that free the
-//               stage and hand the accumulator over; the whole warp checks the
-//               exactness bound on the tile's scale bytes.
+//   warps 2, 3  MMA issuers (one thread each): scale factors to TMEM
+//               (tcgen05.cp), the two MMAs, commits that release the stage and
+//               hand the accumulator over.
 //   the rest    epilogue: four warps (one per 32-lane TMEM quarter) per
 //               accumulator, four accumulators (two when 4 x N columns do not
 //               fit TMEM beside the scale factors).  A thread owns one key: it
@@ -47,6 +47,9 @@
 //               score keys (and, in FULL mode, the 8-position block maxima) in
 //               shared memory and adds them to the row's global histogram once
 //               the CTA is done with the row, so top-k needs no pass of its own.
+//               Each epilogue thread also reads its key's four block scale
+//               codes from the scale-factor columns the MMA used (TMEM) and
+//               checks the exactness bound for its key.
 // Every mbarrier wait is bounded; a wait that runs out raises
 // CSA2_DEVERR_TIMEOUT, sets a CTA abort flag and the CTA drains and exits.
 #include "csa2_internal.cuh"
@@ -439,102 +442,48 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       for (; npend > 0; --npend) hand_over((jlast - (npend - 1) * nprod) % kStages);
     }
     if (lane == 0) sm.issued[pw] = mine;
-  } else if (warp >= kProducers && warp < kProducers + kIssuers) {
-    // ------------------------------------------------------------ MMA issuers (one warp each)
+  } else if (warp >= kProducers && warp < kProducers + kIssuers && lane == 0) {
+    // ------------------------------------------------------------ MMA issuers (one thread each)
     // issuer `who` takes the CTA's tiles j with j % kIssuers == who (accumulators
     // and stages who, who + kIssuers, ...); each keeps its own copy of the row's
-    // query scale factors in TMEM.  Lane 0 issues every tcgen05 op; the whole
-    // warp checks the exactness bound.
+    // query scale factors in TMEM
     const int who = warp - kProducers;
     int bchanges = 0, jrow = 0;
     const uint32_t id0 = tc::idesc_mxf4(128, np, 0, 0), id1 = tc::idesc_mxf4(128, np, 2, 2);
-    bool dead = false, flagged = false;
+    bool dead = false;
     for (int row = row0; row <= row_last && !dead; ++row) {
       int t0, t1;
       row_span(row, t0, t1);
       if (t1 <= t0) continue;
       const int bs = bchanges & 1;
-      if (!wait_all(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
+      if (!wait1(sm, &sm.bfull[bs], (bchanges >> 1) & 1, a.s.err)) {
         dead = true;
         break;
       }
       ++bchanges;
+      tc::tc_fence_after();
       const uint32_t sfb = tmem + col_sfb + 8 * (2 * who + bs);
-      if (lane == 0) {
-        tc::tc_fence_after();
-        tc::tmem_cp_32x128b_x4(sfb, tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
-      }
-      // widest block-exponent span over the row's query heads (padding heads are zero)
-      const uint8_t *qsf = sm.bslot[bs] + np * 64;
-      int qspan = 0;
-      for (int h = lane; h < np; h += 32) qspan = max(qspan, code_span(sfb_word(qsf, h)));
-      qspan = __reduce_max_sync(0xffffffffu, qspan);
-      const int64_t nslots = row_slots(a, row);
+      tc::tmem_cp_32x128b_x4(sfb, tc::smem_desc_noswizzle(tc::smem_addr(sm.bslot[bs] + np * 64), 128, 128));
       for (int tile = first_own(t0, jrow, kIssuers, who); tile < t1; tile += kIssuers) {
         const int j = jrow + (tile - t0), s = j % kStages, acc = j % kAcc;
-        if (!wait_all(sm, &sm.full[s], (j / kStages) & 1, a.s.err)) {
+        if (!wait1(sm, &sm.full[s], (j / kStages) & 1, a.s.err) ||
+            (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err))) {
           dead = true;
           break;
         }
-        // this lane's keys m = lane + 32 i: word i holds their four block scale codes
-        const uint4 kw = *reinterpret_cast<const uint4 *>(sm.stage[s] + kIdxTileCodeBytes + 16 * lane);
-        const uint32_t kwi[4] = {kw.x, kw.y, kw.z, kw.w};
-        int kspan = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (pool_mode || static_cast<int64_t>(tile) * kIdxTile + lane + 32 * i < nslots)
-            kspan = max(kspan, code_span(kwi[i]));
-        kspan = __reduce_max_sync(0xffffffffu, kspan);  // the scale bytes are in registers: the stage may go
-        if (lane == 0) {
-          if (j >= kAcc && !wait1(sm, &sm.tempty[acc], ((j / kAcc) - 1) & 1, a.s.err)) {
-            dead = true;
-          } else {
-            tc::tc_fence_after();
-            const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
-            tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc,
-                                   tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
-            const uint32_t d = tmem + acc * np;
-            tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
-                         tmem + col_sfa + 8 * acc, sfb, 0);
-            tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
-                         tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb,
-                         1);
-            tc::mma_commit(&sm.empty[s]);
-            tc::mma_commit(&sm.tfull[acc]);
-          }
-        }
-        if (__shfl_sync(0xffffffffu, dead ? 1 : 0, 0)) {
-          dead = true;
-          break;
-        }
-        if (!flagged && qspan + kspan > kMaxExactSpan) {
-          // rare: the per-tile bound fails; check every (head, visible key) pair
-          int bad = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + lane + 32 * i;
-            bool valid;
-            if (!pool_mode) {
-              valid = slot < nslots;
-            } else {
-              const int32_t pid = slot < static_cast<int64_t>(a.s.pool_blocks) * a.s.pool_bs
-                                      ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + slot / a.s.pool_bs]
-                                      : -1;
-              const int64_t p = static_cast<int64_t>(pid) * a.s.pool_bs + slot % a.s.pool_bs;
-              valid = pid >= 0 && p < a.s.q_pos[row] / a.s.ratio && p < a.s.cap;
-            }
-            if (!valid || code_span(kwi[i]) + qspan <= kMaxExactSpan) continue;
-#pragma unroll 1
-            for (int h = 0; h < np && !bad; ++h) bad = pair_span(sfb_word(qsf, h), kwi[i]) > kMaxExactSpan;
-          }
-          if (__any_sync(0xffffffffu, bad)) {
-            if (lane == 0) raise_err(a.s.err, CSA2_DEVERR_INEXACT);
-            flagged = true;
-          }
-        }
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_addr(sm.stage[s]), sb = tc::smem_addr(sm.bslot[bs]);
+        tc::tmem_cp_32x128b_x4(tmem + col_sfa + 8 * acc, tc::smem_desc_noswizzle(sa + kIdxTileCodeBytes, 128, 128));
+        const uint32_t d = tmem + acc * np;
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa, 2048, 128), tc::smem_desc_noswizzle(sb, np * 16, 128), id0,
+                     tmem + col_sfa + 8 * acc, sfb, 0);
+        tc::mma_mxf4(d, tc::smem_desc_noswizzle(sa + 4096, 2048, 128),
+                     tc::smem_desc_noswizzle(sb + 2 * np * 16, np * 16, 128), id1, tmem + col_sfa + 8 * acc, sfb, 1);
+        tc::mma_commit(&sm.empty[s]);
+        tc::mma_commit(&sm.tfull[acc]);
       }
       // the row's B slot is free once both issuers' MMAs of the row are done
-      if (!dead && lane == 0) tc::mma_commit(&sm.bempty[bs]);
+      if (!dead) tc::mma_commit(&sm.bempty[bs]);
       jrow += t1 - t0;
     }
   } else if (warp >= kFirstEpiWarp) {
@@ -554,6 +503,8 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       ++bchanges;
       const int64_t row_nslots = row_slots(a, row);
       const int64_t row_T = pool_mode ? a.s.q_pos[row] / a.s.ratio : 0;  // POOL: visible positions
+      const uint8_t *qsf = sm.bslot[bs] + np * 64;  // the row's query scale codes
+      int qspan = -1;                               // the widest, read once the record has landed
       for (int tile = first_own(t0, jrow, kAcc, parity); tile < t1 && !dead; tile += kAcc) {
         const int j = jrow + (tile - t0);
         const int64_t slot = static_cast<int64_t>(tile) * kIdxTile + m;
@@ -571,8 +522,19 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
           dead = true;
         } else {
           tc::tc_fence_after();
+          if (qspan < 0) {
+            qspan = 0;
+            for (int h = lane; h < np; h += 32) qspan = max(qspan, code_span(sfb_word(qsf, h)));
+            qspan = __reduce_max_sync(0xffffffffu, qspan);
+          }
           const float4 *wv = reinterpret_cast<const float4 *>(sm.bslot[bs] + np * 64 + 512);  // head weights
           const uint32_t base = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + parity * np;
+          // the key's block scale codes: the scale-factor columns of this accumulator
+          // hold, in lane 32q + r, the codes of keys r, r + 32, r + 64, r + 96 (one
+          // column each); this thread's key 32 quarter + lane is column `quarter`
+          uint32_t kcodes;
+          tc::tmem_ld_32x32b_x1(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + col_sfa + 8 * parity + quarter,
+                                kcodes);
           // up to kRound columns per round: every load of the round, then one
           // wait; the fma chain runs over the heads in order
           float acc = 0.0f;
@@ -608,6 +570,8 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
               }
             }
           }
+          // kcodes landed with the rounds' waits; keep its uses after them
+          asm volatile("" : "+r"(kcodes));
           bool valid;
           if (!pool_mode) {
             valid = slot < row_nslots;
@@ -617,6 +581,14 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
             if (pid >= 0 && p >= a.s.cap) raise_err(a.s.err, CSA2_DEVERR_INDEX);
           }
           if (valid) a.s.scores[static_cast<size_t>(row) * a.s.stride + slot] = acc;
+          // exactness bound for this key (rarely does it need the per-head check)
+          const int kspan = valid ? code_span(kcodes) : 0;
+          if (__any_sync(0xffffffffu, kspan + qspan > kMaxExactSpan)) {
+            bool bad = false;
+            if (kspan + qspan > kMaxExactSpan)
+              for (int h = 0; h < np && !bad; ++h) bad = pair_span(sfb_word(qsf, h), kcodes) > kMaxExactSpan;
+            if (bad) raise_err(a.s.err, CSA2_DEVERR_INEXACT);
+          }
           if (has_aux) {
             // sideband: score-key histogram; FULL rows also the max of each
             // 8-position block (8 consecutive lanes) and its histogram

@@ -271,13 +271,14 @@ csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t
  * n_heads: a multiple of 16, 16..128.  k: 1..2048.
  * Batch invariance ([P5] §3.3): a row's result is bit-identical whatever the
  *   batch it is computed in.  Its 32-entry chunks (the k selected entries, then
- *   the window) are dealt to S = min(8, chunks) segments, S a function of k
+ *   the window) are dealt to S = min(4, chunks) segments, S a function of k
  *   alone; each segment runs its own online softmax and the row merges the S
- *   partials in segment order.  Only the number of CTAs sharing a row follows
- *   the batch and the GPU's SM count.
+ *   partials in segment order.  Only the launch shape follows the batch and
+ *   the GPU's SM count: how many CTAs share a row's segments, and how many
+ *   heads (64, 32 or 16) a CTA takes.
  * ws: device workspace of csa2_attn_workspace_size() bytes, 16-byte aligned:
  *   the partial (O, m, l) of each segment of a row (S x 131 KB per row and
- *   64-head block), written and read within the call; calls that may run
+ *   64 heads), written and read within the call; calls that may run
  *   concurrently need separate workspaces.
  * Device errors: INDEX (an index >= the visible entries; that entry is skipped).
  */

@@ -56,14 +56,14 @@ def lib():
 
 def test_attn_workspace_holds_every_segment_partial(lib):
     # a segment's partial: O [64][512] + (m, l) [64][2] fp32.  The segment count
-    # is min(8, chunks) with chunks = ceil(k / 32) + 4 (the 128-token window) --
+    # is min(4, chunks) with chunks = ceil(k / 32) + 4 (the 128-token window) --
     # a function of k alone, so the workspace grows linearly with the batch
     part = 64 * (512 + 2) * 4
-    assert lib.csa2_attn_workspace_size(1, 64, 512) == 8 * part + 256
-    assert lib.csa2_attn_workspace_size(19, 64, 512) == 19 * 8 * part + 256
-    assert lib.csa2_attn_workspace_size(32, 64, 512) == 32 * 8 * part + 256
-    # 128 heads: two head blocks per row
-    assert lib.csa2_attn_workspace_size(1, 128, 512) == 2 * 8 * part + 256
-    # k = 32: one chunk of selected entries + 4 window chunks = 5 segments
-    assert lib.csa2_attn_workspace_size(1, 64, 32) == 5 * part + 256
-    assert lib.csa2_attn_workspace_size(3, 16, 64) == 3 * 6 * part + 256
+    assert lib.csa2_attn_workspace_size(1, 64, 512) == 4 * part + 256
+    assert lib.csa2_attn_workspace_size(19, 64, 512) == 19 * 4 * part + 256
+    assert lib.csa2_attn_workspace_size(32, 64, 512) == 32 * 4 * part + 256
+    # 128 heads: two 64-head blocks per row; 48 heads: sized as one 64-head block
+    assert lib.csa2_attn_workspace_size(1, 128, 512) == 2 * 4 * part + 256
+    assert lib.csa2_attn_workspace_size(2, 48, 512) == 2 * 4 * part + 256
+    # k = 1: one chunk of selected entries + 4 window chunks, still 4 segments
+    assert lib.csa2_attn_workspace_size(1, 64, 1) == 4 * part + 256

@@ -2,9 +2,11 @@
 output must be bitwise the same whatever the batch it is computed in).
 
 One sequence's decode step -- index scores, top-k and candidate pool, sparse
-attention -- is run inside batches of 1, 32, 76 and 160 sequences, which spread
-a row over 8, 4, 2 and 1 CTAs on a 152-SM GPU.  Its scores, selection, output
-and lse must be bit-identical across the batches.
+attention -- is run inside batches of 1, 32, 76 and 160 sequences.  On a
+152-SM GPU these launch the attention of a row as 4 CTAs of 16 heads each for
+each of the 4 head blocks, 4 CTAs of 64 heads, 2 CTAs, and 1 CTA: the same 4
+segments merged in the same order.  Its scores, selection, output and lse
+must be bit-identical across the batches.
 """
 import numpy as np
 import pytest

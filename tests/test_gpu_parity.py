@@ -266,13 +266,13 @@ def test_topk_nan_score_is_reported(orc):
 
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("B,T,H,k,swa_dtype,use_sink", [
-    (3, 700, 64, 64, csa2.SWA_MXFP8, False),   # 6 segments, one per CTA
+    (3, 700, 64, 64, csa2.SWA_MXFP8, False),   # 4 segments, one per CTA; 16-head blocks
     (3, 700, 64, 64, csa2.SWA_BF16, True),
-    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # 6 segments over 4 CTAs per row
-    (80, 200, 64, 48, csa2.SWA_BF16, False),   # one CTA per row computes all 6 segments
+    (32, 200, 64, 48, csa2.SWA_MXFP8, True),   # 4 CTAs per row, 64 heads each
+    (80, 200, 64, 48, csa2.SWA_BF16, False),   # one CTA per row computes all 4 segments
     (1, 90, 32, 128, csa2.SWA_MXFP8, False),   # window shorter than 128, idx padded with -1
-    (3, 1500, 128, 1024, csa2.SWA_BF16, True), # two head blocks, 8-CTA clusters, 5 chunks per segment
-    (2, 300, 48, 200, csa2.SWA_MXFP8, False),  # a partial head block
+    (3, 1500, 128, 1024, csa2.SWA_BF16, True), # 8 head blocks of 16, 9 chunks per segment
+    (2, 300, 48, 200, csa2.SWA_MXFP8, False),  # 48 heads in blocks of 16
 ])
 def test_sparse_attn_decode(orc, B, T, H, k, swa_dtype, use_sink):
     c, oc, _, err = build_r1(orc, B, T, swa_dtype, seed=41 + B)
