@@ -462,7 +462,20 @@ def run_ours(args):
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(W, args)
+    if rank == 0 and args.workload == "full_decode" and not args.headline_only:
+        # the metric's other context lengths and the prefill indexer, measured in
+        # the same run: the 1 M-context decoder group (config of 8 sequences x
+        # 1,048,576 tokens) and the chunked prefill, with the FP4 tensor peak
+        del bench, graphs
+        torch.cuda.empty_cache()
+        fp4 = measure_fp4_peak(dev)
+        line["fp4_peak"] = fp4
+        line["stack_1m"] = measure_group(wl.stack_1m(device="cuda"), max(10, min(args.steps, 20)), 3, dev)
+        torch.cuda.empty_cache()
+        line["prefill"] = measure_prefill(wl.prefill_chunk(device="cuda"), 3, 3, dev, fp4["tflops"])
+        torch.cuda.empty_cache()
     if world > 1:
+        torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -710,21 +723,13 @@ class PrefillBench:
                                 W.topk, W.sm_scale, self.idx, self.out, self.lse, self.ws, err=self.err)
 
 
-def run_secondary(args):
-    from fp4_compressed_sparse_gb300 import build_lib, csa2
-    from fp4_compressed_sparse_gb300 import workloads as wl
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    build_lib.build()
-    csa2.load()
-    W = getattr(wl, args.workload)(device="cuda")
-    prefill = args.workload == "prefill_chunk"
-    steps = args.steps
-    bench = PrefillBench(W, dev) if prefill else GroupDecode(W, args.warmup + steps, dev)
+def measure_group(W, steps, warmup, dev):
+    """One decoder-group workload (Full / Reindex / Reuse layers over one cache):
+    `steps` timed steps, one CUDA graph each, L2 flushed between them; then one
+    more step run layer by layer with events between, for the per-layer split."""
+    bench = GroupDecode(W, warmup + steps, dev)
     flush = L2Flush(dev)
-    prep = bench.restore if prefill else (lambda: None)
-    for s in range(args.warmup):
-        prep()
+    for s in range(warmup):
         flush()
         bench.step(s)
     torch.cuda.synchronize()
@@ -734,15 +739,87 @@ def run_secondary(args):
     for i in range(steps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            bench.step(0 if prefill else args.warmup + i)
+            bench.step(warmup + i)
         graphs.append(g)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    sampler = ClockSampler(0)
+    sampler = ClockSampler(dev.index or 0)
     sampler.start()
     t_begin = time.perf_counter()
     for i in range(steps):
-        prep()
+        flush()
+        ev[i][0].record()
+        graphs[i].replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    sampler.mark(t_begin, time.perf_counter())
+    clocks = sampler.stop()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} in the timed steps")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(step_ms)
+    del graphs
+    # per-layer breakdown: one more step, parts in order with events between
+    # (the cache is then one token longer, which changes nothing measurable)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(W.layers) + 1)]
+    flush()
+    bench.step(warmup + steps - 1, marks=list(marks))
+    torch.cuda.synchronize()
+    parts = []
+    for l, role in enumerate(W.layers):
+        a, b, c2 = marks[2 * l], marks[2 * l + 1], marks[2 * l + 2]
+        parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
+                      "attention_ms": round(b.elapsed_time(c2), 4)})
+    hbm, hbm_kind = peaks()
+    T = (W.context + warmup + steps // 2) // W.ratio  # visible entries at the middle step
+    nbytes = group_step_bytes(W, T)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del bench
+    return {"metric": "decoder-group tokens/s and algorithmic HBM GB/s (% of roofline)",
+            "workload": W.name, "value": round(W.batch / (ms / 1e3), 2), "unit": "tokens/s",
+            "higher_is_better": True, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4),
+            "ms_per_step_min_max": [round(min(step_ms), 4), round(max(step_ms), 4)],
+            "layers": list(W.layers), "batch": W.batch, "context": W.context,
+            "kv_hbm": {"algorithmic_bytes_per_step": nbytes, "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                       "peak_gbs": hbm, "peak_kind": hbm_kind},
+            "layer_breakdown": parts, "clocks": clocks, "l2": "flushed between timed steps",
+            "launch": "one CUDA graph per step"}
+
+
+def prefill_flop(W):
+    """FP4 indexer scoring FLOP of one chunk: 2 * H_I * 128 per (query, visible
+    entry); query i sees prior/2 + i//2 entries."""
+    return sum(2 * W.index_heads * 128 * (W.prior // 2 + i // 2) for i in range(W.chunk))
+
+
+def measure_prefill(W, steps, warmup, dev, fp4_peak=None):
+    """Chunked prefill: `steps` timed chunks (one CUDA graph each, the cache's token
+    count, window ring and compression buffer restored and the L2 flushed before
+    each, outside the events), then one chunk with the library's phase events for
+    the append / score / select / attention split."""
+    from fp4_compressed_sparse_gb300 import csa2
+    bench = PrefillBench(W, dev)
+    flush = L2Flush(dev)
+    for s in range(warmup):
+        bench.restore()
+        flush()
+        bench.step(s)
+    torch.cuda.synchronize()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} during warm-up")
+    graphs = []
+    for i in range(steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            bench.step(0)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    t_begin = time.perf_counter()
+    for i in range(steps):
+        bench.restore()
         flush()
         ev[i][0].record()
         graphs[i].replay()
@@ -753,53 +830,88 @@ def run_secondary(args):
     if bench.err.item() != 0:
         raise RuntimeError(f"device error word {bench.err.item()} in the timed steps")
     ms = statistics.median([a.elapsed_time(b) for a, b in ev])
-    hbm, hbm_kind = peaks()
-    line = {"workload": W.name, "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "data": "synthetic (seeded)", "clocks": clocks, "impl": "ours",
-            "l2": "flushed between timed steps", "launch": "one CUDA graph per step"}
-    if prefill:
-        Q = W.chunk
-        # FP4 indexer scoring: 2 * H_I * 128 per (query, visible entry); query i sees prior/2 + i//2 entries
-        flop = sum(2 * W.index_heads * 128 * (W.prior // 2 + i // 2) for i in range(Q))
-        fp4_peak = None
-        try:
-            fp4_peak = json.load(open(PEAKS_FILE))["bf16_tflops"] * 6.0
-        except Exception:
-            fp4_peak = 1900.0 * 6.0
-        rate = flop / (ms / 1e3) / 1e12
-        line.update({"metric": "prefill chunk: query tokens/s, and FP4 scoring TFLOP/s over the whole chunk",
-                     "value": round(Q / (ms / 1e3), 2), "unit": "tokens/s", "higher_is_better": True,
-                     "scoring_tflop": round(flop / 1e12, 3),
-                     "tensor": {"achieved_tflops_lower_bound": round(rate, 1), "fp4_peak_tflops": round(fp4_peak, 1),
-                                "peak_kind": "measured bf16 x 6 (nominal fp4 / bf16)",
-                                "frac_lower_bound": round(rate / fp4_peak, 4),
-                                "note": "the whole chunk's time (append, scoring, top-k, attention) divides the scoring FLOP"}})
-    else:
-        # per-layer breakdown: one more step, parts in order with events between
-        # (the cache is then one token longer, which changes nothing measurable)
-        marks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(W.layers) + 1)]
-        ev_list = list(marks)
-        flush()
-        bench.step(args.warmup + steps - 1, marks=ev_list)
+    del graphs
+    # phase split: events recorded by the library at its phase boundaries
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(256)]
+    for e in pev:
+        e.record()
+    torch.cuda.synchronize()
+    bench.restore()
+    flush()
+    csa2.set_phase_events(pev)
+    bench.step(0)
+    n = csa2.phase_events_recorded()
+    csa2.set_phase_events(None)
+    torch.cuda.synchronize()
+    phases = {"append": pev[0].elapsed_time(pev[1]), "score": 0.0, "select": 0.0, "attention": 0.0}
+    for b in range(2, n - 2, 3):
+        phases["score"] += pev[b - 1].elapsed_time(pev[b])
+        phases["select"] += pev[b].elapsed_time(pev[b + 1])
+        phases["attention"] += pev[b + 1].elapsed_time(pev[b + 2])
+    flop = prefill_flop(W)
+    score_rate = flop / (phases["score"] / 1e3) / 1e12
+    chunk_rate = flop / (ms / 1e3) / 1e12
+    out = {"metric": "prefill chunk: query tokens/s, and FP4 scoring TFLOP/s",
+           "workload": W.name, "value": round(W.chunk / (ms / 1e3), 2), "unit": "tokens/s",
+           "higher_is_better": True, "steps": steps, "warmup": warmup, "ms_per_chunk": round(ms, 4),
+           "chunk": W.chunk, "prior_tokens": W.prior, "scoring_tflop": round(flop / 1e12, 3),
+           "phase_ms": {k: round(v, 4) for k, v in phases.items()},
+           "phase_note": "one extra chunk with the library's phase events (score blocks of queries, "
+                         "each scored, selected and attended in turn)",
+           "tensor": {"scoring_tflops_in_score_phase": round(score_rate, 1),
+                      "scoring_tflops_over_chunk": round(chunk_rate, 1)},
+           "clocks": clocks, "l2": "flushed between timed chunks", "launch": "one CUDA graph per chunk"}
+    if fp4_peak:
+        out["tensor"].update({"fp4_peak_tflops": fp4_peak, "frac_in_score_phase": round(score_rate / fp4_peak, 4),
+                              "peak_kind": "measured (tcgen05 kind::mxf4 M128 N128 K64 back to back)"})
+    del bench
+    return out
+
+
+def measure_fp4_peak(dev, reps=5):
+    """Dense rate of the index score's block-scaled FP4 MMA (tcgen05 kind::mxf4,
+    M 128 x N 128 x K 64), operands resident in shared memory, one CTA per SM:
+    best of `reps` launches of ~2-4 ms, timed with CUDA events."""
+    from fp4_compressed_sparse_gb300 import csa2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    iters = 1 << 15
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    sink = torch.zeros(sms, dtype=torch.int32, device=dev)
+    csa2.mxf4_peak_launch(sms, 64, sink, err)  # warm-up
+    best = 0.0
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        csa2.mxf4_peak_launch(sms, iters, sink, err)
+        b.record()
         torch.cuda.synchronize()
-        parts = []
-        for l, role in enumerate(W.layers):
-            a, b, c2 = marks[2 * l], marks[2 * l + 1], marks[2 * l + 2]
-            parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
-                          "attention_ms": round(b.elapsed_time(c2), 4)})
-        line["layer_breakdown"] = parts
-        T = (W.context + args.warmup + steps // 2) // W.ratio  # visible entries at the middle step
-        nbytes = group_step_bytes(W, T)
-        gbs = nbytes / (ms / 1e3) / 1e9
-        line.update({"metric": "decoder-group tokens/s and algorithmic HBM GB/s (% of roofline)",
-                     "value": round(W.batch / (ms / 1e3), 2), "unit": "tokens/s", "higher_is_better": True,
-                     "layers": list(W.layers), "batch": W.batch, "context": W.context,
-                     "kv_hbm": {"algorithmic_bytes_per_step": nbytes, "gbs": round(gbs, 1),
-                                "frac": round(gbs / hbm, 4), "peak_gbs": hbm, "peak_kind": hbm_kind}})
+        ms = a.elapsed_time(b)
+        times.append(ms)
+        best = max(best, sms * iters * 2.0 * 128 * 128 * 64 / (ms / 1e3) / 1e12)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the FP4 peak kernel")
+    return {"tflops": round(best, 1), "ctas": sms, "mma_per_cta": iters, "launch_ms": [round(t, 3) for t in times],
+            "instruction": "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X M128 N128 K64"}
+
+
+def run_secondary(args):
+    from fp4_compressed_sparse_gb300 import build_lib, csa2
+    from fp4_compressed_sparse_gb300 import workloads as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build_lib.build()
+    csa2.load()
+    W = getattr(wl, args.workload)(device="cuda")
+    if args.workload == "prefill_chunk":
+        line = measure_prefill(W, args.steps, args.warmup, dev, measure_fp4_peak(dev)["tflops"])
+    else:
+        line = measure_group(W, args.steps, args.warmup, dev)
+    line.update({"data": "synthetic (seeded)", "impl": "ours"})
     print(json.dumps(line), flush=True)
 
 # ----------------------------------------------------------------------------- oracle arm
-def cpu_baseline(W, args, sample_steps=None, min_seconds=10.0, max_steps=1024):
+def cpu_baseline(W, args, sample_steps=None, min_seconds=10.0, max_steps=1024, single_thread_steps=3):
     """The CPU oracle (as it stands) on a bounded sample of the workload: sequence 0,
     decode steps (append the token, Full-layer score over every visible position,
     top-k, pool, attention) on the host cores, `sample_steps` of them, or when that is
@@ -832,11 +944,29 @@ def cpu_baseline(W, args, sample_steps=None, min_seconds=10.0, max_steps=1024):
         orc.full_layer(cache, q_idx, w, q, W.context + s, W.topk, W.sm_scale)
         t_total += time.perf_counter() - t0
         done += 1
-    return {"value": round(done / t_total, 4), "unit": UNIT, "cores": orc.num_threads(),
-            "kind": "oracle", "seconds": round(t_total, 3), "steps": done,
-            "sample": f"sequence 0 x {done} decode step(s) of {W.name}: append + Full-layer "
-                      f"score over {W.context} positions x {W.index_heads} heads + top-{W.topk} + "
-                      f"pool + attention ({W.heads} heads)"}
+    out = {"value": round(done / t_total, 4), "unit": UNIT, "cores": orc.num_threads(),
+           "kind": "oracle", "seconds": round(t_total, 3), "steps": done,
+           "sample": f"sequence 0 x {done} decode step(s) of {W.name}: append + Full-layer "
+                     f"score over {W.context} positions x {W.index_heads} heads + top-{W.topk} + "
+                     f"pool + attention ({W.heads} heads)"}
+    if single_thread_steps > 0:
+        # the same steps again on one host thread
+        threads = orc.num_threads()
+        orc.set_num_threads(1)
+        t1 = 0.0
+        n1 = min(single_thread_steps, done)
+        for s in range(n1):
+            q_idx = u16(W.q_idx(s, 0, device=dev)[0])
+            w = W.w(s, 0, device=dev)[0].cpu().numpy()
+            q = u16(W.q(s, 0, device=dev)[0])
+            t0 = time.perf_counter()
+            orc.full_layer(cache, q_idx, w, q, W.context + s, W.topk, W.sm_scale)
+            t1 += time.perf_counter() - t0
+        orc.set_num_threads(threads)
+        out["single_thread"] = {"value": round(n1 / t1, 4), "unit": UNIT, "cores": 1, "seconds": round(t1, 3),
+                                "steps": n1, "note": "Full-layer score + top-k + pool + attention of the first "
+                                                     "steps again (the cache already holds their tokens)"}
+    return out
 
 
 def run_reference(args):
@@ -846,7 +976,7 @@ def run_reference(args):
     from fp4_compressed_sparse_gb300 import workloads as wl
     W = getattr(wl, args.workload)(device="cuda" if torch.cuda.is_available() else "cpu")
     steps = max(1, args.steps)
-    cb = cpu_baseline(W, args, sample_steps=steps)
+    cb = cpu_baseline(W, args, sample_steps=steps, single_thread_steps=0)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * cb["seconds"] / steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32",
@@ -856,6 +986,18 @@ def run_reference(args):
             "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def spawn_ranks(n):
+    """Run this command as n local ranks (torch.distributed.run on 127.0.0.1) and
+    return its exit status; rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def main():
@@ -874,9 +1016,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch every kernel eagerly instead of one "
                     "CUDA graph per step")
+    ap.add_argument("--headline-only", action="store_true", help="skip the 1 M-context group, the prefill chunk "
+                    "and the FP4 peak that the default run adds to its line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" in os.environ:
+        if int(os.environ["WORLD_SIZE"]) != args.gpus:
+            ap.error(f"--gpus {args.gpus} but WORLD_SIZE={os.environ['WORLD_SIZE']}")
+    elif args.gpus > 1:
+        # one process per GPU: start the ranks here, as the launcher would
+        sys.exit(spawn_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
     elif args.workload in ("reindex_decode", "stack_1m", "encoder_decode", "prefill_chunk"):

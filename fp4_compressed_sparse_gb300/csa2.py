@@ -25,8 +25,8 @@ EXPORTS = [
     "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
     "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
-    "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_status_string",
-    "csa2_last_error_detail", "csa2_version",
+    "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mxf4_peak_launch", "csa2_set_phase_events",
+    "csa2_phase_events_recorded", "csa2_status_string", "csa2_last_error_detail", "csa2_version",
 ]
 
 
@@ -86,6 +86,9 @@ def load() -> ctypes.CDLL:
         "csa2_prefill_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "csa2_prefill_chunk": (i32, [vp, i32, vp, vp, i64, i32, vp, vp, i32, vp, i32, i32, vp, f32,
                                      vp, vp, vp, vp, sz, vp, vp]),
+        "csa2_mxf4_peak_launch": (i32, [i32, i32, vp, vp, vp]),
+        "csa2_set_phase_events": (i32, [vp, i32]),
+        "csa2_phase_events_recorded": (i32, []),
         "csa2_status_string": (ctypes.c_char_p, [i32]),
         "csa2_last_error_detail": (ctypes.c_char_p, []),
         "csa2_version": (i32, []),
@@ -276,3 +279,32 @@ def prefill_chunk(cache: Cache, seq, cmp, rope_cs, q_idx, w, q, k, sm_scale, idx
                               float(sm_scale), _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws),
                               ws.numel(), _ptr(err), _stream(stream))
     _check("csa2_prefill_chunk", st)
+
+
+# --------------------------------------------------------------------------- measurement helpers
+def mxf4_peak_launch(n_ctas, iters, sink=None, err=None, stream=None):
+    """Back-to-back block-scaled FP4 MMAs (M 128 x N 128 x K 64) on every CTA;
+    the caller times it: n_ctas * iters * 2 * 128 * 128 * 64 FLOP."""
+    _check("csa2_mxf4_peak_launch", load().csa2_mxf4_peak_launch(n_ctas, iters, _ptr(sink), _ptr(err),
+                                                                  _stream(stream)))
+
+
+_phase_keep = None
+
+
+def set_phase_events(events):
+    """Record the given torch.cuda.Events at the phase boundaries of this thread's
+    next prefill_chunk calls (None or [] stops); each must have been recorded once
+    so that its CUDA event exists."""
+    global _phase_keep
+    if not events:
+        _phase_keep = None
+        _check("csa2_set_phase_events", load().csa2_set_phase_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _phase_keep = arr
+    _check("csa2_set_phase_events", load().csa2_set_phase_events(arr, len(events)))
+
+
+def phase_events_recorded():
+    return int(load().csa2_phase_events_recorded())

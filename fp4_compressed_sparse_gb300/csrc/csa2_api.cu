@@ -16,6 +16,15 @@ namespace {
 
 thread_local std::string g_detail;
 
+// Optional phase markers of this thread's next csa2_prefill_chunk calls
+// (csa2_set_phase_events): events recorded on the call's stream in order.
+thread_local cudaEvent_t *g_phase_ev = nullptr;
+thread_local int g_phase_cap = 0, g_phase_used = 0;
+
+void mark_phase(cudaStream_t s) {
+  if (g_phase_ev != nullptr && g_phase_used < g_phase_cap) cudaEventRecord(g_phase_ev[g_phase_used++], s);
+}
+
 }  // namespace
 
 namespace csa2 {
@@ -197,6 +206,17 @@ const char *csa2_status_string(csa2_status s) {
 }
 
 const char *csa2_last_error_detail(void) { return g_detail.c_str(); }
+
+csa2_status csa2_set_phase_events(void *const *events, int32_t n_events) {
+  REQUIRE(n_events >= 0, CSA2_ERR_SHAPE, "n_events %d < 0", n_events);
+  REQUIRE(n_events == 0 || events != nullptr, CSA2_ERR_NULL, "events is NULL");
+  g_phase_ev = n_events ? reinterpret_cast<cudaEvent_t *>(const_cast<void **>(events)) : nullptr;
+  g_phase_cap = n_events;
+  g_phase_used = 0;
+  return CSA2_OK;
+}
+
+int32_t csa2_phase_events_recorded(void) { return g_phase_used; }
 
 size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane, int32_t swa_dtype) {
   const size_t e = static_cast<size_t>(batch) * capacity;
@@ -540,12 +560,15 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
   float *scores = reinterpret_cast<float *>(wb + L.off_scores);
   const csa2_cache v = seq_view(*cache, seq);
 
+  g_phase_used = 0;
+  mark_phase(s);  // start
   csa2::k_prefill_snapshot<<<64, 256, 0, s>>>(v, Q, P, qpos, ring_c, ring_s);
   cudaError_t e = csa2::launch_kv_append(v, nullptr, nullptr, CSA2_IN_F32, cmp, rope_cs, rope_len, Q, nullptr,
                                          err_word, s);
   if (e != cudaSuccess) return cuda_status(e, "prefill append");
   csa2::k_prefill_window<<<(Q + 7) / 8, 256, 0, s>>>(cmp->ca, Q, P, rope_cs, rope_len, cache->swa_dtype, lin_c,
                                                       cache->swa_dtype == CSA2_SWA_MXFP8 ? lin_s : nullptr);
+  mark_phase(s);  // append and window rows done
   for (int q0 = 0; q0 < Q; q0 += L.qb) {
     const int nq = Q - q0 < L.qb ? Q - q0 : L.qb;
     csa2::ScoreArgs sa{};
@@ -566,6 +589,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     sa.err = err_word;
     e = csa2::launch_index_score_tc(sa, wb + L.off_qrec, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill score");
+    mark_phase(s);  // block scored
     csa2::TopkArgs se{};
     se.rows = nq;
     se.scores = scores;
@@ -581,6 +605,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     se.err = err_word;
     e = csa2::launch_topk(se, wb + L.off_sel, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill top-k");
+    mark_phase(s);  // block selected
     csa2::AttnArgs aa{};
     aa.rows = nq;
     aa.heads = n_heads;
@@ -611,6 +636,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     // one segment per query: each query's attention is one pass over its entries
     e = csa2::launch_attn(aa, 1, wb + L.off_attn, L.total - L.off_attn, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill attention");
+    mark_phase(s);  // block attended
   }
   return cuda_status(cudaGetLastError(), "csa2_prefill_chunk");
 }

@@ -315,6 +315,32 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
                                float sm_scale, int32_t *idx_out, float *out, float *lse, void *ws,
                                size_t ws_bytes, int32_t *err_word, csa2_stream_t stream);
 
+/*
+ * csa2_mxf4_peak_launch: measurement helper (not a step of the method).
+ * Launches n_ctas CTAs that each issue `iters` back-to-back block-scaled FP4
+ * tensor-core MMAs (tcgen05 kind::mxf4, M 128 x N 128 x K 64, the index score's
+ * instruction) on operands resident in shared memory: n_ctas x iters x
+ * 2,097,152 FLOP.  The caller times it (events on `stream`) to get the dense
+ * FP4 rate the prefill indexer's tensor-pipe utilisation is reported against
+ * ([P5] §2.3.4: the indexer QK product runs in FP4).  sink: NULL, or device
+ * uint32 [n_ctas] receiving one accumulator word per CTA.  err_word: the
+ * TIMEOUT bit if the final wait gave up.  n_ctas 1..4096, iters 2..2^24.
+ */
+csa2_status csa2_mxf4_peak_launch(int32_t n_ctas, int32_t iters, uint32_t *sink, int32_t *err_word,
+                                  csa2_stream_t stream);
+
+/*
+ * csa2_set_phase_events: measurement helper.  events: n_events cudaEvent_t
+ * (created by the caller, owned by it) that this thread's next
+ * csa2_prefill_chunk calls record on their stream, in order, at the phase
+ * boundaries: the start, append + window rows done, then per block of queries
+ * scored, selected, attended (each call restarts at the first event; events
+ * beyond n_events are not recorded).  NULL / 0 stops the recording.
+ * csa2_phase_events_recorded() gives how many the last call recorded.
+ */
+csa2_status csa2_set_phase_events(void *const *events, int32_t n_events);
+int32_t csa2_phase_events_recorded(void);
+
 /* Status text, and the thread-local detail of this thread's last failure. */
 const char *csa2_status_string(csa2_status status);
 const char *csa2_last_error_detail(void);

@@ -575,3 +575,9 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads the parallel loops over independent rows use from now on (the
+ * single-thread time of the CPU baseline); n <= 0 leaves the count as it is. */
+void orc_set_num_threads(int n) {
+  if (n > 0) omp_set_num_threads(n);
+}

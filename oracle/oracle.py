@@ -105,6 +105,7 @@ def _declare(L):
         "orc_main_entry_bytes": (i32, [i32, i32]),
         "orc_mx_entry_bytes": (i32, [i32, i32]),
         "orc_num_threads": (i32, []),
+        "orc_set_num_threads": (None, [i32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -114,6 +115,11 @@ def _declare(L):
 
 def num_threads() -> int:
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops over independent rows from now on."""
+    lib().orc_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------------

@@ -99,3 +99,35 @@ def test_cache_plane_bytes_match_record(lib):
     assert lib.csa2_cache_plane_bytes(2, 129, 5, 1) == 2 * 2 * 512
     assert lib.csa2_cache_plane_bytes(1, 1, 6, 1) == 128 * 576
     assert lib.csa2_cache_plane_bytes(1, 1, 6, 0) == 128 * 1152
+
+
+def test_topk_noalloc_failures_carry_their_own_detail(lib):
+    """Every non-OK status of the no-allocation top-k sets its own detail text
+    (a previous call's text must not leak through)."""
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    lib.csa2_topk_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    cases = [
+        ((None, 100, 1, 1, fake, None, 0, 8, 16, fake, 0, None, None, None, None), 1, b"scores is NULL"),
+        ((odd, 100, 1, 1, fake, None, 0, 8, 16, fake, 0, None, None, None, None), 3, b"scores is not 16-byte"),
+        ((fake, 100, 0, 1, fake, None, 0, 8, 16, fake, 0, None, None, None, None), 2, b"batch 0"),
+        ((fake, 100, 1, 3, fake, None, 0, 8, 16, fake, 0, None, None, None, None), 4, b"ratio 3"),
+        ((fake, 100, 1, 1, fake, None, 0, 8, 0, fake, 0, None, None, None, None), 4, b"k 0"),
+        ((fake, 100, 1, 1, fake, None, 0, 4, 16, fake, 64, fake, fake, None, None), 5, b"8-position"),
+        ((fake, 1 << 26, 8, 1, fake, None, 0, 8, 16, fake, 0, None, None, None, None), 7, b"built-in array"),
+    ]
+    for args, status, text in cases:
+        lib.csa2_set_phase_events(None, 0)  # an OK call in between: leaves the old detail behind
+        assert lib.csa2_topk_noalloc(*args) == status, text
+        assert text in lib.csa2_last_error_detail(), (text, lib.csa2_last_error_detail())
+
+
+def test_measurement_helpers_validate(lib):
+    assert lib.csa2_mxf4_peak_launch(0, 100, None, None, None) == 2
+    assert lib.csa2_mxf4_peak_launch(152, 1, None, None, None) == 2
+    assert b"iters" in lib.csa2_last_error_detail()
+    assert lib.csa2_set_phase_events(None, 3) == 1
+    assert lib.csa2_set_phase_events(None, 0) == 0 and lib.csa2_phase_events_recorded() == 0
