@@ -903,7 +903,7 @@ def run_secondary(args):
     build_lib.build()
     csa2.load()
     W = getattr(wl, args.workload)(device="cuda")
-    if args.workload == "prefill_chunk":
+    if args.workload.startswith("prefill_chunk"):
         line = measure_prefill(W, args.steps, args.warmup, dev, measure_fp4_peak(dev)["tflops"])
     else:
         line = measure_group(W, args.steps, args.warmup, dev)
@@ -1007,7 +1007,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full_decode",
                     choices=["full_decode", "full_decode_small", "tiny_decode", "reindex_decode", "stack_1m",
-                             "encoder_decode", "prefill_chunk"],
+                             "encoder_decode", "prefill_chunk", "prefill_chunk_small"],
                     help="full_decode is the headline; reindex_decode, stack_1m, encoder_decode and prefill_chunk "
                          "print their own "
                          "measurement line")
@@ -1031,7 +1031,7 @@ def main():
         sys.exit(spawn_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("reindex_decode", "stack_1m", "encoder_decode", "prefill_chunk"):
+    elif args.workload in ("reindex_decode", "stack_1m", "encoder_decode", "prefill_chunk", "prefill_chunk_small"):
         run_secondary(args)
     else:
         run_ours(args)

@@ -587,6 +587,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     sa.stride = cache->capacity;
     sa.aux = wb + L.off_aux;
     sa.err = err_word;
+    sa.no_block_max = 1;  // the prefill's top-k builds no pool: the score histogram is all it reads
     e = csa2::launch_index_score_tc(sa, wb + L.off_qrec, s);
     if (e != cudaSuccess) return cuda_status(e, "prefill score");
     mark_phase(s);  // block scored

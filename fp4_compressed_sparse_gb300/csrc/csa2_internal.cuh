@@ -72,6 +72,7 @@ struct ScoreArgs {
   int64_t stride;
   uint8_t *aux;               // [rows][aux_row_bytes(stride)] sideband (its histograms are cleared by the launch), or nullptr
   int32_t *err;
+  int no_block_max;           // FULL with aux: 1 = the score histogram alone (no pool will be built from it)
 };
 cudaError_t launch_index_score(const ScoreArgs &a, cudaStream_t s);  // CUDA cores (dp4a), no sideband
 // tensor cores (tcgen05 kind::mxf4); needs pool == nullptr or pool_bs == 8, heads <= 128; fills aux

@@ -40,8 +40,8 @@
 //               (tcgen05.cp), the two MMAs, commits that release the stage and
 //               hand the accumulator over.
 //   the rest    epilogue: four warps (one per 32-lane TMEM quarter) per
-//               accumulator, four accumulators (two when 4 x N columns do not
-//               fit TMEM beside the scale factors).  A thread owns one key: it
+//               accumulator, six accumulators (four or two when 6 x N columns
+//               do not fit TMEM beside the scale factors).  A thread owns one key: it
 //               reads the key's N accumulator columns and runs the fixed-order
 //               chain.  With a sideband buffer the epilogue also histograms the
 //               score keys (and, in FULL mode, the 8-position block maxima) in
@@ -70,8 +70,10 @@ constexpr int kIssuers = 2;              // MMA-issuing warps, alternate tiles
 constexpr int kStages = 14;
 // TMEM accumulator buffers (tiles in flight in the epilogue): four while they
 // and the scale-factor columns fit the 512 TMEM columns, else two
-__host__ __device__ constexpr int acc_of(int np) { return 4 * np + 8 * 4 + 8 * 2 * kIssuers <= 512 ? 4 : 2; }
-constexpr int kAccMax = 4;
+__host__ __device__ constexpr int acc_of(int np) {
+  return 6 * np + 8 * 6 + 8 * 2 * kIssuers <= 512 ? 6 : 4 * np + 8 * 4 + 8 * 2 * kIssuers <= 512 ? 4 : 2;
+}
+constexpr int kAccMax = 6;
 static_assert(kStages % kProducers == 0 && kStages % kIssuers == 0, "each role must own whole stages");
 constexpr int kFirstEpiWarp = kProducers + kIssuers;
 // four epilogue warps (one per TMEM lane quarter) per accumulator
@@ -80,7 +82,7 @@ constexpr int kStageBytes = kIdxTileCodeBytes + kIdxTileScaleBytes;  // 8704
 constexpr int kMaxRowsPerCta = 256;
 constexpr int kGatherDepth = 4;          // POOL: gathered tiles in flight per producer warp
 constexpr int kTouchCap = 2048;          // touched bins listed per histogram (more: the flush scans them all)
-constexpr int kRound = 32;               // accumulator columns read per TMEM load round in the epilogue
+constexpr int kRound = 16;               // accumulator columns read per TMEM load round in the epilogue
 constexpr uint32_t kWaitIters = 200;  // suspended polls of <= 1 ms each: a wait gives up after ~0.2 s
 
 // Per-row query record built by k_qprep: B codes (NP x 64 B, K-major no-swizzle:
@@ -238,9 +240,17 @@ __device__ __forceinline__ uint32_t sfb_word(const uint8_t *sf, int h) {
 __device__ __forceinline__ uint32_t sel_key(float f) { return isnan(f) ? 0u : orderable(f); }
 
 // Count one key in bin b of histogram h; a bin's first key also lists the bin.
+// atomic add on a shared-memory word, returning the old value (shared-space
+// atomics: the Smem reference alone does not tell the compiler the space)
+__device__ __forceinline__ uint32_t atom_add_shared(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(tc::smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void note_bin(Smem &sm, int h, uint32_t b) {
-  if (atomicAdd(&sm.hist[h][b], 1u) == 0u) {
-    const int k = atomicAdd(&sm.ntouched[h], 1);
+  if (atom_add_shared(&sm.hist[h][b], 1u) == 0u) {
+    const int k = static_cast<int>(atom_add_shared(reinterpret_cast<uint32_t *>(&sm.ntouched[h]), 1u));
     if (k < kTouchCap) sm.touched[h][k] = static_cast<uint16_t>(b);
   }
 }
@@ -267,9 +277,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 
 // kFullAux: the Full-layer scan with a sideband (no pool, aux present), fixed at
 // compile time so that its per-key path carries no mode tests
-template <int NP, bool kFullAux>
+// Modes fixed at compile time, so that the per-key path carries no mode tests:
+//   kModeGeneric   FULL or POOL, with or without a sideband
+//   kModeFullAux   FULL with the whole sideband (score histogram, 8-position
+//                  block maxima and their histogram: top-k can build a pool)
+//   kModeFullHist  FULL with the score histogram alone (the chunked prefill,
+//                  whose top-k builds no pool)
+constexpr int kModeGeneric = 0, kModeFullAux = 1, kModeFullHist = 2;
+
+template <int NP, int kMode>
 __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, int max_tiles, int64_t total_items,
                                                                 int64_t per_cta) {
+  constexpr bool kFullAux = kMode == kModeFullAux, kFullHist = kMode == kModeFullHist;
   extern __shared__ uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -281,8 +300,8 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
   constexpr int kAcc = acc_of(NP), kEpiWarps = 4 * kAcc;
   static_assert(kAcc % kIssuers == 0, "each accumulator must be fed by one issuer");
   const int brec = qrec_bytes(np);
-  const bool pool_mode = kFullAux ? false : a.s.pool != nullptr;
-  const bool has_aux = kFullAux ? true : a.s.aux != nullptr;
+  const bool pool_mode = (kFullAux || kFullHist) ? false : a.s.pool != nullptr;
+  const bool has_aux = (kFullAux || kFullHist) ? true : a.s.aux != nullptr;
   const int64_t seq_tiles = idx_tiles(a.s.cap);
 
   if (warp == 0) {
@@ -593,7 +612,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
             // sideband: score-key histogram; FULL rows also the max of each
             // 8-position block (8 consecutive lanes) and its histogram
             if (valid) note_bin(sm, 0, sel_key(acc) >> kSelBinShift);
-            if (!pool_mode) {
+            if (!pool_mode && !kFullHist) {
               float v = valid ? acc : -INFINITY;
               v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
               v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
@@ -687,8 +706,11 @@ cudaError_t launch_index_score_tc(const ScoreArgs &s, void *ws, cudaStream_t st)
   const size_t smem = sizeof(Smem) + 1024;
   using KernelFn = void (*)(TcArgs, int, int64_t, int64_t);
   KernelFn fn = nullptr;
-  const bool full_aux = s.pool == nullptr && s.aux != nullptr;
-#define CSA2_SCORE_FN(N) (full_aux ? k_index_score_tc<N, true> : k_index_score_tc<N, false>)
+  const int mode = (s.pool != nullptr || s.aux == nullptr) ? kModeGeneric : s.no_block_max ? kModeFullHist : kModeFullAux;
+#define CSA2_SCORE_FN(N)                                                                  \
+  (mode == kModeFullAux ? k_index_score_tc<N, kModeFullAux>                               \
+                        : mode == kModeFullHist ? k_index_score_tc<N, kModeFullHist>      \
+                                                : k_index_score_tc<N, kModeGeneric>)
   switch (a.np) {
     case 16: fn = CSA2_SCORE_FN(16); break;
     case 32: fn = CSA2_SCORE_FN(32); break;

@@ -201,6 +201,13 @@ def prefill_chunk(device="cuda"):
                            index_heads=64, topk=512, swa_dtype=1, seed=3, device=device)
 
 
+def prefill_chunk_small(device="cuda"):
+    """The chunked prefill with a chunk of 512 queries against the same 131,072 prior
+    tokens: one block of queries per launch, for small profiler captures."""
+    return PrefillWorkload("prefill_q512_prior131072_r2", prior=131072, chunk=512, heads=64,
+                           index_heads=64, topk=512, swa_dtype=1, seed=3, device=device)
+
+
 def encoder_decode(device="cuda"):
     """An encoder group at decode: ratio-2 caches of 131,072 tokens (65,536 entries),
     one token appended per step through the compression buffer, a Full layer and

@@ -424,8 +424,13 @@ def test_encoder_group_decode_steps(orc):
 
 
 # ------------------------------------------------------------------ prefill (small)
-def test_prefill_chunk_small(orc):
-    prior, Q, H_I, H, k = 300, 70, 4, 16, 32
+@pytest.mark.parametrize("prior,Q,H_I", [
+    (300, 70, 4),
+    (300, 71, 64),   # 64 indexer heads (the workloads' count), an odd chunk
+    (301, 40, 64),   # odd prior: a token waits in the compression buffer
+])
+def test_prefill_chunk_small(orc, prior, Q, H_I):
+    H, k = 16, 32
     c, oc, rope, err, (ba, bb), _, _ = build_r2(orc, 2, prior, csa2.SWA_MXFP8, seed=61,
                                                chunks=[prior], cap=(prior + Q) // 2 + 8)
     seq = 1
