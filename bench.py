@@ -472,6 +472,12 @@ def run_ours(args):
         line["fp4_peak"] = fp4
         line["stack_1m"] = measure_group(wl.stack_1m(device="cuda"), max(10, min(args.steps, 20)), 3, dev)
         torch.cuda.empty_cache()
+        # the 256 K Reindex + 3 Reuse group, then the same group with its Reindex
+        # layer in the published reference code's form (every position scored,
+        # the rest of the row masked)
+        line["reindex_256k"] = measure_group(wl.reindex_decode(device="cuda"), max(10, min(args.steps, 20)), 3, dev,
+                                             variant_layers=("reindex_masked", "reuse", "reuse", "reuse"))
+        torch.cuda.empty_cache()
         line["prefill"] = measure_prefill(wl.prefill_chunk(device="cuda"), 3, 3, dev, fp4["tflops"])
         torch.cuda.empty_cache()
     if world > 1:
@@ -565,6 +571,8 @@ def group_step_bytes(W, T):
             per_seq += T * 68 + qidx + attn
         elif role == "reindex":
             per_seq += W.pool_blocks * W.pool_block_size * 68 + W.pool_blocks * 4 + qidx + attn
+        elif role == "reindex_masked":  # every visible key is read
+            per_seq += T * 68 + W.pool_blocks * 4 + qidx + attn
         else:
             per_seq += attn
     return B * per_seq
@@ -675,6 +683,13 @@ class GroupDecode:
                               pool=self.pool, err=self.err, ws=self.ws_score, aux=self.paux)
                 c.topk(self.pscores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_ptopk, pool=self.pool,
                        err=self.err, aux=self.paux)
+            elif role == "reindex_masked":
+                # the published reference code's form: score every visible position,
+                # mask the positions outside the pool, top-k of the whole row
+                c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.scores, err=self.err,
+                              ws=self.ws_score)
+                c.mask_to_pool(self.scores, W.ratio, self.q_pos[s], self.pool, W.pool_block_size)
+                c.topk(self.scores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_topk, err=self.err)
             if not joined:
                 main.wait_event(join)  # the attention reads the new token's window slot
                 joined = True
@@ -723,15 +738,33 @@ class PrefillBench:
                                 W.topk, W.sm_scale, self.idx, self.out, self.lse, self.ws, err=self.err)
 
 
-def measure_group(W, steps, warmup, dev):
+def measure_group(W, steps, warmup, dev, variant_layers=None):
     """One decoder-group workload (Full / Reindex / Reuse layers over one cache):
     `steps` timed steps, one CUDA graph each, L2 flushed between them; then one
-    more step run layer by layer with events between, for the per-layer split."""
-    bench = GroupDecode(W, warmup + steps, dev)
+    more step run layer by layer with events between, for the per-layer split.
+    With variant_layers, the same cache and inputs are timed again with those
+    layer roles (a comparison of two forms of the same group)."""
+    # inputs (and cache room) for every step: warm-up, timed, the breakdown step,
+    # and the variant's timed and breakdown steps after them
+    n_steps = warmup + steps + 1 + ((steps + 1) if variant_layers else 0)
+    bench = GroupDecode(W, n_steps, dev)
+    out = _time_group(bench, W, steps, warmup, dev, first=0)
+    if variant_layers:
+        import dataclasses
+        Wv = dataclasses.replace(W, layers=tuple(variant_layers))
+        bench.W = Wv
+        out["variant"] = _time_group(bench, Wv, steps, 0, dev, first=warmup + steps + 1)
+    del bench
+    return out
+
+
+def _time_group(bench, W, steps, warmup, dev, first=0):
+    """Time `steps` steps of a GroupDecode whose step inputs start at index
+    `first` (warm-up steps first, then the timed ones, then one breakdown step)."""
     flush = L2Flush(dev)
     for s in range(warmup):
         flush()
-        bench.step(s)
+        bench.step(first + s)
     torch.cuda.synchronize()
     if bench.err.item() != 0:
         raise RuntimeError(f"device error word {bench.err.item()} during warm-up")
@@ -739,7 +772,7 @@ def measure_group(W, steps, warmup, dev):
     for i in range(steps):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            bench.step(warmup + i)
+            bench.step(first + warmup + i)
         graphs.append(g)
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -760,10 +793,9 @@ def measure_group(W, steps, warmup, dev):
     ms = statistics.mean(step_ms)
     del graphs
     # per-layer breakdown: one more step, parts in order with events between
-    # (the cache is then one token longer, which changes nothing measurable)
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(W.layers) + 1)]
     flush()
-    bench.step(warmup + steps - 1, marks=list(marks))
+    bench.step(first + warmup + steps, marks=list(marks))
     torch.cuda.synchronize()
     parts = []
     for l, role in enumerate(W.layers):
@@ -771,10 +803,9 @@ def measure_group(W, steps, warmup, dev):
         parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
                       "attention_ms": round(b.elapsed_time(c2), 4)})
     hbm, hbm_kind = peaks()
-    T = (W.context + warmup + steps // 2) // W.ratio  # visible entries at the middle step
+    T = (W.context + first + warmup + steps // 2) // W.ratio  # visible entries at the middle step
     nbytes = group_step_bytes(W, T)
     gbs = nbytes / (ms / 1e3) / 1e9
-    del bench
     return {"metric": "decoder-group tokens/s and algorithmic HBM GB/s (% of roofline)",
             "workload": W.name, "value": round(W.batch / (ms / 1e3), 2), "unit": "tokens/s",
             "higher_is_better": True, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4),
@@ -1006,8 +1037,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="full_decode",
-                    choices=["full_decode", "full_decode_small", "tiny_decode", "reindex_decode", "stack_1m",
-                             "encoder_decode", "prefill_chunk", "prefill_chunk_small"],
+                    choices=["full_decode", "full_decode_small", "tiny_decode", "reindex_decode", "reindex_masked_decode",
+                             "stack_1m", "encoder_decode", "prefill_chunk", "prefill_chunk_small"],
                     help="full_decode is the headline; reindex_decode, stack_1m, encoder_decode and prefill_chunk "
                          "print their own "
                          "measurement line")
@@ -1031,7 +1062,8 @@ def main():
         sys.exit(spawn_ranks(args.gpus))
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload in ("reindex_decode", "stack_1m", "encoder_decode", "prefill_chunk", "prefill_chunk_small"):
+    elif args.workload in ("reindex_decode", "reindex_masked_decode", "stack_1m", "encoder_decode", "prefill_chunk",
+                           "prefill_chunk_small"):
         run_secondary(args)
     else:
         run_ours(args)

@@ -25,7 +25,8 @@ EXPORTS = [
     "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
     "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
-    "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mxf4_peak_launch", "csa2_set_phase_events",
+    "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mask_to_pool", "csa2_mxf4_peak_launch",
+    "csa2_set_phase_events",
     "csa2_phase_events_recorded", "csa2_status_string", "csa2_last_error_detail", "csa2_version",
 ]
 
@@ -86,6 +87,7 @@ def load() -> ctypes.CDLL:
         "csa2_prefill_workspace_size": (sz, [i32, i32, i32, i32, i32]),
         "csa2_prefill_chunk": (i32, [vp, i32, vp, vp, i64, i32, vp, vp, i32, vp, i32, i32, vp, f32,
                                      vp, vp, vp, vp, sz, vp, vp]),
+        "csa2_mask_to_pool": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, vp]),
         "csa2_mxf4_peak_launch": (i32, [i32, i32, vp, vp, vp]),
         "csa2_set_phase_events": (i32, [vp, i32]),
         "csa2_phase_events_recorded": (i32, []),
@@ -279,6 +281,14 @@ def prefill_chunk(cache: Cache, seq, cmp, rope_cs, q_idx, w, q, k, sm_scale, idx
                               float(sm_scale), _ptr(idx_out), _ptr(out), _ptr(lse), _ptr(ws),
                               ws.numel(), _ptr(err), _stream(stream))
     _check("csa2_prefill_chunk", st)
+
+
+def mask_to_pool(scores, ratio, q_pos, pool, pool_block_size=8, stream=None):
+    """Set FULL-mode scores outside each row's candidate pool to -inf, in place
+    (the Reindex form of the published reference code)."""
+    B, stride = scores.shape
+    _check("csa2_mask_to_pool", load().csa2_mask_to_pool(_ptr(scores), stride, B, ratio, _ptr(q_pos), _ptr(pool),
+                                                          pool.shape[1], pool_block_size, _stream(stream)))
 
 
 # --------------------------------------------------------------------------- measurement helpers

@@ -196,6 +196,15 @@ def reindex_decode(device="cuda"):
                           layers=("reindex", "reuse", "reuse", "reuse"), device=device)
 
 
+def reindex_masked_decode(device="cuda"):
+    """reindex_decode with its Reindex layer in the published reference code's form:
+    every visible position scored, the positions outside the pool masked, top-k of
+    the whole row (same cache, pool and queries)."""
+    return DecodeWorkload("reindex_masked_reuse3_b64_t262144", batch=64, context=262144, heads=64,
+                          index_heads=64, topk=512, swa_dtype=1, seed=2,
+                          layers=("reindex_masked", "reuse", "reuse", "reuse"), device=device)
+
+
 def prefill_chunk(device="cuda"):
     return PrefillWorkload("prefill_q8192_prior131072_r2", prior=131072, chunk=8192, heads=64,
                            index_heads=64, topk=512, swa_dtype=1, seed=3, device=device)

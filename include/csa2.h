@@ -256,6 +256,22 @@ csa2_status csa2_topk_noalloc(const float *scores, int64_t score_stride, int32_t
                               int32_t *err_word, csa2_stream_t stream);
 
 /*
+ * csa2_mask_to_pool: the Reindex selection in the form of the published
+ * reference code ([P1] "DeepSeek V4.1 Flash 아키텍처 분석", §"공개 코드를 읽어 보니
+ * 남는 차이": Indexer.forward scores every key, then masks the positions outside
+ * the candidates), kept for comparison with scoring only inside the pool.
+ * scores [batch][score_stride] FULL-mode scores (csa2_index_score with pool ==
+ * NULL); every visible position s < floor(q_pos[b] / ratio) whose block
+ * s / pool_block_size is not among pool[b] (ascending block ids, -1 padded,
+ * pool_blocks per row) is set to -inf in place.  csa2_topk (FULL, k) over the
+ * masked row then selects what csa2_topk over the pool's scores selects
+ * whenever the pool holds at least k visible positions.  pool_block_size 1..64.
+ */
+csa2_status csa2_mask_to_pool(float *scores, int64_t score_stride, int32_t batch, int32_t ratio,
+                              const int64_t *q_pos, const int32_t *pool, int32_t pool_blocks,
+                              int32_t pool_block_size, csa2_stream_t stream);
+
+/*
  * csa2_sparse_attn_decode: core attention of one decode step over the k
  * selected entries and the window ([P5] §2.3.1 "Shared Key-Value MQA": each
  * entry is key and value; [P2] §4 absorbed query: logits over 576 dims, values

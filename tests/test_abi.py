@@ -131,3 +131,11 @@ def test_measurement_helpers_validate(lib):
     assert b"iters" in lib.csa2_last_error_detail()
     assert lib.csa2_set_phase_events(None, 3) == 1
     assert lib.csa2_set_phase_events(None, 0) == 0 and lib.csa2_phase_events_recorded() == 0
+
+
+def test_mask_to_pool_validates(lib):
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.csa2_mask_to_pool(None, 100, 1, 1, fake, fake, 8, 8, None) == 1
+    assert lib.csa2_mask_to_pool(fake, 100, 1, 3, fake, fake, 8, 8, None) == 4
+    assert lib.csa2_mask_to_pool(fake, 100, 1, 1, fake, fake, 8, 0, None) == 2
+    assert b"pool_block_size" in lib.csa2_last_error_detail()
