@@ -22,7 +22,7 @@ IN_F32, IN_BF16 = 0, 1
 D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128
 
 EXPORTS = [
-    "csa2_cache_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
+    "csa2_cache_plane_bytes", "csa2_paged_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
     "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mask_to_pool", "csa2_mxf4_peak_launch",
@@ -46,6 +46,8 @@ class CacheStruct(ctypes.Structure):
         ("idx_codes", ctypes.c_void_p), ("idx_scales", ctypes.c_void_p),
         ("swa_codes", ctypes.c_void_p), ("swa_scales", ctypes.c_void_p),
         ("cmp_buf", ctypes.c_void_p), ("n_tokens", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("page_entries", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+        ("n_pages", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -74,6 +76,7 @@ def load() -> ctypes.CDLL:
                                   ctypes.c_double, ctypes.c_size_t)
     sig = {
         "csa2_cache_plane_bytes": (sz, [i32, i32, i32, i32]),
+        "csa2_paged_plane_bytes": (sz, [i32, i32, i32]),
         "csa2_rope_table": (i32, [f64, i64, vp]),
         "csa2_kv_append": (i32, [vp, vp, vp, i32, vp, vp, i64, i32, vp, vp, vp]),
         "csa2_index_score_workspace_size": (sz, [i32, i32]),
@@ -120,21 +123,44 @@ def _stream(stream=None):
 
 # --------------------------------------------------------------------------- cache
 class Cache:
-    """Caller-owned device planes of one global-KV cache (see csa2_cache in csa2.h)."""
+    """Caller-owned device planes of one global-KV cache (see csa2_cache in csa2.h).
 
-    def __init__(self, batch, capacity, ratio=1, swa_dtype=SWA_MXFP8, device="cuda"):
+    Dense by default: every entry plane is [batch][capacity][...].  With
+    page_entries (a multiple of 128) the entry planes are a pool of n_pages
+    physical pages of page_entries entries, and block_table [batch][max_pages]
+    (int32, max_pages = capacity / page_entries) names the page that holds
+    entries p*page_entries .. of each sequence; by default n_pages = batch *
+    max_pages and the table is the identity."""
+
+    def __init__(self, batch, capacity, ratio=1, swa_dtype=SWA_MXFP8, device="cuda", page_entries=None,
+                 n_pages=None, block_table=None):
         L = load()
         self.batch, self.capacity, self.ratio, self.swa_dtype = batch, capacity, ratio, swa_dtype
+        self.page_entries = page_entries
         nb = [L.csa2_cache_plane_bytes(batch, capacity, p, swa_dtype) for p in range(10)]
         u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device=device)
-        self.lat_codes = u8(nb[0]).view(batch, capacity, 256)
-        self.lat_scales = u8(nb[1]).view(batch, capacity, 32)
-        self.rope_codes = u8(nb[2]).view(batch, capacity, 32)
-        self.rope_scales = u8(nb[3]).view(batch, capacity, 4)
-        # tile-major indexer planes (see csa2_cache in csa2.h)
-        self.idx_tiles = (capacity + 127) // 128
-        self.idx_codes = u8(nb[4]).view(batch, self.idx_tiles, 8192)
-        self.idx_scales = u8(nb[5]).view(batch, self.idx_tiles, 512)
+        if page_entries:
+            assert capacity % page_entries == 0 and page_entries % 128 == 0
+            self.max_pages = capacity // page_entries
+            self.n_pages = n_pages or batch * self.max_pages
+            if block_table is None:
+                block_table = torch.arange(batch * self.max_pages, dtype=torch.int32).view(batch, self.max_pages)
+            self.block_table = block_table.to(device=device, dtype=torch.int32).contiguous()
+            pb = [L.csa2_paged_plane_bytes(self.n_pages, page_entries, p) for p in range(6)]
+            rows, lead = self.n_pages * page_entries, (self.n_pages * page_entries,)
+            self.idx_tiles = rows // 128
+            planes = [u8(pb[0]).view(*lead, 256), u8(pb[1]).view(*lead, 32), u8(pb[2]).view(*lead, 32),
+                      u8(pb[3]).view(*lead, 4), u8(pb[4]).view(self.idx_tiles, 8192), u8(pb[5]).view(self.idx_tiles, 512)]
+        else:
+            self.max_pages = self.n_pages = 0
+            self.block_table = None
+            # tile-major indexer planes (see csa2_cache in csa2.h)
+            self.idx_tiles = (capacity + 127) // 128
+            planes = [u8(nb[0]).view(batch, capacity, 256), u8(nb[1]).view(batch, capacity, 32),
+                      u8(nb[2]).view(batch, capacity, 32), u8(nb[3]).view(batch, capacity, 4),
+                      u8(nb[4]).view(batch, self.idx_tiles, 8192), u8(nb[5]).view(batch, self.idx_tiles, 512)]
+        (self.lat_codes, self.lat_scales, self.rope_codes, self.rope_scales, self.idx_codes,
+         self.idx_scales) = planes
         sw = 576 if swa_dtype == SWA_MXFP8 else 1152
         self.swa_codes = u8(nb[6]).view(batch, WINDOW, sw)
         self.swa_scales = u8(nb[7]).view(batch, WINDOW, 32)
@@ -146,13 +172,32 @@ class Cache:
             self.lat_codes.data_ptr(), self.lat_scales.data_ptr(), self.rope_codes.data_ptr(),
             self.rope_scales.data_ptr(), self.idx_codes.data_ptr(), self.idx_scales.data_ptr(),
             self.swa_codes.data_ptr(), self.swa_scales.data_ptr(),
-            self.cmp_buf.data_ptr() if self.cmp_buf is not None else None, self.n_tokens.data_ptr())
+            self.cmp_buf.data_ptr() if self.cmp_buf is not None else None, self.n_tokens.data_ptr(),
+            self.block_table.data_ptr() if self.block_table is not None else None, page_entries or 0,
+            self.max_pages, self.n_pages, 0)
 
     def ref(self):
         return ctypes.byref(self.struct)
 
+    def _rows(self):
+        """Physical entry row of every (sequence, entry) of a paged cache: [B, cap] int64."""
+        pe = self.page_entries
+        pages = self.block_table.to(torch.int64)  # [B, max_pages]
+        return (pages[:, :, None] * pe + torch.arange(pe, device=pages.device)).reshape(self.batch, -1)
+
+    def plane(self, name):
+        """Entry plane `name` (lat_codes, lat_scales, rope_codes, rope_scales) per sequence: [B, cap, bytes]."""
+        t = getattr(self, name)
+        return t if not self.page_entries else t[self._rows()]
+
     def idx_entries(self):
         """The indexer planes re-read per entry: (codes [B,cap,64], scales [B,cap,4])."""
+        if self.page_entries:
+            nt = self.idx_tiles
+            codes = self.idx_codes.view(nt, 4, 128, 16).permute(0, 2, 1, 3).reshape(nt * 128, 64)
+            scales = self.idx_scales.view(nt, 32, 4, 4).permute(0, 2, 1, 3).reshape(nt * 128, 4)
+            rows = self._rows()
+            return codes[rows], scales[rows]
         B, nt = self.batch, self.idx_tiles
         codes = self.idx_codes.view(B, nt, 4, 128, 16).permute(0, 1, 3, 2, 4).reshape(B, nt * 128, 64)
         scales = self.idx_scales.view(B, nt, 32, 4, 4).permute(0, 1, 3, 2, 4).reshape(B, nt * 128, 4)

@@ -120,20 +120,33 @@ csa2_status check_cache(const csa2_cache *c) {
   if (c->swa_dtype == CSA2_SWA_MXFP8) REQUIRE_PTR(c->swa_scales);
   REQUIRE_PTR(c->n_tokens);
   if (c->ratio == 2) REQUIRE_PTR(c->cmp_buf);
+  if (c->block_table != nullptr) {
+    REQUIRE_PTR(c->block_table);
+    REQUIRE(c->page_entries >= 128 && c->page_entries % 128 == 0, CSA2_ERR_SHAPE,
+            "page_entries %d must be a positive multiple of 128", c->page_entries);
+    REQUIRE(c->max_pages >= 1 && c->n_pages >= 1, CSA2_ERR_SHAPE, "max_pages %d / n_pages %d", c->max_pages,
+            c->n_pages);
+    REQUIRE(static_cast<int64_t>(c->max_pages) * c->page_entries == c->capacity, CSA2_ERR_SHAPE,
+            "capacity %d != max_pages %d x page_entries %d", c->capacity, c->max_pages, c->page_entries);
+  }
   return CSA2_OK;
 }
 
 // A view of one sequence of a cache (batch 1).
 csa2_cache seq_view(const csa2_cache &c, int seq) {
   csa2_cache v = c;
-  const size_t e = static_cast<size_t>(seq) * c.capacity;
   v.batch = 1;
-  v.lat_codes += e * 256;
-  v.lat_scales += e * 32;
-  v.rope_codes += e * 32;
-  v.rope_scales += e * 4;
-  v.idx_codes += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileCodeBytes;
-  v.idx_scales += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileScaleBytes;
+  if (c.block_table != nullptr) {
+    v.block_table += static_cast<size_t>(seq) * c.max_pages;  // the entry planes are the shared page pool
+  } else {
+    const size_t e = static_cast<size_t>(seq) * c.capacity;
+    v.lat_codes += e * 256;
+    v.lat_scales += e * 32;
+    v.rope_codes += e * 32;
+    v.rope_scales += e * 4;
+    v.idx_codes += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileCodeBytes;
+    v.idx_scales += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileScaleBytes;
+  }
   v.swa_codes += static_cast<size_t>(seq) * csa2::kWin * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152);
   if (v.swa_scales) v.swa_scales += static_cast<size_t>(seq) * csa2::kWin * csa2::kSwaScaleStride;
   if (v.cmp_buf) v.cmp_buf += static_cast<size_t>(seq) * 4 * 4 * csa2::kDcmp;
@@ -189,7 +202,7 @@ __global__ void __launch_bounds__(256) k_prefill_window(const float *ca, int Q, 
 // ===================================================================== C ABI
 extern "C" {
 
-int32_t csa2_version(void) { return 100; }
+int32_t csa2_version(void) { return 200; }
 
 const char *csa2_status_string(csa2_status s) {
   switch (s) {
@@ -231,6 +244,20 @@ size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane, in
     case 7: return static_cast<size_t>(batch) * csa2::kWin * csa2::kSwaScaleStride;
     case 8: return static_cast<size_t>(batch) * 4 * 4 * csa2::kDcmp * sizeof(float);
     case 9: return static_cast<size_t>(batch) * sizeof(int64_t);
+  }
+  return 0;
+}
+
+size_t csa2_paged_plane_bytes(int32_t n_pages, int32_t page_entries, int32_t plane) {
+  if (n_pages <= 0 || page_entries <= 0 || page_entries % 128 != 0) return 0;
+  const size_t e = static_cast<size_t>(n_pages) * page_entries;
+  switch (plane) {
+    case 0: return e * 256;
+    case 1: return e * 32;
+    case 2: return e * 32;
+    case 3: return e * 4;
+    case 4: return e / csa2::kIdxTile * csa2::kIdxTileCodeBytes;
+    case 5: return e / csa2::kIdxTile * csa2::kIdxTileScaleBytes;
   }
   return 0;
 }
@@ -315,6 +342,7 @@ csa2_status csa2_index_score(const csa2_cache *cache, const uint16_t *q_idx, con
   csa2::ScoreArgs a{};
   a.idx_codes = cache->idx_codes;
   a.idx_scales = cache->idx_scales;
+  a.map = csa2::entry_map(*cache);
   a.cap = cache->capacity;
   a.ratio = cache->ratio;
   a.rows = cache->batch;
@@ -447,6 +475,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
   a.lat_scales = cache->lat_scales;
   a.rope_codes = cache->rope_codes;
   a.rope_scales = cache->rope_scales;
+  a.map = csa2::entry_map(*cache);
   a.cap = cache->capacity;
   a.ratio = cache->ratio;
   a.n_tokens = cache->n_tokens;
@@ -574,6 +603,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     csa2::ScoreArgs sa{};
     sa.idx_codes = v.idx_codes;
     sa.idx_scales = v.idx_scales;
+    sa.map = csa2::entry_map(v);
     sa.cap = cache->capacity;
     sa.ratio = 2;
     sa.rows = nq;
@@ -619,6 +649,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     aa.lat_scales = v.lat_scales;
     aa.rope_codes = v.rope_codes;
     aa.rope_scales = v.rope_scales;
+    aa.map = csa2::entry_map(v);
     aa.cap = cache->capacity;
     aa.ratio = 2;
     aa.n_tokens = v.n_tokens;

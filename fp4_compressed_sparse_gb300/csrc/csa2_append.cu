@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kEncThreads) k_append_r1(csa2_cache c, const v
   __syncthreads();
   block_rope(row, rope_cs + t * 64, rot);
   __syncthreads();
-  block_encode_entry(c, b, t, row, rot);
+  block_encode_entry(c, b, t, row, rot, err);
   if (j >= n_new - kWin) {
     const size_t slot = static_cast<size_t>(b) * kWin + (t % kWin);
     block_encode_swa(c.swa_codes + slot * (c.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152),
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) k_append_r2_entries(csa2_cache c, csa2_co
     if (dst_dbg) dst_dbg[j] = v;
   }
   __syncwarp();
-  warp_encode_entry(c, b, i, srow[warp], rope_cs + (2 * i) * 64, lane);
+  warp_encode_entry(c, b, i, srow[warp], rope_cs + (2 * i) * 64, lane, err);
 }
 
 // Ratio 2 tail: window slots of the last min(n_new,128) tokens (their own C^a

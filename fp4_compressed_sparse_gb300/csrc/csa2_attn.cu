@@ -160,7 +160,11 @@ __device__ __forceinline__ int entry_kind(const AttnArgs &a, int seq, int j, int
       raise_err(a.err, CSA2_DEVERR_INDEX);
       return 0;
     }
-    src = static_cast<int64_t>(seq) * a.cap + sel;
+    src = phys_entry(a.map, seq, sel);
+    if (src < 0) {  // a page id outside the pool
+      raise_err(a.err, CSA2_DEVERR_INDEX);
+      return 0;
+    }
     return 1;
   }
   const int64_t tok = qpos - (kWin - 1) + (j - kpad);

@@ -34,12 +34,41 @@ constexpr int kIdxTile = 128;
 constexpr int kIdxTileCodeBytes = 8192;
 constexpr int kIdxTileScaleBytes = 512;
 __host__ __device__ __forceinline__ int64_t idx_tiles(int64_t capacity) { return (capacity + kIdxTile - 1) / kIdxTile; }
-__host__ __device__ __forceinline__ size_t idx_code_off(int64_t seq_tiles_base, int64_t e, int chunk) {
-  return static_cast<size_t>(seq_tiles_base + e / kIdxTile) * kIdxTileCodeBytes + chunk * 2048 + (e % kIdxTile) * 16;
+// byte offsets of block `chunk` of row m (0..127) of physical tile `tile`
+__host__ __device__ __forceinline__ size_t idx_code_at(int64_t tile, int m, int chunk) {
+  return static_cast<size_t>(tile) * kIdxTileCodeBytes + chunk * 2048 + m * 16;
 }
-__host__ __device__ __forceinline__ size_t idx_scale_off(int64_t seq_tiles_base, int64_t e) {
-  const int m = static_cast<int>(e % kIdxTile);
-  return static_cast<size_t>(seq_tiles_base + e / kIdxTile) * kIdxTileScaleBytes + 16 * (m % 32) + 4 * (m / 32);
+__host__ __device__ __forceinline__ size_t idx_scale_at(int64_t tile, int m) {
+  return static_cast<size_t>(tile) * kIdxTileScaleBytes + 16 * (m % 32) + 4 * (m / 32);
+}
+
+// ---------------------------------------------------------------- entry addressing
+// Where entry e of sequence b lives: the dense layout ([batch][capacity], each
+// sequence's entries contiguous, its indexer tiles padded per sequence) or the
+// paged one (a block table maps page e / page of sequence b to a physical page
+// of `page` entries, a multiple of 128).
+struct EntryMap {
+  const int32_t *bt;  // [batch][max_pages], or nullptr: dense
+  int32_t page, max_pages, n_pages;
+  int64_t cap;        // entries per sequence
+};
+__host__ __device__ __forceinline__ EntryMap entry_map(const csa2_cache &c) {
+  return EntryMap{c.block_table, c.page_entries, c.max_pages, c.n_pages, c.capacity};
+}
+// physical entry of (b, e) for the 288 B / 36 B planes; -1 for a page id outside the pool
+__host__ __device__ __forceinline__ int64_t phys_entry(const EntryMap &m, int b, int64_t e) {
+  if (m.bt == nullptr) return static_cast<int64_t>(b) * m.cap + e;
+  const int32_t pg = m.bt[static_cast<int64_t>(b) * m.max_pages + e / m.page];
+  if (pg < 0 || pg >= m.n_pages) return -1;
+  return static_cast<int64_t>(pg) * m.page + e % m.page;
+}
+// physical 128-entry tile of tile t of sequence b for the indexer planes; -1 as above
+__host__ __device__ __forceinline__ int64_t phys_tile(const EntryMap &m, int b, int64_t t) {
+  if (m.bt == nullptr) return static_cast<int64_t>(b) * idx_tiles(m.cap) + t;
+  const int tpp = m.page / kIdxTile;
+  const int32_t pg = m.bt[static_cast<int64_t>(b) * m.max_pages + t / tpp];
+  if (pg < 0 || pg >= m.n_pages) return -1;
+  return static_cast<int64_t>(pg) * tpp + t % tpp;
 }
 
 // ---------------------------------------------------------------- error word

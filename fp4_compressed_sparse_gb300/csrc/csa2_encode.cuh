@@ -9,9 +9,16 @@ namespace csa2 {
 
 // Encode entry `e` of sequence b from an fp32 row in shared memory:
 // row[0:576] = main vector (RoPE dims 512..575 not yet rotated), row[576:704] = indexer key.
+// A paged cache whose table names a page outside the pool gets the INDEX bit.
 __device__ __forceinline__ void warp_encode_entry(const csa2_cache &c, int b, int64_t e, const float *row, const float *cs,
-                                  int lane) {
-  const size_t ent = static_cast<size_t>(b) * c.capacity + e;
+                                                  int lane, int32_t *err) {
+  const EntryMap map = entry_map(c);
+  const int64_t pe = phys_entry(map, b, e), pt = phys_tile(map, b, e / kIdxTile);
+  if (pe < 0 || pt < 0) {  // a page id outside the pool: nothing written
+    if (lane == 0) raise_err(err, CSA2_DEVERR_INDEX);
+    return;
+  }
+  const size_t ent = static_cast<size_t>(pe);
   float x[32];
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = row[16 * lane + i];
@@ -40,9 +47,8 @@ __device__ __forceinline__ void warp_encode_entry(const csa2_cache &c, int b, in
     for (int i = 0; i < 32; ++i) x[i] = row[kDqk + 32 * blk + i];
     uint32_t w[4];
     quant_mxfp4_32(x, w, &sc);
-    const int64_t tbase = static_cast<int64_t>(b) * idx_tiles(c.capacity);
-    *reinterpret_cast<uint4 *>(c.idx_codes + idx_code_off(tbase, e, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
-    c.idx_scales[idx_scale_off(tbase, e) + blk] = static_cast<uint8_t>(sc);
+    *reinterpret_cast<uint4 *>(c.idx_codes + idx_code_at(pt, e % kIdxTile, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
+    c.idx_scales[idx_scale_at(pt, e % kIdxTile) + blk] = static_cast<uint8_t>(sc);
   }
 }
 
@@ -127,9 +133,15 @@ __device__ __forceinline__ uint32_t nvfp4_pair(float x0, float x1, uint32_t *sc)
 // Entry e of sequence b from row[0:704] (smem: main vector, RoPE dims
 // unrotated, then the indexer key) and rot[0:64] (smem, rotated RoPE dims).
 __device__ __forceinline__ void block_encode_entry(const csa2_cache &c, int b, int64_t e, const float *row,
-                                                   const float *rot) {
+                                                   const float *rot, int32_t *err) {
   const int t = threadIdx.x, lane = t & 31;
-  const size_t ent = static_cast<size_t>(b) * c.capacity + e;
+  const EntryMap map = entry_map(c);
+  const int64_t pe = phys_entry(map, b, e), pt = phys_tile(map, b, e / kIdxTile);
+  if (pe < 0 || pt < 0) {  // a page id outside the pool: nothing written
+    if (t == 0) raise_err(err, CSA2_DEVERR_INDEX);
+    return;
+  }
+  const size_t ent = static_cast<size_t>(pe);
   uint32_t sc;
   {  // latent: thread t has dims 2t, 2t+1 (group t / 8)
     const float2 v = reinterpret_cast<const float2 *>(row)[t];
@@ -160,10 +172,9 @@ __device__ __forceinline__ void block_encode_entry(const csa2_cache &c, int b, i
       sc = static_cast<uint32_t>(ex + 127);
     }
     const int blk = lane >> 3;
-    const int64_t tbase = static_cast<int64_t>(b) * idx_tiles(c.capacity);
-    *reinterpret_cast<uint16_t *>(c.idx_codes + idx_code_off(tbase, e, blk) + 2 * (lane & 7)) =
+    *reinterpret_cast<uint16_t *>(c.idx_codes + idx_code_at(pt, e % kIdxTile, blk) + 2 * (lane & 7)) =
         static_cast<uint16_t>(codes);
-    if ((lane & 7) == 0) c.idx_scales[idx_scale_off(tbase, e) + blk] = static_cast<uint8_t>(sc);
+    if ((lane & 7) == 0) c.idx_scales[idx_scale_at(pt, e % kIdxTile) + blk] = static_cast<uint8_t>(sc);
   }
 }
 

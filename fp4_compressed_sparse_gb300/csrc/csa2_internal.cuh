@@ -58,6 +58,7 @@ __host__ __device__ __forceinline__ int64_t aux_row_bytes(int64_t stride) {
 struct ScoreArgs {
   const uint8_t *idx_codes;   // cache plane base
   const uint8_t *idx_scales;
+  EntryMap map;               // where a sequence's entries live (dense or paged)
   int64_t cap;                // entries per sequence
   int ratio;
   int rows;                   // query rows
@@ -109,6 +110,7 @@ struct AttnArgs {
   const int64_t *q_pos;       // [rows]
   int cache_seq;              // -1: row = sequence
   const uint8_t *lat_codes, *lat_scales, *rope_codes, *rope_scales;
+  EntryMap map;               // where a sequence's entries live (dense or paged)
   int64_t cap;
   int ratio;
   const int64_t *n_tokens;    // [batch]

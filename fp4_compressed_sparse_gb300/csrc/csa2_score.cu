@@ -100,12 +100,17 @@ __global__ void __launch_bounds__(kThreads) k_index_score_dp4a(ScoreArgs a) {
     }
     if (s >= T) return;
   }
-  const int64_t tbase = static_cast<int64_t>(seq) * idx_tiles(a.cap);
-  const uint32_t ksc = *reinterpret_cast<const uint32_t *>(a.idx_scales + idx_scale_off(tbase, s));
+  const int64_t pt = phys_tile(a.map, seq, s / kIdxTile);
+  if (pt < 0) {  // a page id outside the pool
+    raise_err(a.err, CSA2_DEVERR_INDEX);
+    return;
+  }
+  const int mrow = static_cast<int>(s % kIdxTile);
+  const uint32_t ksc = *reinterpret_cast<const uint32_t *>(a.idx_scales + idx_scale_at(pt, mrow));
   uint32_t kw[32];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
-    const uint4 u = *reinterpret_cast<const uint4 *>(a.idx_codes + idx_code_off(tbase, s, v));
+    const uint4 u = *reinterpret_cast<const uint4 *>(a.idx_codes + idx_code_at(pt, mrow, v));
     const uint32_t words[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {

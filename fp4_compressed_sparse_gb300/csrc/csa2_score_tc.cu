@@ -407,11 +407,17 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
         if (!ok) break;
         uint8_t *dst = sm.stage[s];
         if (!pool_mode) {
-          const size_t t = static_cast<size_t>(seq * seq_tiles + tile);
-          tc::mbar_expect_tx(&sm.full[s], kStageBytes);
-          bulk_g2s(tc::smem_addr(dst), a.s.idx_codes + t * kIdxTileCodeBytes, kIdxTileCodeBytes, &sm.full[s]);
-          bulk_g2s(tc::smem_addr(dst + kIdxTileCodeBytes), a.s.idx_scales + t * kIdxTileScaleBytes,
-                   kIdxTileScaleBytes, &sm.full[s]);
+          const int64_t t = phys_tile(a.s.map, seq, tile);
+          if (t >= 0) {
+            tc::mbar_expect_tx(&sm.full[s], kStageBytes);
+            bulk_g2s(tc::smem_addr(dst), a.s.idx_codes + static_cast<size_t>(t) * kIdxTileCodeBytes,
+                     kIdxTileCodeBytes, &sm.full[s]);
+            bulk_g2s(tc::smem_addr(dst + kIdxTileCodeBytes), a.s.idx_scales + static_cast<size_t>(t) * kIdxTileScaleBytes,
+                     kIdxTileScaleBytes, &sm.full[s]);
+          } else {  // a page id outside the pool: the tile is not read (its scores are unspecified)
+            raise_err(a.s.err, CSA2_DEVERR_INDEX);
+            tc::mbar_arrive(&sm.full[s]);
+          }
         } else {
           // 16 pool blocks of 8 keys: lane l gathers block l/2, code chunks 2*(l%2)..+1
           // and 4 of its scale words; outside the pool or the cache the copy reads
@@ -421,14 +427,17 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
           const int32_t pid =
               pidx < a.s.pool_blocks ? a.s.pool[static_cast<size_t>(row) * a.s.pool_blocks + pidx] : -1;
           const int64_t p0 = static_cast<int64_t>(pid) * a.s.pool_bs;
-          const bool okb = pid >= 0 && p0 + a.s.pool_bs <= seq_tiles * kIdxTile;
+          const int64_t pt = (pid >= 0 && p0 + a.s.pool_bs <= seq_tiles * kIdxTile) ? phys_tile(a.s.map, seq, p0 / kIdxTile)
+                                                                                   : -1;
+          const bool okb = pt >= 0;
           const uint32_t d0 = tc::smem_addr(dst);
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int c = 2 * (lane & 1) + cc;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const uint8_t *src = okb ? a.s.idx_codes + idx_code_off(seq * seq_tiles, p0 + i, c) : a.s.idx_codes;
+              const uint8_t *src = okb ? a.s.idx_codes + idx_code_at(pt, static_cast<int>((p0 + i) % kIdxTile), c)
+                                       : a.s.idx_codes;
               asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d0 + c * 2048 + (jb * 8 + i) * 16),
                            "l"(src), "r"(okb ? 16 : 0)
                            : "memory");
@@ -437,7 +446,8 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
 #pragma unroll
           for (int i4 = 0; i4 < 4; ++i4) {
             const int i = (lane & 1) * 4 + i4, m = jb * 8 + i;
-            const uint8_t *src = okb ? a.s.idx_scales + idx_scale_off(seq * seq_tiles, p0 + i) : a.s.idx_scales;
+            const uint8_t *src = okb ? a.s.idx_scales + idx_scale_at(pt, static_cast<int>((p0 + i) % kIdxTile))
+                                     : a.s.idx_scales;
             asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(
                              d0 + kIdxTileCodeBytes + 16 * (m % 32) + 4 * (m / 32)),
                          "l"(src), "r"(okb ? 4 : 0)

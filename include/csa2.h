@@ -105,6 +105,24 @@ typedef enum csa2_status {
  *   csa2_prefill_chunk advance it).  A ratio-r cache holds floor(n_tokens/r) entries.
  * ratio: 1 (one token per entry, decoder) or 2 (two tokens per entry, encoder;
  *   [P1] "Global KV는 네 곳에서 만든다", [P4] 178 B per token).
+ *
+ * Paged layout ([P5] §3.5.1 "Sparse Attention Kernel Co-Design": the global
+ * entries live in fixed-size blocks whose token count is a multiple of the
+ * compression ratios; the window and the compression buffer are
+ * per-sequence state, "State Cache"): with block_table != NULL the six entry
+ * planes hold n_pages physical pages of page_entries entries each, page-major
+ * (lat_codes [n_pages][page_entries][256], ..., the indexer planes
+ * [n_pages][page_entries/128][8192 B] and [..][512 B] in the same tile layout),
+ * and entry e of sequence b is entry e % page_entries of physical page
+ * block_table[b * max_pages + e / page_entries].  page_entries is a multiple of
+ * 128 (an indexer tile never straddles pages; a page's tokens are then a
+ * multiple of every ratio and of the 8-position pool block), capacity must
+ * equal max_pages * page_entries, and page ids lie in 0..n_pages-1 (an id
+ * outside raises the INDEX device bit and the access is skipped).  Pages may be
+ * shared between sequences only for entries they hold in common; the caller
+ * fills the table before the entries are appended.  The window ring, the
+ * compression buffer and n_tokens stay indexed by sequence.  block_table ==
+ * NULL: the dense layout above (page fields ignored).
  */
 typedef struct csa2_cache {
   int32_t batch;
@@ -117,6 +135,11 @@ typedef struct csa2_cache {
   uint8_t *swa_codes, *swa_scales;
   float *cmp_buf;
   int64_t *n_tokens;
+  const int32_t *block_table; /* [batch][max_pages] physical page ids, or NULL (dense) */
+  int32_t page_entries;       /* entries per page: a multiple of 128 */
+  int32_t max_pages;          /* pages a sequence may use: capacity / page_entries */
+  int32_t n_pages;            /* physical pages in the entry planes */
+  int32_t reserved;
 } csa2_cache;
 
 /* Ratio-2 compression inputs ([P5] §2.3.1 "압축된 Key-Value Entry"): per token
@@ -130,6 +153,8 @@ typedef struct csa2_compress_in {
 /* Bytes each plane of a cache needs (host helper; no device work). */
 size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane /* 0..9 as listed */,
                               int32_t swa_dtype);
+/* Bytes of entry plane 0..5 in the paged layout (n_pages pages of page_entries). */
+size_t csa2_paged_plane_bytes(int32_t n_pages, int32_t page_entries, int32_t plane);
 
 /*
  * csa2_rope_table (host): cos/sin table for the 64 RoPE dims, rope_cs[pos][i][2]

@@ -139,3 +139,18 @@ def test_mask_to_pool_validates(lib):
     assert lib.csa2_mask_to_pool(fake, 100, 1, 3, fake, fake, 8, 8, None) == 4
     assert lib.csa2_mask_to_pool(fake, 100, 1, 1, fake, fake, 8, 0, None) == 2
     assert b"pool_block_size" in lib.csa2_last_error_detail()
+
+
+def test_paged_cache_validation(lib):
+    from fp4_compressed_sparse_gb300 import csa2
+    fake = 1 << 20
+    st = csa2.CacheStruct(1, 512, 1, 1, *([fake] * 10), fake, 100, 5, 8, 0)  # page not a multiple of 128
+    assert lib.csa2_index_score(ctypes.byref(st), None, None, 4, None, None, 0, 8, None, 0, None, None, 0,
+                                None, None) == 2
+    assert b"page_entries" in lib.csa2_last_error_detail()
+    st = csa2.CacheStruct(1, 512, 1, 1, *([fake] * 10), fake, 128, 3, 8, 0)  # capacity != 3 x 128
+    assert lib.csa2_kv_append(ctypes.byref(st), None, None, 0, None, None, 1, 1, None, None, None) == 2
+    assert b"max_pages" in lib.csa2_last_error_detail()
+    assert lib.csa2_paged_plane_bytes(10, 256, 0) == 10 * 256 * 256
+    assert lib.csa2_paged_plane_bytes(10, 256, 4) == 10 * 2 * 8192
+    assert lib.csa2_paged_plane_bytes(10, 100, 0) == 0
