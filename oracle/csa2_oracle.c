@@ -256,6 +256,24 @@ void orc_encode_entry(const float *v, const float *ik, const float *cs, uint8_t 
   for (int b = 0; b < ORC_DI / 32; ++b) orc_mxfp4_quant32(ik + 32 * b, idx_codes + 16 * b, idx_scales + b);
 }
 
+/* The V4 entry, kept for comparison ([P5] §2.3.4: the KV entries are stored in
+ * FP8 except the RoPE dims, which stay BF16).  READING: the FP8 part uses the
+ * 8-bit window's MXFP8 rule (E4M3 with one E8M0 per 32 values); the RoPE dims
+ * are rotated first, as for the V4.1 record.
+ *   v[576] = entry vector, rope dims 512..575 NOT yet rotated; ik[128] = key
+ * Outputs: lat_codes[512] (E4M3), lat_scales[16] (E8M0), rope_codes[128]
+ *          (64 bf16, little-endian), idx_codes[64], idx_scales[4] (MXFP4). */
+void orc_encode_entry_v4(const float *v, const float *ik, const float *cs, uint8_t *lat_codes,
+                         uint8_t *lat_scales, uint8_t *rope_codes, uint8_t *idx_codes, uint8_t *idx_scales) {
+  float r[ORC_ROPE];
+  memcpy(r, v + ORC_LAT, sizeof(r));
+  orc_rope_apply(r, cs);
+  for (int b = 0; b < ORC_LAT / 32; ++b) orc_mxfp8_quant32(v + 32 * b, lat_codes + 32 * b, lat_scales + b);
+  uint16_t *h = (uint16_t *)rope_codes;
+  for (int i = 0; i < ORC_ROPE; ++i) h[i] = orc_bf16_encode(r[i]);
+  for (int b = 0; b < ORC_DI / 32; ++b) orc_mxfp4_quant32(ik + 32 * b, idx_codes + 16 * b, idx_scales + b);
+}
+
 /* The indexer-key records alone of n entries (the idx planes of
  * orc_encode_entry, entry by entry): ik [n][128] -> idx_codes [n][64],
  * idx_scales [n][4].  Entries are independent, so rows run in parallel. */
@@ -490,6 +508,14 @@ void orc_dequant_main(const uint8_t *lat_codes, const uint8_t *lat_scales, const
   orc_dequant_nvfp4(rope_codes, rope_scales, ORC_ROPE, out576 + ORC_LAT);
 }
 
+/* A V4 entry (orc_encode_entry_v4) back to 576 exact values. */
+void orc_dequant_main_v4(const uint8_t *lat_codes, const uint8_t *lat_scales, const uint8_t *rope_codes,
+                         double *out576) {
+  for (int i = 0; i < ORC_LAT; ++i) out576[i] = orc_e4m3_decode(lat_codes[i]) * orc_e8m0_decode(lat_scales[i >> 5]);
+  const uint16_t *h = (const uint16_t *)rope_codes;
+  for (int i = 0; i < ORC_ROPE; ++i) out576[ORC_LAT + i] = orc_bf16_decode(h[i]);
+}
+
 void orc_dequant_swa(const uint8_t *codes, const uint8_t *scales, int swa_mxfp8, double *out576) {
   if (swa_mxfp8) {
     for (int i = 0; i < ORC_DQK; ++i) out576[i] = orc_e4m3_decode(codes[i]) * orc_e8m0_decode(scales[i >> 5]);
@@ -503,7 +529,8 @@ int orc_sparse_attn(int H, const uint16_t *q_bf16 /* H x 576 */, const uint8_t *
                     const uint8_t *lat_scales, const uint8_t *rope_codes, const uint8_t *rope_scales,
                     const int32_t *idx, int k, const uint8_t *swa_codes, int64_t swa_code_stride,
                     const uint8_t *swa_scales, int64_t swa_scale_stride, int n_swa, int swa_mxfp8,
-                    const float *sink, float sm_scale, float *out /* H x 512 */, float *lse /* H */) {
+                    const float *sink, float sm_scale, float *out /* H x 512 */, float *lse /* H */,
+                    int entry_format /* 0: V4.1 FP4 record, 1: V4 FP8 + bf16 RoPE */) {
   int n = 0;
   for (int j = 0; j < k; ++j)
     if (idx[j] >= 0) ++n;
@@ -513,8 +540,11 @@ int orc_sparse_attn(int H, const uint16_t *q_bf16 /* H x 576 */, const uint8_t *
   for (int j = 0; j < k; ++j) {
     int64_t s = idx[j];
     if (s < 0) continue;
-    orc_dequant_main(lat_codes + s * 256, lat_scales + s * 32, rope_codes + s * 32, rope_scales + s * 4,
-                     ent + (size_t)e * ORC_DQK);
+    if (entry_format == 1)
+      orc_dequant_main_v4(lat_codes + s * 512, lat_scales + s * 16, rope_codes + s * 128, ent + (size_t)e * ORC_DQK);
+    else
+      orc_dequant_main(lat_codes + s * 256, lat_scales + s * 32, rope_codes + s * 32, rope_scales + s * 4,
+                       ent + (size_t)e * ORC_DQK);
     ++e;
   }
   for (int j = 0; j < n_swa; ++j) {

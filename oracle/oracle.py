@@ -91,6 +91,7 @@ def _declare(L):
         "orc_rope_cs": (None, [f64, i64, vp]),
         "orc_rope_apply": (None, [vp, vp]),
         "orc_encode_entry": (None, [vp] * 9),
+        "orc_encode_entry_v4": (None, [vp] * 8),
         "orc_encode_swa": (None, [vp, vp, i32, vp, vp]),
         "orc_encode_keys": (None, [i64, vp, vp, vp]),
         "orc_compress": (None, [i32, i32, vp, vp, vp, vp, vp, vp, vp]),
@@ -101,7 +102,7 @@ def _declare(L):
         "orc_dequant_main": (None, [vp, vp, vp, vp, vp]),
         "orc_dequant_swa": (None, [vp, vp, i32, vp]),
         "orc_sparse_attn": (i32, [i32, vp, vp, vp, vp, vp, vp, i32, vp, i64, vp, i64, i32, i32,
-                                  vp, f32, vp, vp]),
+                                  vp, f32, vp, vp, i32]),
         "orc_main_entry_bytes": (i32, [i32, i32]),
         "orc_mx_entry_bytes": (i32, [i32, i32]),
         "orc_num_threads": (i32, []),
@@ -229,6 +230,14 @@ def rope_apply(x64, cs):
 # --------------------------------------------------------------------------
 # Cache built by the oracle (host numpy arrays, one sequence)
 # --------------------------------------------------------------------------
+# Main-entry formats: bytes per entry of (lat_codes, lat_scales, rope_codes, rope_scales)
+ENTRY_FP4, ENTRY_FP8 = 0, 1
+ENTRY_PLANES = {
+    ENTRY_FP4: (256, 32, 32, 4),   # V4.1: the 288 B record + the 36 B RoPE sidecar
+    ENTRY_FP8: (512, 16, 128, 1),  # V4 ([P5] §2.3.4): E4M3 + E8M0 per 32 (528 B), RoPE in bf16 (128 B)
+}
+
+
 class Cache:
     """One sequence's cache, laid out like the pages' records.
 
@@ -238,14 +247,16 @@ class Cache:
     swa_codes [WIN, 576 or 1152] swa_scales [WIN, 18] -> window ring, slot = token % WIN
     """
 
-    def __init__(self, cap: int, swa_dtype: int = SWA_MXFP8, ratio: int = 1):
+    def __init__(self, cap: int, swa_dtype: int = SWA_MXFP8, ratio: int = 1, entry_format: int = ENTRY_FP4):
         self.cap = cap
         self.ratio = ratio
         self.swa_dtype = swa_dtype
-        self.lat_codes = np.zeros((cap, 256), np.uint8)
-        self.lat_scales = np.zeros((cap, 32), np.uint8)
-        self.rope_codes = np.zeros((cap, 32), np.uint8)
-        self.rope_scales = np.zeros((cap, 4), np.uint8)
+        self.entry_format = entry_format
+        lat, lsc, rop, rsc = ENTRY_PLANES[entry_format]
+        self.lat_codes = np.zeros((cap, lat), np.uint8)
+        self.lat_scales = np.zeros((cap, lsc), np.uint8)
+        self.rope_codes = np.zeros((cap, rop), np.uint8)
+        self.rope_scales = np.zeros((cap, rsc), np.uint8)
         self.idx_codes = np.zeros((cap, 64), np.uint8)
         self.idx_scales = np.zeros((cap, 4), np.uint8)
         sw = 576 if swa_dtype == SWA_MXFP8 else 1152
@@ -286,6 +297,24 @@ def encode_keys(cache, start: int, ik):
     cache.idx_scales[start:start + n] = scales
 
 
+def encode_entry_v4(v576, ik128, cs):
+    """The V4 entry ([P5] §2.3.4: FP8 except the RoPE dims, kept bf16): the record
+    bytes (lat_codes 512, lat_scales 16, rope_codes 128, rope_scales (unused) 1,
+    idx_codes 64, idx_scales 4)."""
+    v, ik = _f32(v576), _f32(ik128)
+    out = [np.zeros(n, np.uint8) for n in (512, 16, 128, 1, 64, 4)]
+    lib().orc_encode_entry_v4(_p(v), _p(ik), _p(_f32(cs)), _p(out[0]), _p(out[1]), _p(out[2]), _p(out[4]),
+                              _p(out[5]))
+    return out
+
+
+def encode_for(cache, v576, ik128, cs):
+    """The record of an entry in the cache's entry format."""
+    if getattr(cache, "entry_format", ENTRY_FP4) == ENTRY_FP8:
+        return encode_entry_v4(v576, ik128, cs)
+    return encode_entry(v576, ik128, cs)
+
+
 def encode_swa(v576, cs, swa_dtype):
     codes = np.zeros(576 if swa_dtype == SWA_MXFP8 else 1152, np.uint8)
     scales = np.zeros(18, np.uint8)
@@ -304,7 +333,7 @@ def append_r1(cache: Cache, kv, ik, theta: float):
     for j in range(n):
         t = cache.n_tokens + j
         cs = rope_cs(theta, t)
-        rec = encode_entry(kv[j], ik[j], cs)
+        rec = encode_for(cache, kv[j], ik[j], cs)
         for arr, val in zip((cache.lat_codes, cache.lat_scales, cache.rope_codes,
                              cache.rope_scales, cache.idx_codes, cache.idx_scales), rec):
             arr[t] = val
@@ -370,7 +399,7 @@ def append_r2(cache: Cache, ca, cb, za, zb, ba, bb, theta: float, dbg=None):
         if dbg is not None:
             dbg.append(v.copy())
         cs = rope_cs(theta, 2 * i)
-        rec = encode_entry(v[:576], v[576:], cs)
+        rec = encode_for(cache, v[:576], v[576:], cs)
         for arr, val in zip((cache.lat_codes, cache.lat_scales, cache.rope_codes,
                              cache.rope_scales, cache.idx_codes, cache.idx_scales), rec):
             arr[i] = val
@@ -461,7 +490,7 @@ def sparse_attn(cache: Cache, q_bf16, idx, q_pos: int, sm_scale: float, sink=Non
                           _p(cache.rope_scales), _p(idx), idx.shape[0], _p(swa_codes),
                           swa_codes.shape[1] if n_swa else 0, _p(swa_scales), 18, n_swa,
                           int(cache.swa_dtype == SWA_MXFP8), _p(sk) if sk is not None else None,
-                          float(sm_scale), _p(out), _p(lse))
+                          float(sm_scale), _p(out), _p(lse), int(getattr(cache, "entry_format", ENTRY_FP4)))
     return out, lse
 
 

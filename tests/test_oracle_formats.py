@@ -240,3 +240,57 @@ def test_encode_swa_matches_torch_route(orc):
         hb, _ = orc.encode_swa(v, cs, 0)
         ref_bf16 = torch.from_numpy(rot).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
         assert np.array_equal(hb.view(np.uint16), ref_bf16), trial
+
+
+def test_encode_entry_v4_independent_route(orc):
+    """The V4 entry ([P5] §2.3.4: FP8 except the RoPE dims, kept bf16) rebuilt by
+    an independent route: the 512 latent dims in 32-value blocks scaled by 2^-e
+    (e = floor(log2 amax) - 8 from numpy's frexp) and cast by torch's
+    float8_e4m3fn (clamped to +-448), the rotated RoPE dims by torch's bfloat16,
+    the indexer key as in the V4.1 record."""
+    rng = np.random.default_rng(43)
+    for trial in range(20):
+        v = (rng.standard_normal(576) * 2.0 ** rng.integers(-10, 10)).astype(np.float32)
+        ik = rng.standard_normal(128).astype(np.float32)
+        if trial == 2:
+            v[32:64] = 0.0
+        cs = orc.rope_cs(1e4, int(rng.integers(0, 100000)))
+        lc, ls, rc, _, ic, isc = orc.encode_entry_v4(v, ik, cs)
+        for b in range(16):
+            blk = v[32 * b:32 * b + 32].astype(np.float64)
+            amax = np.max(np.abs(blk))
+            if amax == 0.0:
+                assert ls[b] == 0 and not lc[32 * b:32 * b + 32].any()
+                continue
+            e = max(-127, min(127, int(np.frexp(amax)[1]) - 1 - 8))
+            assert ls[b] == e + 127
+            ref = torch.from_numpy(np.clip(np.ldexp(blk, -e), -448, 448).astype(np.float32)).to(
+                torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(lc[32 * b:32 * b + 32], ref), (trial, b)
+        rot = orc.rope_apply(v[512:], cs)
+        ref_r = torch.from_numpy(rot).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(rc.view(np.uint16), ref_r)
+        v41 = orc.encode_entry(v, ik, cs)
+        assert np.array_equal(ic, v41[4]) and np.array_equal(isc, v41[5])
+
+
+def test_attention_over_one_v4_entry_returns_its_latent(orc):
+    """Attention over a single V4 entry (no window, no sink): the output is that
+    entry's latent exactly, whatever the query -- values on the E4M3 grid times a
+    power of two survive the encoding unchanged."""
+    grid = torch.arange(0, 120, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    rng = np.random.default_rng(44)
+    lat = (rng.choice(grid, 512) * rng.choice([-1.0, 1.0], 512)).astype(np.float32)
+    lat[::32] = 448.0  # each block's amax: the scale is exactly 1
+    v = np.concatenate([lat * np.float32(2.0 ** -3), rng.standard_normal(64).astype(np.float32)])
+    c = orc.Cache(4, entry_format=orc.ENTRY_FP8)
+    c.swa_codes[:] = 0
+    rec = orc.encode_entry_v4(v, np.ones(128, np.float32), orc.rope_cs(1e4, 0))
+    for arr, val in zip((c.lat_codes, c.lat_scales, c.rope_codes, c.rope_scales, c.idx_codes, c.idx_scales), rec):
+        arr[0] = val
+    c.n_tokens = c.n_entries = 1
+    q = (rng.standard_normal((4, 576)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    out, lse = orc.sparse_attn(c, q, np.array([0, -1], np.int32), 1, 0.05,
+                               swa_codes=np.zeros((0, 576), np.uint8), swa_scales=np.zeros((0, 18), np.uint8))
+    for h in range(4):
+        assert np.array_equal(out[h], lat * np.float32(2.0 ** -3))
