@@ -243,13 +243,22 @@ def decode_step_bytes(B, T, H, H_I, k, swa_dtype):
 class FullDecode:
     """Full-layer decode on a batch: caches built through csa2_kv_append."""
 
-    def __init__(self, W, n_steps, device):
+    def __init__(self, W, n_steps, device, page_entries=None):
         from fp4_compressed_sparse_gb300 import csa2
         self.csa2 = csa2
         self.W = W
         B, ctx = W.batch, W.context
         self.cap = ctx + n_steps + 8
-        self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
+        if page_entries:
+            # paged: the sequences' pages spread over the pool in a seeded random order
+            self.cap = -(-self.cap // page_entries) * page_entries
+            max_pages = self.cap // page_entries
+            g = torch.Generator().manual_seed(W.seed + 77)
+            table = torch.randperm(B * max_pages, generator=g).to(torch.int32).view(B, max_pages)
+            self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype, page_entries=page_entries,
+                                    block_table=table)
+        else:
+            self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
         self.rope = csa2.rope_table(W.theta, self.cap + 8)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         chunk = 8192
@@ -467,6 +476,9 @@ def run_ours(args):
         # the same run: the 1 M-context decoder group (config of 8 sequences x
         # 1,048,576 tokens) and the chunked prefill, with the FP4 tensor peak
         del bench, graphs
+        torch.cuda.empty_cache()
+        # the same step on a paged cache (256-entry pages in shuffled order)
+        line["paged"] = measure_paged(W, max(10, min(args.steps, 30)), 3, dev, 256)
         torch.cuda.empty_cache()
         fp4 = measure_fp4_peak(dev)
         line["fp4_peak"] = fp4
@@ -736,6 +748,37 @@ class PrefillBench:
         W = self.W
         self.csa2.prefill_chunk(self.cache, 0, self.rows + [self.ba, self.bb], self.rope, self.q_idx, self.w, self.q,
                                 W.topk, W.sm_scale, self.idx, self.out, self.lse, self.ws, err=self.err)
+
+
+def measure_paged(W, steps, warmup, dev, page_entries):
+    """The headline decode step on a paged cache (pages of page_entries entries in
+    a shuffled order over the pool): `steps` CUDA-graph steps, L2 flushed between."""
+    bench = FullDecode(W, warmup + steps, dev, page_entries=page_entries)
+    flush = L2Flush(dev)
+    for s in range(warmup):
+        flush()
+        bench.step(s)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            bench.step(warmup + i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        graphs[i].replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} in the paged steps")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del graphs, bench
+    return {"workload": W.name, "page_entries": page_entries, "page_order": "seeded random permutation of the pool",
+            "steps": steps, "ms_per_step": round(ms, 4), "value": round(W.batch / (ms / 1e3), 2), "unit": UNIT}
 
 
 def measure_group(W, steps, warmup, dev, variant_layers=None):

@@ -18,11 +18,12 @@ ERR_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_RAN
              5: "ERR_UNSUPPORTED", 6: "ERR_CUDA", 7: "ERR_WORKSPACE"}
 DEVERR_CAPACITY, DEVERR_INDEX, DEVERR_NAN, DEVERR_ROPE, DEVERR_TIMEOUT, DEVERR_INEXACT = 1, 2, 4, 8, 16, 32
 SWA_BF16, SWA_MXFP8 = 0, 1
+ENTRY_FP4, ENTRY_FP8 = 0, 1
 IN_F32, IN_BF16 = 0, 1
 D_LATENT, D_ROPE, D_QK, D_INDEX, D_CMP, WINDOW = 512, 64, 576, 128, 704, 128
 
 EXPORTS = [
-    "csa2_cache_plane_bytes", "csa2_paged_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
+    "csa2_cache_plane_bytes", "csa2_paged_plane_bytes", "csa2_entry_plane_bytes", "csa2_rope_table", "csa2_kv_append", "csa2_index_score_workspace_size",
     "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mask_to_pool", "csa2_mxf4_peak_launch",
@@ -47,7 +48,7 @@ class CacheStruct(ctypes.Structure):
         ("swa_codes", ctypes.c_void_p), ("swa_scales", ctypes.c_void_p),
         ("cmp_buf", ctypes.c_void_p), ("n_tokens", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p), ("page_entries", ctypes.c_int32), ("max_pages", ctypes.c_int32),
-        ("n_pages", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("n_pages", ctypes.c_int32), ("entry_format", ctypes.c_int32),
     ]
 
 
@@ -77,6 +78,7 @@ def load() -> ctypes.CDLL:
     sig = {
         "csa2_cache_plane_bytes": (sz, [i32, i32, i32, i32]),
         "csa2_paged_plane_bytes": (sz, [i32, i32, i32]),
+        "csa2_entry_plane_bytes": (sz, [i32, i32]),
         "csa2_rope_table": (i32, [f64, i64, vp]),
         "csa2_kv_append": (i32, [vp, vp, vp, i32, vp, vp, i64, i32, vp, vp, vp]),
         "csa2_index_score_workspace_size": (sz, [i32, i32]),
@@ -133,12 +135,13 @@ class Cache:
     max_pages and the table is the identity."""
 
     def __init__(self, batch, capacity, ratio=1, swa_dtype=SWA_MXFP8, device="cuda", page_entries=None,
-                 n_pages=None, block_table=None):
+                 n_pages=None, block_table=None, entry_format=ENTRY_FP4):
         L = load()
         self.batch, self.capacity, self.ratio, self.swa_dtype = batch, capacity, ratio, swa_dtype
-        self.page_entries = page_entries
+        self.page_entries, self.entry_format = page_entries, entry_format
         nb = [L.csa2_cache_plane_bytes(batch, capacity, p, swa_dtype) for p in range(10)]
-        u8 = lambda n: torch.zeros(n, dtype=torch.uint8, device=device)
+        eb = [L.csa2_entry_plane_bytes(entry_format, p) for p in range(4)]  # bytes per entry, planes 0..3
+        u8 = lambda n: torch.zeros(max(n, 16), dtype=torch.uint8, device=device)[:n]
         if page_entries:
             assert capacity % page_entries == 0 and page_entries % 128 == 0
             self.max_pages = capacity // page_entries
@@ -147,18 +150,18 @@ class Cache:
                 block_table = torch.arange(batch * self.max_pages, dtype=torch.int32).view(batch, self.max_pages)
             self.block_table = block_table.to(device=device, dtype=torch.int32).contiguous()
             pb = [L.csa2_paged_plane_bytes(self.n_pages, page_entries, p) for p in range(6)]
-            rows, lead = self.n_pages * page_entries, (self.n_pages * page_entries,)
+            rows = self.n_pages * page_entries
             self.idx_tiles = rows // 128
-            planes = [u8(pb[0]).view(*lead, 256), u8(pb[1]).view(*lead, 32), u8(pb[2]).view(*lead, 32),
-                      u8(pb[3]).view(*lead, 4), u8(pb[4]).view(self.idx_tiles, 8192), u8(pb[5]).view(self.idx_tiles, 512)]
+            planes = [u8(rows * eb[p]).view(rows, eb[p]) if eb[p] else None for p in range(4)] + \
+                     [u8(pb[4]).view(self.idx_tiles, 8192), u8(pb[5]).view(self.idx_tiles, 512)]
         else:
             self.max_pages = self.n_pages = 0
             self.block_table = None
             # tile-major indexer planes (see csa2_cache in csa2.h)
             self.idx_tiles = (capacity + 127) // 128
-            planes = [u8(nb[0]).view(batch, capacity, 256), u8(nb[1]).view(batch, capacity, 32),
-                      u8(nb[2]).view(batch, capacity, 32), u8(nb[3]).view(batch, capacity, 4),
-                      u8(nb[4]).view(batch, self.idx_tiles, 8192), u8(nb[5]).view(batch, self.idx_tiles, 512)]
+            n = batch * capacity
+            planes = [u8(n * eb[p]).view(batch, capacity, eb[p]) if eb[p] else None for p in range(4)] + \
+                     [u8(nb[4]).view(batch, self.idx_tiles, 8192), u8(nb[5]).view(batch, self.idx_tiles, 512)]
         (self.lat_codes, self.lat_scales, self.rope_codes, self.rope_scales, self.idx_codes,
          self.idx_scales) = planes
         sw = 576 if swa_dtype == SWA_MXFP8 else 1152
@@ -170,11 +173,11 @@ class Cache:
         self.struct = CacheStruct(
             batch, capacity, ratio, swa_dtype,
             self.lat_codes.data_ptr(), self.lat_scales.data_ptr(), self.rope_codes.data_ptr(),
-            self.rope_scales.data_ptr(), self.idx_codes.data_ptr(), self.idx_scales.data_ptr(),
-            self.swa_codes.data_ptr(), self.swa_scales.data_ptr(),
+            self.rope_scales.data_ptr() if self.rope_scales is not None else None, self.idx_codes.data_ptr(),
+            self.idx_scales.data_ptr(), self.swa_codes.data_ptr(), self.swa_scales.data_ptr(),
             self.cmp_buf.data_ptr() if self.cmp_buf is not None else None, self.n_tokens.data_ptr(),
             self.block_table.data_ptr() if self.block_table is not None else None, page_entries or 0,
-            self.max_pages, self.n_pages, 0)
+            self.max_pages, self.n_pages, entry_format)
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -204,8 +207,10 @@ class Cache:
         return codes[:, :self.capacity], scales[:, :self.capacity]
 
     def entry_bytes(self):
-        """Bytes of one stored entry (main 288 + sidecar 36 + indexer 68)."""
-        return 256 + 32 + 32 + 4 + 64 + 4
+        """Bytes of one stored entry: main record + RoPE part + indexer key (68): 288 + 36 + 68
+        for the V4.1 FP4 format, 528 + 128 + 68 for the V4 format."""
+        L = load()
+        return sum(L.csa2_entry_plane_bytes(self.entry_format, p) for p in range(6))
 
 
 def rope_table(theta: float, n_pos: int, device="cuda") -> torch.Tensor:

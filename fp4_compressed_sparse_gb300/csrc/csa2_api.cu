@@ -110,10 +110,12 @@ csa2_status check_cache(const csa2_cache *c) {
   REQUIRE(c->ratio == 1 || c->ratio == 2, CSA2_ERR_RANGE, "cache ratio %d (must be 1 or 2)", c->ratio);
   REQUIRE(c->swa_dtype == CSA2_SWA_BF16 || c->swa_dtype == CSA2_SWA_MXFP8, CSA2_ERR_RANGE, "swa_dtype %d",
           c->swa_dtype);
+  REQUIRE(c->entry_format == CSA2_ENTRY_FP4 || c->entry_format == CSA2_ENTRY_FP8, CSA2_ERR_RANGE,
+          "entry_format %d", c->entry_format);
   REQUIRE_PTR(c->lat_codes);
   REQUIRE_PTR(c->lat_scales);
   REQUIRE_PTR(c->rope_codes);
-  REQUIRE_PTR(c->rope_scales);
+  if (c->entry_format == CSA2_ENTRY_FP4) REQUIRE_PTR(c->rope_scales);
   REQUIRE_PTR(c->idx_codes);
   REQUIRE_PTR(c->idx_scales);
   REQUIRE_PTR(c->swa_codes);
@@ -140,10 +142,10 @@ csa2_cache seq_view(const csa2_cache &c, int seq) {
     v.block_table += static_cast<size_t>(seq) * c.max_pages;  // the entry planes are the shared page pool
   } else {
     const size_t e = static_cast<size_t>(seq) * c.capacity;
-    v.lat_codes += e * 256;
-    v.lat_scales += e * 32;
-    v.rope_codes += e * 32;
-    v.rope_scales += e * 4;
+    v.lat_codes += e * csa2_entry_plane_bytes(c.entry_format, 0);
+    v.lat_scales += e * csa2_entry_plane_bytes(c.entry_format, 1);
+    v.rope_codes += e * csa2_entry_plane_bytes(c.entry_format, 2);
+    if (v.rope_scales) v.rope_scales += e * csa2_entry_plane_bytes(c.entry_format, 3);
     v.idx_codes += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileCodeBytes;
     v.idx_scales += static_cast<size_t>(seq) * csa2::idx_tiles(c.capacity) * csa2::kIdxTileScaleBytes;
   }
@@ -245,6 +247,14 @@ size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane, in
     case 8: return static_cast<size_t>(batch) * 4 * 4 * csa2::kDcmp * sizeof(float);
     case 9: return static_cast<size_t>(batch) * sizeof(int64_t);
   }
+  return 0;
+}
+
+size_t csa2_entry_plane_bytes(int32_t entry_format, int32_t plane) {
+  static const size_t fp4[6] = {256, 32, 32, 4, 64, 4}, fp8[6] = {512, 16, 128, 0, 64, 4};
+  if (plane < 0 || plane > 5) return 0;
+  if (entry_format == CSA2_ENTRY_FP4) return fp4[plane];
+  if (entry_format == CSA2_ENTRY_FP8) return fp8[plane];
   return 0;
 }
 
@@ -476,6 +486,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
   a.rope_codes = cache->rope_codes;
   a.rope_scales = cache->rope_scales;
   a.map = csa2::entry_map(*cache);
+  a.entry_format = cache->entry_format;
   a.cap = cache->capacity;
   a.ratio = cache->ratio;
   a.n_tokens = cache->n_tokens;
@@ -650,6 +661,7 @@ csa2_status csa2_prefill_chunk(const csa2_cache *cache, int32_t seq, const csa2_
     aa.rope_codes = v.rope_codes;
     aa.rope_scales = v.rope_scales;
     aa.map = csa2::entry_map(v);
+    aa.entry_format = cache->entry_format;
     aa.cap = cache->capacity;
     aa.ratio = 2;
     aa.n_tokens = v.n_tokens;

@@ -13,6 +13,8 @@
 //   producer warps (4)  gather 32 entries at a time and dequantise them into a
 //                       two-stage fp16 ring: E2M1 pairs by cvt.f16x2.e2m1x2, times
 //                       the E4M3 scale (exact: at most 6 significant bits, >= 2^-10);
+//                       V4-format entries (E4M3 latent with E8M0 scales, bf16
+//                       RoPE dims) like the 8-bit / bf16 window entries;
 //                       window MXFP8 / bf16 entries, scaled by a power of two
 //                       2^-sigma_j only if they would not fit fp16
 //   consumer warps      S = Q K^T (mma.sync m16n8k16 f16, fp32 accumulate; a
@@ -330,9 +332,10 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     int kind = 0;
     Fp4Raw raw;
     int32_t sel_next = -1;
+    const bool fp8 = a.entry_format == CSA2_ENTRY_FP8;
     if (nchunks > 0) {
       kind = entry_kind(a, seq, sm.chunk_id[0] * kE + e, kpad, sel_of(0), qpos, T, ntok, lin_base, src);
-      if (kind == 1) load_fp4(a, src, q4, raw);
+      if (kind == 1 && !fp8) load_fp4(a, src, q4, raw);
       if (nchunks > 1) sel_next = sel_of(1);
     }
     bool dead = false;
@@ -342,7 +345,61 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       if (!dead) {
         uint4 *dst = reinterpret_cast<uint4 *>(&sm.kv[st][e][0]);  // 16-dim unit u at dst[2u], dst[2u+1]
         float sig = 0.0f;
-        if (kind == 1) {
+        if (kind == 1 && fp8) {
+          // V4 entry: 512 E4M3 codes with an E8M0 per 32, then 64 bf16 RoPE dims;
+          // scaled by a power of two 2^-sigma only if they would not fit fp16
+          const uint8_t *lc = a.lat_codes + src * 512;
+          const uint4 sv = *reinterpret_cast<const uint4 *>(a.lat_scales + src * 16);
+          const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+          uint32_t mx = 0;
+#pragma unroll
+          for (int g = 0; g < 16; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+          const uint4 *rc = reinterpret_cast<const uint4 *>(a.rope_codes + src * 128 + 32 * q4);
+          const uint4 r0 = rc[0], r1 = rc[1];
+          const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+          float ramax = 0.0f;
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            ramax = fmaxf(ramax, fmaxf(fabsf(__uint_as_float(rw[b] << 16)), fabsf(__uint_as_float(rw[b] & 0xFFFF0000u))));
+          ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 1));
+          ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 2));
+          // latent values < 448 * 2^(mx-127), RoPE values <= ramax: both below 2^16 after 2^-sigma
+          const int s_lat = static_cast<int>(mx) - 134;
+          const int s_rope = ramax > 0.0f ? floor_log2f(ramax) - 14 : 0;
+          const int sigma = min(15, max(0, max(s_lat, s_rope)));
+#pragma unroll 1
+          for (int i = 0; i < 8; ++i) {
+            const int u = q4 + 4 * i;  // 16 latent dims, half of scale block u / 2
+            const uint4 cw = reinterpret_cast<const uint4 *>(lc)[u];
+            const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
+            const uint32_t swu = wi == 0 ? sv.x : wi == 1 ? sv.y : wi == 2 ? sv.z : sv.w;
+            const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
+            const int kx = sc - 127 - sigma;
+            const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
+            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+              o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
+              o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
+            }
+            dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          {  // RoPE unit 32 + q4: 16 bf16 dims
+            const float inv = pow2f(-sigma);
+            uint32_t o[8];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+              __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(rw[b] << 16), inv),
+                                             __fmul_rn(__uint_as_float(rw[b] & 0xFFFF0000u), inv));
+              o[b] = *reinterpret_cast<uint32_t *>(&t2);
+            }
+            dst[2 * (32 + q4)] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[2 * (32 + q4) + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          sig = pow2f(sigma);
+        } else if (kind == 1) {
           // FP4 entry: unit u < 32 = latent dims 16u.. (8 code bytes, scale u), u = 32 + q4 the RoPE group q4
           const uint32_t sw[8] = {raw.s0.x, raw.s0.y, raw.s0.z, raw.s0.w, raw.s1.x, raw.s1.y, raw.s1.z, raw.s1.w};
 #pragma unroll
@@ -440,7 +497,7 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       tc::mbar_arrive(&sm.full[st]);
       if (c + 1 < nchunks) {
         kind = entry_kind(a, seq, sm.chunk_id[c + 1] * kE + e, kpad, sel_next, qpos, T, ntok, lin_base, src);
-        if (kind == 1) load_fp4(a, src, q4, raw);
+        if (kind == 1 && !fp8) load_fp4(a, src, q4, raw);
         if (c + 2 < nchunks) sel_next = sel_of(c + 2);
       }
     }

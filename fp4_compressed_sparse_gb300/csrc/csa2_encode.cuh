@@ -9,7 +9,9 @@ namespace csa2 {
 
 // Encode entry `e` of sequence b from an fp32 row in shared memory:
 // row[0:576] = main vector (RoPE dims 512..575 not yet rotated), row[576:704] = indexer key.
-// A paged cache whose table names a page outside the pool gets the INDEX bit.
+// The cache's entry format decides the record: V4.1 FP4 (the 288 B record and
+// the 36 B RoPE sidecar) or V4 (MXFP8 latent, bf16 RoPE dims).  A paged cache
+// whose table names a page outside the pool gets the INDEX bit.
 __device__ __forceinline__ void warp_encode_entry(const csa2_cache &c, int b, int64_t e, const float *row, const float *cs,
                                                   int lane, int32_t *err) {
   const EntryMap map = entry_map(c);
@@ -20,9 +22,41 @@ __device__ __forceinline__ void warp_encode_entry(const csa2_cache &c, int b, in
   }
   const size_t ent = static_cast<size_t>(pe);
   float x[32];
+  uint32_t sc;
+  if (c.entry_format == CSA2_ENTRY_FP8) {
+    // V4 entry: latent block `lane` (32 dims) in MXFP8, RoPE dims rotated into bf16
+    if (lane < 16) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = row[32 * lane + i];
+      uint32_t w[8];
+      quant_mxfp8_32(x, w, &sc);
+      uint4 *dst = reinterpret_cast<uint4 *>(c.lat_codes + ent * 512 + 32 * lane);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      c.lat_scales[ent * 16 + lane] = static_cast<uint8_t>(sc);
+    } else if (lane < 20) {
+      __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(c.rope_codes + ent * 128);
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const int pair = 8 * (lane - 16) + p;
+        float a = row[kLat + 2 * pair], bb = row[kLat + 2 * pair + 1];
+        rope_pair(a, bb, cs[2 * pair], cs[2 * pair + 1]);
+        h[2 * pair] = __float2bfloat16_rn(a);
+        h[2 * pair + 1] = __float2bfloat16_rn(bb);
+      }
+    } else if (lane < 24) {
+      const int blk = lane - 20;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = row[kDqk + 32 * blk + i];
+      uint32_t w[4];
+      quant_mxfp4_32(x, w, &sc);
+      *reinterpret_cast<uint4 *>(c.idx_codes + idx_code_at(pt, e % kIdxTile, blk)) = make_uint4(w[0], w[1], w[2], w[3]);
+      c.idx_scales[idx_scale_at(pt, e % kIdxTile) + blk] = static_cast<uint8_t>(sc);
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) x[i] = row[16 * lane + i];
-  uint32_t sc;
   uint64_t packed = quant_nvfp4_16(x, &sc);
   reinterpret_cast<uint2 *>(c.lat_codes + ent * 256)[lane] =
       make_uint2(static_cast<uint32_t>(packed), static_cast<uint32_t>(packed >> 32));
@@ -143,18 +177,44 @@ __device__ __forceinline__ void block_encode_entry(const csa2_cache &c, int b, i
   }
   const size_t ent = static_cast<size_t>(pe);
   uint32_t sc;
-  {  // latent: thread t has dims 2t, 2t+1 (group t / 8)
-    const float2 v = reinterpret_cast<const float2 *>(row)[t];
-    const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
-    c.lat_codes[ent * 256 + t] = static_cast<uint8_t>(byte);
-    if ((t & 7) == 0) c.lat_scales[ent * 32 + (t >> 3)] = static_cast<uint8_t>(sc);
+  if (c.entry_format == CSA2_ENTRY_FP8) {
+    // V4 entry: latent MXFP8 block g (32 dims) on warp g % 8, one dim per lane
+    const int warp = t >> 5;
+    for (int g = warp; g < 16; g += kEncThreads / 32) {
+      const float x = row[32 * g + lane];
+      float amax = fabsf(x);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      uint32_t code = 0;
+      sc = 0;
+      if (amax != 0.0f) {
+        int ex = floor_log2f(amax) - 8;
+        ex = max(-127, min(127, ex));
+        code = e4m3_code(__fmul_rn(x, pow2f(-ex)));
+        sc = static_cast<uint32_t>(ex + 127);
+      }
+      uint32_t w = code << (8 * (lane & 3));  // four lanes' bytes into one word
+      w |= __shfl_xor_sync(0xffffffffu, w, 1);
+      w |= __shfl_xor_sync(0xffffffffu, w, 2);
+      if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(c.lat_codes + ent * 512 + 32 * g)[lane >> 2] = w;
+      if (lane == 0) c.lat_scales[ent * 16 + g] = static_cast<uint8_t>(sc);
+    }
+    if (t < 64) reinterpret_cast<__nv_bfloat16 *>(c.rope_codes + ent * 128)[t] = __float2bfloat16_rn(rot[t]);
+  } else {
+    {  // latent: thread t has dims 2t, 2t+1 (group t / 8)
+      const float2 v = reinterpret_cast<const float2 *>(row)[t];
+      const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
+      c.lat_codes[ent * 256 + t] = static_cast<uint8_t>(byte);
+      if ((t & 7) == 0) c.lat_scales[ent * 32 + (t >> 3)] = static_cast<uint8_t>(sc);
+    }
+    if (t < 32) {  // RoPE sidecar: rotated dims 2t, 2t+1 (group t / 8)
+      const float2 v = reinterpret_cast<const float2 *>(rot)[t];
+      const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
+      c.rope_codes[ent * 32 + t] = static_cast<uint8_t>(byte);
+      if ((t & 7) == 0) c.rope_scales[ent * 4 + (t >> 3)] = static_cast<uint8_t>(sc);
+    }
   }
-  if (t < 32) {  // RoPE sidecar: rotated dims 2t, 2t+1 (group t / 8)
-    const float2 v = reinterpret_cast<const float2 *>(rot)[t];
-    const uint32_t byte = nvfp4_pair(v.x, v.y, &sc);
-    c.rope_codes[ent * 32 + t] = static_cast<uint8_t>(byte);
-    if ((t & 7) == 0) c.rope_scales[ent * 4 + (t >> 3)] = static_cast<uint8_t>(sc);
-  } else if (t < 64) {  // indexer key, MXFP4: lane l has dims 4l..4l+3 (block l / 8)
+  if (t >= 32 && t < 64) {  // indexer key, MXFP4: lane l has dims 4l..4l+3 (block l / 8)
     const float4 v = reinterpret_cast<const float4 *>(row + kDqk)[lane];
     const float x[4] = {v.x, v.y, v.z, v.w};
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));

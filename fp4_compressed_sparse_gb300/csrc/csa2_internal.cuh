@@ -111,6 +111,7 @@ struct AttnArgs {
   int cache_seq;              // -1: row = sequence
   const uint8_t *lat_codes, *lat_scales, *rope_codes, *rope_scales;
   EntryMap map;               // where a sequence's entries live (dense or paged)
+  int entry_format;           // CSA2_ENTRY_FP4 or CSA2_ENTRY_FP8
   int64_t cap;
   int ratio;
   const int64_t *n_tokens;    // [batch]

@@ -63,6 +63,17 @@ typedef enum csa2_status {
 #define CSA2_SWA_BF16 0  /* 576 bf16 values, 1,152 B per token                         */
 #define CSA2_SWA_MXFP8 1 /* 576 E4M3 codes + 18 E8M0 scales (one per 32), 594 B/token */
 
+/* main-entry formats of the global cache (csa2_cache.entry_format):
+ *   CSA2_ENTRY_FP4: V4.1, the 288 B record: lat_codes 256 B (E2M1 x 512),
+ *     lat_scales 32 B (E4M3 per 16); RoPE sidecar rope_codes 32 B, rope_scales 4 B.
+ *   CSA2_ENTRY_FP8: V4 ([P5] §2.3.4: FP8 for the entry except the RoPE dims,
+ *     which stay BF16), for comparison: lat_codes 512 B (E4M3 x 512), lat_scales
+ *     16 B (one E8M0 per 32 latent dims, e = floor(log2 amax) - 8, as the 8-bit
+ *     window), rope_codes 128 B (the 64 rotated RoPE dims in bf16), rope_scales
+ *     unused (may be NULL): 656 B.  The indexer key is MXFP4 (68 B) in both. */
+#define CSA2_ENTRY_FP4 0
+#define CSA2_ENTRY_FP8 1
+
 /* input element types for csa2_kv_append */
 #define CSA2_IN_F32 0
 #define CSA2_IN_BF16 1
@@ -139,7 +150,7 @@ typedef struct csa2_cache {
   int32_t page_entries;       /* entries per page: a multiple of 128 */
   int32_t max_pages;          /* pages a sequence may use: capacity / page_entries */
   int32_t n_pages;            /* physical pages in the entry planes */
-  int32_t reserved;
+  int32_t entry_format;       /* CSA2_ENTRY_FP4 (V4.1) or CSA2_ENTRY_FP8 (V4) */
 } csa2_cache;
 
 /* Ratio-2 compression inputs ([P5] §2.3.1 "압축된 Key-Value Entry"): per token
@@ -155,6 +166,10 @@ size_t csa2_cache_plane_bytes(int32_t batch, int32_t capacity, int32_t plane /* 
                               int32_t swa_dtype);
 /* Bytes of entry plane 0..5 in the paged layout (n_pages pages of page_entries). */
 size_t csa2_paged_plane_bytes(int32_t n_pages, int32_t page_entries, int32_t plane);
+/* Bytes one entry takes in plane 0..5 for an entry format (0 for an unknown
+ * format or plane; the dense and paged plane sizes above are for
+ * CSA2_ENTRY_FP4, scale them by this for CSA2_ENTRY_FP8). */
+size_t csa2_entry_plane_bytes(int32_t entry_format, int32_t plane);
 
 /*
  * csa2_rope_table (host): cos/sin table for the 64 RoPE dims, rope_cs[pos][i][2]

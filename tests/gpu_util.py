@@ -15,16 +15,16 @@ def u16(t):
 
 
 def build_r1(orc, batch, n_tokens, swa_dtype, seed, chunks=None, in_bf16=False, cap=None,
-             theta=10000.0, rope=None, kv_scale=1.0):
+             theta=10000.0, rope=None, kv_scale=1.0, entry_format=0):
     """Append n_tokens per sequence (in the given chunk sizes) on the GPU and in the
     oracle; the latent rows are multiplied by kv_scale (a power of two).
     Returns (gpu cache, [oracle caches], rope table, err word)."""
     cap = cap or n_tokens + 8
-    c = csa2.Cache(batch, cap, ratio=1, swa_dtype=swa_dtype)
+    c = csa2.Cache(batch, cap, ratio=1, swa_dtype=swa_dtype, entry_format=entry_format)
     rope = rope if rope is not None else csa2.rope_table(theta, cap + 8)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     chunks = chunks or [n_tokens]
-    oc = [orc.Cache(cap, swa_dtype=swa_dtype) for _ in range(batch)]
+    oc = [orc.Cache(cap, swa_dtype=swa_dtype, entry_format=entry_format) for _ in range(batch)]
     t0 = 0
     for n in chunks:
         kv = torch.stack([wl.token_rows(seed, wl.S_KV, b, t0, n, 576) for b in range(batch)]) * kv_scale
@@ -44,18 +44,18 @@ def cmp_rows(seed, seq, start, n):
 
 
 def build_r2(orc, batch, n_tokens, swa_dtype, seed, chunks=None, cap=None, theta=10000.0,
-             bias_scale=0.5, dbg=False):
+             bias_scale=0.5, dbg=False, entry_format=0):
     """Ratio-2 appends on both sides.  Returns (gpu cache, oracle caches, rope, err,
     biases, gpu dbg rows per call, oracle dbg rows)."""
     cap = cap or n_tokens // 2 + 8
-    c = csa2.Cache(batch, cap, ratio=2, swa_dtype=swa_dtype)
+    c = csa2.Cache(batch, cap, ratio=2, swa_dtype=swa_dtype, entry_format=entry_format)
     rope = csa2.rope_table(theta, 2 * cap + 16)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     g = torch.Generator().manual_seed(seed + 991)
     ba = (torch.randn((2, 704), generator=g) * bias_scale).float()
     bb = (torch.randn((2, 704), generator=g) * bias_scale).float()
     chunks = chunks or [n_tokens]
-    oc = [orc.Cache(cap, swa_dtype=swa_dtype, ratio=2) for _ in range(batch)]
+    oc = [orc.Cache(cap, swa_dtype=swa_dtype, ratio=2, entry_format=entry_format) for _ in range(batch)]
     t0 = 0
     gdbg, odbg = [], [[] for _ in range(batch)]
     for n in chunks:
@@ -77,6 +77,8 @@ def assert_cache_equal(c, oc, n_entries, check_swa=True):
     planes = {"idx_codes": ic, "idx_scales": isc}
     for b, o in enumerate(oc):
         for name in ("lat_codes", "lat_scales", "rope_codes", "rope_scales", "idx_codes", "idx_scales"):
+            if getattr(c, name, None) is None and name not in planes:
+                continue  # a plane the entry format does not use
             g = planes.get(name, getattr(c, name, None))[b, :n_entries].cpu().numpy()
             ref = getattr(o, name)[:n_entries]
             bad = np.argwhere(g != ref)
