@@ -243,7 +243,7 @@ def decode_step_bytes(B, T, H, H_I, k, swa_dtype):
 class FullDecode:
     """Full-layer decode on a batch: caches built through csa2_kv_append."""
 
-    def __init__(self, W, n_steps, device, page_entries=None):
+    def __init__(self, W, n_steps, device, page_entries=None, entry_format=0):
         from fp4_compressed_sparse_gb300 import csa2
         self.csa2 = csa2
         self.W = W
@@ -256,9 +256,9 @@ class FullDecode:
             g = torch.Generator().manual_seed(W.seed + 77)
             table = torch.randperm(B * max_pages, generator=g).to(torch.int32).view(B, max_pages)
             self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype, page_entries=page_entries,
-                                    block_table=table)
+                                    block_table=table, entry_format=entry_format)
         else:
-            self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype)
+            self.cache = csa2.Cache(B, self.cap, ratio=1, swa_dtype=W.swa_dtype, entry_format=entry_format)
         self.rope = csa2.rope_table(W.theta, self.cap + 8)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         chunk = 8192
@@ -479,6 +479,9 @@ def run_ours(args):
         torch.cuda.empty_cache()
         # the same step on a paged cache (256-entry pages in shuffled order)
         line["paged"] = measure_paged(W, max(10, min(args.steps, 30)), 3, dev, 256)
+        torch.cuda.empty_cache()
+        # the V4 cache formats at the same configuration
+        line["formats"] = measure_formats(W, max(10, min(args.steps, 30)), 3, dev)
         torch.cuda.empty_cache()
         fp4 = measure_fp4_peak(dev)
         line["fp4_peak"] = fp4
@@ -748,6 +751,91 @@ class PrefillBench:
         W = self.W
         self.csa2.prefill_chunk(self.cache, 0, self.rows + [self.ba, self.bb], self.rope, self.q_idx, self.w, self.q,
                                 W.topk, W.sm_scale, self.idx, self.out, self.lse, self.ws, err=self.err)
+
+
+def _time_steps(bench, steps, warmup, dev, step_fn=None):
+    """Mean ms of `steps` CUDA-graph steps of a bench object (warm-up eager, L2
+    flushed before every timed step, events around each)."""
+    step_fn = step_fn or bench.step
+    flush = L2Flush(dev)
+    for s in range(warmup):
+        flush()
+        step_fn(s)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step_fn(warmup + i)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        graphs[i].replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    if bench.err.item() != 0:
+        raise RuntimeError(f"device error word {bench.err.item()} in the timed steps")
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+class HcaDecode:
+    """A heavily compressed attention layer in the V4 format, for the comparison of
+    cache formats ([P5] §2.3.2: one entry per m' = 128 tokens, no overlap, attention
+    over every compressed entry, no indexer): a cache of context/128 V4-format
+    entries (seeded N(0,1) rows standing for the compressed entries), and each step
+    attends over all of them plus the 128-token window through the sparse-attention
+    call with every entry selected."""
+
+    def __init__(self, W, n_steps, device, m=128):
+        from fp4_compressed_sparse_gb300 import csa2
+        self.csa2, self.W = csa2, W
+        B, n = W.batch, W.context // m
+        self.n = n
+        self.cache = csa2.Cache(B, n + 8, ratio=1, swa_dtype=W.swa_dtype, entry_format=csa2.ENTRY_FP8)
+        rope = csa2.rope_table(W.theta, n + 16)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        kv = torch.stack([W.kv(b, 0, n, device=device) for b in range(B)])
+        ik = torch.stack([W.ik(b, 0, n, device=device) for b in range(B)])
+        csa2.kv_append(self.cache, kv, ik, rope, err=self.err)
+        del kv, ik
+        self.idx = torch.arange(n, dtype=torch.int32, device=device).repeat(B, 1).contiguous()
+        self.q = [W.q(s, 7, device=device) for s in range(n_steps)]
+        self.q_pos = torch.full((B,), n, dtype=torch.int64, device=device)
+        self.out = torch.empty((B, W.heads, 512), device=device)
+        self.lse = torch.empty((B, W.heads), device=device)
+        self.ws = csa2.attn_workspace(B, W.heads, n)
+
+    def step(self, s):
+        self.csa2.sparse_attn_decode(self.cache, self.q[s], self.q_pos, self.idx, self.out, self.lse, self.ws,
+                                     self.W.sm_scale, err=self.err)
+
+
+def measure_formats(W, steps, warmup, dev):
+    """The cache formats compared at the headline configuration ([P5] §2.3.2,
+    §2.3.4; [P3] per-token global KV by generation): the Full-layer decode step
+    with V4.1 FP4 entries and with V4 FP8 + bf16-RoPE entries (same indexer keys,
+    scan and selection), and an HCA-style layer (m' = 128, dense over its entries)."""
+    from fp4_compressed_sparse_gb300 import csa2
+    out = {}
+    for name, fmt in (("v41_fp4", csa2.ENTRY_FP4), ("v4_fp8", csa2.ENTRY_FP8)):
+        bench = FullDecode(W, warmup + steps, dev, entry_format=fmt)
+        ms = _time_steps(bench, steps, warmup, dev)
+        out[name] = {"ms_per_step": round(ms, 4), "tokens_per_s": round(W.batch / (ms / 1e3), 2),
+                     "entry_bytes": bench.cache.entry_bytes(),
+                     "selected_entry_bytes": bench.cache.entry_bytes() - 68}
+        del bench
+        torch.cuda.empty_cache()
+    hca = HcaDecode(W, warmup + steps, dev)
+    ms = _time_steps(hca, steps, warmup, dev)
+    out["hca_m128_fp8"] = {"ms_per_step": round(ms, 4), "entries_per_sequence": hca.n,
+                           "entry_bytes": hca.cache.entry_bytes() - 68,
+                           "note": "attention over every compressed entry + the window; no indexer"}
+    del hca
+    out["config"] = f"{W.name}: batch {W.batch}, context {W.context}, {W.heads} heads, top-{W.topk}"
+    return out
 
 
 def measure_paged(W, steps, warmup, dev, page_entries):

@@ -43,6 +43,7 @@ def test_v4_append_r2_bitexact(orc):
     (32, 300, 64, 128, 1.0, True),        # 4 CTAs per row
     (2, 500, 64, 256, 2.0 ** 18, False),  # latent and RoPE values beyond fp16: a power-of-two scale per entry
     (1, 90, 16, 64, 1.0, True),           # window shorter than 128
+    (2, 600, 64, 599, 1.0, False),        # every visible entry selected: the dense (HCA-style) layer
 ])
 def test_v4_sparse_attn(orc, B, T, H, k, kv_scale, use_sink):
     c, oc, _, err = build_r1(orc, B, T, csa2.SWA_MXFP8, seed=103 + B, kv_scale=kv_scale, entry_format=FP8)
