@@ -864,9 +864,20 @@ def measure_paged(W, steps, warmup, dev, page_entries):
     if bench.err.item() != 0:
         raise RuntimeError(f"device error word {bench.err.item()} in the paged steps")
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    del graphs, bench
+    del graphs
+    # the parts one after another with events between (a few eager steps)
+    parts = {n: [] for n in FullDecode.PARTS}
+    for i in range(min(steps, 5)):
+        pev = [torch.cuda.Event(enable_timing=True) for _ in range(len(FullDecode.PARTS) + 1)]
+        flush()
+        bench.step(warmup + i, ev=pev)
+        torch.cuda.synchronize()
+        for k, n in enumerate(FullDecode.PARTS):
+            parts[n].append(pev[k].elapsed_time(pev[k + 1]))
+    del bench
     return {"workload": W.name, "page_entries": page_entries, "page_order": "seeded random permutation of the pool",
-            "steps": steps, "ms_per_step": round(ms, 4), "value": round(W.batch / (ms / 1e3), 2), "unit": UNIT}
+            "steps": steps, "ms_per_step": round(ms, 4), "value": round(W.batch / (ms / 1e3), 2), "unit": UNIT,
+            "part_ms_eager": {k: round(statistics.median(v), 4) for k, v in parts.items()}}
 
 
 def measure_group(W, steps, warmup, dev, variant_layers=None):

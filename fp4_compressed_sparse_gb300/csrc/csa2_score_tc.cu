@@ -400,14 +400,19 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
       }
       ++bchanges;
       const int seq = a.s.cache_seq < 0 ? row : a.s.cache_seq;
-      for (int tile = first_own(t0, jrow, nprod, pw); tile < t1; tile += nprod) {
+      // FULL: the physical tile of the next own tile is looked up one step ahead,
+      // so that a paged cache's table read overlaps the wait for a free stage
+      const int tile_first = first_own(t0, jrow, nprod, pw);
+      int64_t t_next = (!pool_mode && tile_first < t1) ? phys_tile(a.s.map, seq, tile_first) : 0;
+      for (int tile = tile_first; tile < t1; tile += nprod) {
         const int j = jrow + (tile - t0), s = j % kStages;
+        const int64_t t = t_next;
+        if (!pool_mode && tile + nprod < t1) t_next = phys_tile(a.s.map, seq, tile + nprod);
         if (j >= kStages) ok = pool_mode ? wait_warp(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err)
                                          : wait1(sm, &sm.empty[s], ((j / kStages) - 1) & 1, a.s.err);
         if (!ok) break;
         uint8_t *dst = sm.stage[s];
         if (!pool_mode) {
-          const int64_t t = phys_tile(a.s.map, seq, tile);
           if (t >= 0) {
             tc::mbar_expect_tx(&sm.full[s], kStageBytes);
             bulk_g2s(tc::smem_addr(dst), a.s.idx_codes + static_cast<size_t>(t) * kIdxTileCodeBytes,
