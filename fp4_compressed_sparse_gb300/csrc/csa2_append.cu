@@ -50,17 +50,23 @@ __global__ void __launch_bounds__(kEncThreads) k_append_r1(csa2_cache c, const v
   __shared__ __align__(16) float row[kDcmp];
   __shared__ __align__(16) float rot[kRope];
   const int b = blockIdx.y, j = blockIdx.x;
+  // the token's rows do not depend on the token count: request them together
+  // with it, so that the RoPE row (which does) is the only later round trip
   const int64_t t0 = c.n_tokens[b];
-  if (!append_ok(c, t0, n_new, rope_len)) {
-    if (j == 0 && threadIdx.x == 0) append_fail(c, t0, n_new, rope_len, err);
-    return;
-  }
-  const int64_t t = t0 + j;
   const size_t base = static_cast<size_t>(b) * n_new + j;
   for (int i = threadIdx.x; i < kDqk; i += blockDim.x) row[i] = load_in(kv, base * kDqk + i, in_bf16);
   for (int i = threadIdx.x; i < kDi; i += blockDim.x) row[kDqk + i] = load_in(ik, base * kDi + i, in_bf16);
+  const bool ok = append_ok(c, t0, n_new, rope_len);
+  const int64_t t = t0 + j;
+  float cs = 0.0f;  // this thread's RoPE table value (threads 0..63)
+  if (ok && threadIdx.x < 64) cs = rope_cs[t * 64 + threadIdx.x];
+  if (!ok) {
+    if (j == 0 && threadIdx.x == 0) append_fail(c, t0, n_new, rope_len, err);
+    return;
+  }
+  if (threadIdx.x < 64) rot[threadIdx.x] = cs;  // staged through rot, rotated in place below
   __syncthreads();
-  block_rope(row, rope_cs + t * 64, rot);
+  block_rope_inplace(row, rot);
   __syncthreads();
   block_encode_entry(c, b, t, row, rot, err);
   if (j >= n_new - kWin) {

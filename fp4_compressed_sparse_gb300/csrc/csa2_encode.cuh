@@ -147,6 +147,18 @@ __device__ __forceinline__ void block_rope(const float *row, const float *cs, fl
   }
 }
 
+// The same with the table row already in rot[0:64] (cos, sin per pair), which
+// the rotated dims then replace; threads 0..31, each reading its own pair.
+__device__ __forceinline__ void block_rope_inplace(const float *row, float *rot) {
+  const int t = threadIdx.x;
+  if (t < 32) {
+    float a = row[kLat + 2 * t], bb = row[kLat + 2 * t + 1];
+    rope_pair(a, bb, rot[2 * t], rot[2 * t + 1]);
+    rot[2 * t] = a;
+    rot[2 * t + 1] = bb;
+  }
+}
+
 // Two values of an NVFP4 group of 16 held by 8 consecutive lanes: returns the
 // packed byte (first value in the low nibble); *sc = the group's scale code.
 __device__ __forceinline__ uint32_t nvfp4_pair(float x0, float x1, uint32_t *sc) {

@@ -269,6 +269,20 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
+// the same with an L2 cache policy (createpolicy)
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(tc::smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(tc::smem_addr(bar))
@@ -367,6 +381,7 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
     // over once its copies have landed.  Producer 0 also loads each row's query
     // record into a B slot.
     const int pw = warp, nprod = kProducers;
+    const uint64_t pol = policy_evict_first();  // each key tile is read once per call
     int bchanges = 0, jrow = 0, mine = 0;
     bool ok = true;
     int npend = 0, jlast = 0;  // POOL: own tiles in flight, the newest one's index
@@ -415,10 +430,11 @@ __global__ void __launch_bounds__(threads_of(NP), 1) k_index_score_tc(TcArgs a, 
         if (!pool_mode) {
           if (t >= 0) {
             tc::mbar_expect_tx(&sm.full[s], kStageBytes);
-            bulk_g2s(tc::smem_addr(dst), a.s.idx_codes + static_cast<size_t>(t) * kIdxTileCodeBytes,
-                     kIdxTileCodeBytes, &sm.full[s]);
-            bulk_g2s(tc::smem_addr(dst + kIdxTileCodeBytes), a.s.idx_scales + static_cast<size_t>(t) * kIdxTileScaleBytes,
-                     kIdxTileScaleBytes, &sm.full[s]);
+            bulk_g2s_hint(tc::smem_addr(dst), a.s.idx_codes + static_cast<size_t>(t) * kIdxTileCodeBytes,
+                          kIdxTileCodeBytes, &sm.full[s], pol);
+            bulk_g2s_hint(tc::smem_addr(dst + kIdxTileCodeBytes),
+                          a.s.idx_scales + static_cast<size_t>(t) * kIdxTileScaleBytes, kIdxTileScaleBytes, &sm.full[s],
+                          pol);
           } else {  // a page id outside the pool: the tile is not read (its scores are unspecified)
             raise_err(a.s.err, CSA2_DEVERR_INDEX);
             tc::mbar_arrive(&sm.full[s]);

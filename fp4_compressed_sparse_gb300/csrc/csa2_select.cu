@@ -522,6 +522,276 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
   }
 }
 
+// ----------------------------------------------------------------------------- one CTA per row
+// Many rows of at most kRowMaxSlots slots (the chunked prefill's query rows):
+// one CTA of 1024 threads per (row, problem), no cluster, so that the launch
+// needs a quarter of the CTAs (and waves) of the cluster kernel.  The same
+// selection as k_select with every step inside one CTA: threshold bin from the
+// sideband histogram, one pass over the row (bitmap of the keys above the bin,
+// candidate list of the keys in it), exact radix select among the candidates
+// (or over the row after a list overflow), then the ascending output from a
+// block scan of the bitmap's popcounts.
+constexpr int kRowThreads = 1024;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int64_t kRowMaxSlots = 131072;
+constexpr int kRowMaxWords = static_cast<int>(kRowMaxSlots / 32);
+
+struct RowSmem {
+  uint32_t hist[kSelBins];
+  uint64_t cand[kSelCap];
+  uint32_t bitmap[kRowMaxWords];
+  uint32_t warp_tot[kRowWarps + 1];
+  uint32_t dhist[256];
+  uint64_t prefix;
+  uint32_t thr, above, total, ncand, overflow, rem, done;
+};
+
+// Block-wide exclusive scan over kRowThreads threads; *total = the sum.
+__device__ __forceinline__ uint32_t row_excl_scan(uint32_t v, uint32_t *warp_tot, uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = warp_tot[lane];
+    uint32_t inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    warp_tot[lane] = inc - t;  // exclusive warp offsets
+    if (lane == 31) warp_tot[kRowWarps] = inc;
+  }
+  __syncthreads();
+  const uint32_t r = warp_tot[warp] + x - v;
+  *total = warp_tot[kRowWarps];
+  __syncthreads();  // warp_tot may be reused right away
+  return r;
+}
+
+// grid (rows, problems), kRowThreads; dynamic smem: RowSmem
+__global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const uint8_t *aux, int64_t aux_row) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  RowSmem &sm = *reinterpret_cast<RowSmem *>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x, p = blockIdx.y;
+  const int64_t ns = n_slots(a, row, p);
+  const int64_t T = row_T(a, row);
+  const uint32_t k = static_cast<uint32_t>(prob_k(a, p));
+  const int nw = static_cast<int>((ns + 31) / 32);
+  const float *src = p == 1 ? aux_bmax(aux, aux_row, row) : a.scores + static_cast<size_t>(row) * a.stride;
+  const int32_t *prow = a.pool ? a.pool + static_cast<size_t>(row) * a.pool_blocks : nullptr;
+  const bool plain = p == 1 || a.pool == nullptr;
+  const uint32_t nsu = static_cast<uint32_t>(ns);
+
+  // the first batch of the pass does not depend on the threshold: request it now
+  constexpr int kFB = 16;  // words per warp per batch
+  float fb[kFB];
+  if (plain) {
+#pragma unroll
+    for (int b = 0; b < kFB; ++b) {
+      const int w = warp * kFB + b;
+      const uint32_t slot = static_cast<uint32_t>(w) * 32 + lane;
+      fb[b] = (w < nw && slot < nsu) ? src[slot] : __uint_as_float(0x7FC00000u);
+    }
+  }
+
+  // ---- 1. threshold bin from the histogram
+  {
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
+    for (int i = tid; i < kSelBins / 4; i += kRowThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
+    for (int i = tid; i < nw; i += kRowThreads) sm.bitmap[i] = 0;
+    if (tid == 0) {
+      sm.ncand = 0;
+      sm.overflow = 0;
+      sm.rem = 0;
+      sm.done = 0;
+      sm.prefix = 0;
+    }
+    __syncthreads();
+    constexpr int per = kSelBins / kRowThreads;  // 8 bins per thread, thread 0 the top ones
+    const int top = kSelBins - 1 - tid * per;
+    uint32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) local += sm.hist[top - ((i + tid) & (per - 1))];
+    uint32_t total;
+    const uint32_t above = row_excl_scan(local, sm.warp_tot, &total);
+    if (total <= k) {
+      if (tid == 0) {  // every valid slot is chosen: bin 0 is the threshold bin
+        sm.thr = 0;
+        sm.above = total - sm.hist[0];
+        sm.total = total;
+      }
+    } else if (above < k && k <= above + local) {
+      uint32_t acc = above;
+      for (int i = 0; i < per; ++i) {
+        const uint32_t bin = top - i;
+        if (acc + sm.hist[bin] >= k) {
+          sm.thr = bin;
+          sm.above = acc;
+          sm.total = total;
+          break;
+        }
+        acc += sm.hist[bin];
+      }
+    }
+    __syncthreads();
+  }
+  const uint32_t thr = sm.thr;
+  const uint32_t kt = min(k, sm.total);
+  const uint32_t need = kt - sm.above;
+
+  // ---- 2. one pass over the row: bitmap words of the keys above the bin,
+  // candidates in it
+  auto add_cands = [&](uint32_t mask, bool want, uint64_t K) {
+    if (!mask) return;
+    const int leader = __ffs(mask) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(&sm.ncand, static_cast<uint32_t>(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (want) {
+      const uint32_t at = base + __popc(mask & ((1u << lane) - 1u));
+      if (at < kSelCap) sm.cand[at] = K;
+      else sm.overflow = 1;
+    }
+  };
+  if (plain && thr > 0) {
+    // "above the bin" is f > hi and "in the bin" lo <= f <= hi (order keys are
+    // monotone in the float value; -0 == +0; NaN is neither)
+    const float lo = float_of_key(thr << kSelBinShift);
+    const float hi = float_of_key(((thr + 1) << kSelBinShift) - 1);
+    for (int w0 = warp * kFB; w0 < nw; w0 += kRowWarps * kFB) {
+      if (w0 != warp * kFB) {
+#pragma unroll
+        for (int b = 0; b < kFB; ++b) {
+          const int w = w0 + b;
+          const uint32_t slot = static_cast<uint32_t>(w) * 32 + lane;
+          fb[b] = (w < nw && slot < nsu) ? src[slot] : __uint_as_float(0x7FC00000u);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kFB; ++b) {
+        const int w = w0 + b;
+        if (w >= nw) break;  // warp-uniform
+        const float f = fb[b];
+        const uint32_t slot = static_cast<uint32_t>(w) * 32 + lane;
+        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && slot < nsu)) {
+          if (isnan(f) && slot < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
+        }
+        const uint32_t word = __ballot_sync(0xffffffffu, f > hi);
+        if (lane == 0) sm.bitmap[w] = word;
+        const bool want = f >= lo && f <= hi;
+        add_cands(__ballot_sync(0xffffffffu, want), want,
+                  (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
+      }
+    }
+  } else {
+    for (int w = warp; w < nw; w += kRowWarps) {
+      bool ok;
+      const int64_t slot = static_cast<int64_t>(w) * 32 + lane;
+      const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+      if (p == 0 && ok && isnan(f)) raise_err(a.err, CSA2_DEVERR_NAN);
+      const uint32_t key = key_of(f);
+      const uint32_t bin = key >> kSelBinShift;
+      const uint32_t word = __ballot_sync(0xffffffffu, ok && bin > thr);
+      if (lane == 0) sm.bitmap[w] = word;
+      const bool want = ok && bin == thr;
+      add_cands(__ballot_sync(0xffffffffu, want), want,
+                (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(slot)));
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. exact select of the need-th largest low key in the bin: 8-bit
+  // digits over bits 50..3, then bits 2..0 (over the row after a list overflow)
+  const uint32_t n = sm.ncand;
+  const bool from_row = sm.overflow != 0 || n > static_cast<uint32_t>(kSelCap);
+  const int nc = static_cast<int>(n);
+  const bool all = !from_row && need == n;
+  if (tid == 0) sm.rem = need;
+  __syncthreads();
+  if (need > 0 && !all) {
+    for (int d = 0; d < 7; ++d) {
+      const int sh = d < 6 ? 43 - 8 * d : 0;
+      const uint32_t dmask = d < 6 ? 0xFFu : 0x7u;
+      const uint64_t hi_mask = kLow & ~((1ull << (sh + (d < 6 ? 8 : 3))) - 1);
+      for (int i = tid; i < 256; i += kRowThreads) sm.dhist[i] = 0;
+      __syncthreads();
+      const uint64_t prefix = sm.prefix;
+      if (!from_row) {
+        for (int i = tid; i < nc; i += kRowThreads) {
+          const uint64_t low = sm.cand[i] & kLow;
+          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+        }
+      } else {
+        for (int64_t slot = tid; slot < ns; slot += kRowThreads) {
+          bool ok;
+          const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+          const uint32_t key = key_of(f);
+          if (!ok || (key >> kSelBinShift) != thr) continue;
+          const uint64_t low = low_of(key, static_cast<uint32_t>(slot));
+          if ((low & hi_mask) == prefix) atomicAdd(&sm.dhist[(low >> sh) & dmask], 1u);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) pick_digit(sm.dhist, sh, &sm.rem, &sm.prefix, &sm.done);
+      __syncthreads();
+      if (sm.done) break;
+    }
+  }
+  // mark the chosen keys of the bin (low >= the need-th largest)
+  const uint64_t cut = sm.prefix;
+  if (need > 0) {
+    if (!from_row) {
+      for (int i = tid; i < nc; i += kRowThreads) {
+        const uint64_t K = sm.cand[i];
+        if (all || (K & kLow) >= cut) {
+          const uint32_t slot = 0xFFFFFFFFu - static_cast<uint32_t>(K);
+          atomicOr(&sm.bitmap[slot >> 5], 1u << (slot & 31));
+        }
+      }
+    } else {
+      for (int64_t slot = tid; slot < ns; slot += kRowThreads) {
+        bool ok;
+        const float f = slot_value(a, src, prow, p, slot, ns, T, ok);
+        const uint32_t key = key_of(f);
+        if (!ok || (key >> kSelBinShift) != thr) continue;
+        if (low_of(key, static_cast<uint32_t>(slot)) >= cut)
+          atomicOr(&sm.bitmap[slot >> 5], 1u << (static_cast<uint32_t>(slot) & 31));
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 4. ascending output: block scan of the popcounts of contiguous word ranges
+  const int per = (nw + kRowThreads - 1) / kRowThreads;
+  const int wb = min(nw, tid * per), we = min(nw, wb + per);
+  uint32_t c = 0;
+  for (int w = wb; w < we; ++w) c += __popc(sm.bitmap[w]);
+  uint32_t tot;
+  uint32_t off = row_excl_scan(c, sm.warp_tot, &tot);
+  int32_t *out = p == 0 ? a.idx_out + static_cast<size_t>(row) * a.k
+                        : a.pool_out + static_cast<size_t>(row) * a.out_pool_blocks;
+  for (int w = wb; w < we; ++w) {
+    uint32_t word = sm.bitmap[w];
+    while (word) {
+      const int b = __ffs(word) - 1;
+      word &= word - 1;
+      if (off < kt) out[off] = slot_position(a, row, p, static_cast<uint32_t>(w) * 32 + b);
+      ++off;
+    }
+  }
+  const int kout = p == 0 ? a.k : a.out_pool_blocks;
+  for (int i = kt + tid; i < kout; i += kRowThreads) out[i] = -1;
+  if (p == 1 && tid == 0) a.pool_count[row] = static_cast<int32_t>(kt);
+}
+
 }  // namespace
 
 // Workspace: bitmaps (used when a row has more than 2^20 slots) | the
@@ -559,6 +829,16 @@ cudaError_t launch_topk(const TopkArgs &a0, void *ws, cudaStream_t s) {
     aux = own;
   }
   const int nprob = (!a.pool && a.out_pool_blocks > 0) ? 2 : 1;
+  const int64_t max_slots = a.pool ? static_cast<int64_t>(a.pool_blocks) * a.bs : a.stride;
+  if (max_slots <= kRowMaxSlots && static_cast<int64_t>(a.rows) * nprob * 4 > 2 * device_sm_count()) {
+    // more (row, problem) clusters of four than one wave of two CTAs per SM
+    // holds: one CTA per (row, problem) instead
+    const int smem = static_cast<int>(sizeof(RowSmem));
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_select_row), smem);
+    if (e != cudaSuccess) return e;
+    k_select_row<<<dim3(a.rows, nprob), kRowThreads, smem, s>>>(a, aux, aux_row);
+    return cudaGetLastError();
+  }
   // CTAs per (row, problem): 8 for long rows while the launch still fits one wave
   // of two CTAs per SM, else 4
   const int ncl = (a.rows * nprob * kSelClusterMax <= 2 * device_sm_count() && w0 >= 4096) ? kSelClusterMax : 4;

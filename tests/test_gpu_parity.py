@@ -252,6 +252,74 @@ def test_topk_crowded_bins_against_oracle(orc, levels, T, k, nblk):
         assert cnt[b].item() == n and pool[b].tolist() == pids.tolist()
 
 
+@pytest.mark.parametrize("levels", [0, 2, 4])
+def test_topk_many_rows_against_oracle(orc, levels):
+    """More (row, problem) pairs than one wave of four-CTA clusters holds, so the
+    selector runs one CTA per (row, problem): heavy ties and crowded bins, both
+    signs and -0/+0, rows of every length down to none, and the pool build; every
+    row against the oracle."""
+    B, T, k, nblk = 96, 20000, 512, 2048
+    g = torch.Generator().manual_seed(2000 + levels)
+    stride = T + 40
+    if levels:
+        vals = torch.tensor([-0.0, 0.0, 1.5, -2.25, 1.5 + 2 ** -20][:levels + 1])
+        sc = vals[torch.randint(0, len(vals), (B, stride), generator=g)]
+    else:
+        sc = torch.randn((B, stride), generator=g) * 3
+    sc = sc.float().contiguous()
+    lens = [max(0, T - 211 * b) for b in range(B)]
+    q_pos = torch.tensor(lens, dtype=torch.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    pool = torch.empty((B, nblk), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = csa2.topk_workspace(B, stride, k, nblk)
+    csa2.topk(sc.cuda(), 1, q_pos.cuda(), k, idx, ws, pool_out=pool, pool_count=cnt, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    idx, pool, cnt = idx.cpu(), pool.cpu(), cnt.cpu()
+    for b in range(B):
+        row = sc[b, :lens[b]].numpy()
+        assert idx[b].tolist() == orc.topk(row, k).tolist(), f"row {b} (T {lens[b]})"
+        pids, n = orc.pool(row, lens[b], 8, nblk)
+        assert cnt[b].item() == n and pool[b].tolist() == pids.tolist(), f"row {b} pool"
+
+
+def test_topk_many_pool_rows_against_oracle(orc):
+    """POOL rows (a Reindex layer's candidate pools), more of them than one wave of
+    four-CTA clusters holds: one CTA per row, against the oracle over the pool's
+    visible positions."""
+    B, T, k, nblk = 100, 6000, 128, 96
+    g = torch.Generator().manual_seed(77)
+    pools = []
+    for b in range(B):
+        p = torch.sort(torch.randperm((T - 1) // 8 + 1, generator=g)[:nblk]).values.to(torch.int32)
+        if b % 3 == 1 and b % 17:
+            p[-(b % 17):] = -1  # padded pools
+        pools.append(p)
+    pool = torch.stack(pools)
+    stride = nblk * 8
+    vals = torch.tensor([0.5, 0.75, -1.0, 2.0])
+    sc = torch.where(torch.rand((B, stride), generator=g) < 0.5, vals[torch.randint(0, 4, (B, stride), generator=g)],
+                     torch.randn((B, stride), generator=g)).float().contiguous()
+    q_pos = torch.tensor([T - 1 - 13 * b for b in range(B)], dtype=torch.int64)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    ws = csa2.topk_workspace(B, stride, k)
+    csa2.topk(sc.cuda(), 1, q_pos.cuda(), k, idx, ws, pool=pool.cuda(), err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    idx = idx.cpu()
+    for b in range(B):
+        pl = pool[b].numpy()
+        cnt = int((pl >= 0).sum())
+        Tv = int(q_pos[b])
+        pos = orc.pool_positions(pl, cnt, Tv)
+        slots = np.array([list(pl[:cnt]).index(p // 8) * 8 + p % 8 for p in pos], dtype=np.int64)
+        ref = sc[b].numpy()[slots] if len(slots) else np.zeros(0, np.float32)
+        assert idx[b].tolist() == orc.topk(ref, k, positions=pos).tolist(), f"row {b}"
+
+
 def test_topk_nan_score_is_reported(orc):
     sc = torch.randn((1, 5000))
     sc[0, 123] = float("nan")
