@@ -8,8 +8,14 @@
 // (absorbed query: the logit is q_lat . c + q_rope . k_rope, the value is the
 // 512-dim latent c).
 //
-// One CTA = (some segments of a row's entry list, up to 64 heads).  Every head
-// shares the entries, so each entry is dequantised once per CTA:
+// Two kernels with the same entry gather, dequantisation and segment schedule:
+// k_attn (below) for decode rows, with both contractions on mma.sync and O in
+// registers; k_attn_tc (further below) for one-segment rows (the chunked
+// prefill, a query's whole entry list in one CTA), with both contractions on
+// the tcgen05 tensor cores and O in tensor memory.
+//
+// k_attn: one CTA = (some segments of a row's entry list, up to 64 heads).
+// Every head shares the entries, so each entry is dequantised once per CTA:
 //   producer warps (4)  gather 32 entries at a time and dequantise them into a
 //                       two-stage fp16 ring: E2M1 pairs by cvt.f16x2.e2m1x2, times
 //                       the E4M3 scale (exact: at most 6 significant bits, >= 2^-10);
@@ -197,6 +203,216 @@ __device__ __forceinline__ void load_fp4(const AttnArgs &a, int64_t src, int q4,
   r.rsc = a.rope_scales[src * 4 + q4];
 }
 
+// Dequantises this producer thread's quarter of one entry of kind `kind` (at
+// src) into fp16 through put(u, lo, hi): 16-dim unit u (dims 16u .. 16u + 7 in
+// lo, the next 8 in hi), units q4, q4 + 4, ... of the 36.  FP4 entries are exact
+// (E2M1 pairs by cvt.f16x2.e2m1x2, times the E4M3 scale); V4 entries and window
+// entries are scaled by a power of two 2^-sigma only when they would not fit
+// fp16.  Returns 2^sigma, 0 for an empty entry.  The four threads of an entry
+// (qmask) take the same branch.
+template <class Put>
+__device__ __forceinline__ float dequant_entry(const AttnArgs &a, int kind, int64_t src, const Fp4Raw &raw, int q4,
+                                               uint32_t qmask, bool fp8, Put put) {
+  float sig = 0.0f;
+  if (kind == 1 && fp8) {
+    // V4 entry: 512 E4M3 codes with an E8M0 per 32, then 64 bf16 RoPE dims;
+    // scaled by a power of two 2^-sigma only if they would not fit fp16
+    const uint8_t *lc = a.lat_codes + src * 512;
+    const uint4 sv = *reinterpret_cast<const uint4 *>(a.lat_scales + src * 16);
+    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+    uint32_t mx = 0;
+#pragma unroll
+    for (int g = 0; g < 16; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+    const uint4 *rc = reinterpret_cast<const uint4 *>(a.rope_codes + src * 128 + 32 * q4);
+    const uint4 r0 = rc[0], r1 = rc[1];
+    const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    float ramax = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+      ramax = fmaxf(ramax, fmaxf(fabsf(__uint_as_float(rw[b] << 16)), fabsf(__uint_as_float(rw[b] & 0xFFFF0000u))));
+    ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 1));
+    ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 2));
+    // latent values < 448 * 2^(mx-127), RoPE values <= ramax: both below 2^16 after 2^-sigma
+    const int s_lat = static_cast<int>(mx) - 134;
+    const int s_rope = ramax > 0.0f ? floor_log2f(ramax) - 14 : 0;
+    const int sigma = min(15, max(0, max(s_lat, s_rope)));
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const int u = q4 + 4 * i;  // 16 latent dims, half of scale block u / 2
+      const uint4 cw = reinterpret_cast<const uint4 *>(lc)[u];
+      const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
+      const uint32_t swu = wi == 0 ? sv.x : wi == 1 ? sv.y : wi == 2 ? sv.z : sv.w;
+      const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
+      const int kx = sc - 127 - sigma;
+      const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
+      const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
+        o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
+      }
+      put(u, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+    }
+    {  // RoPE unit 32 + q4: 16 bf16 dims
+      const float inv = pow2f(-sigma);
+      uint32_t o[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(rw[b] << 16), inv),
+                                       __fmul_rn(__uint_as_float(rw[b] & 0xFFFF0000u), inv));
+        o[b] = *reinterpret_cast<uint32_t *>(&t2);
+      }
+      put(32 + q4, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+    }
+    sig = pow2f(sigma);
+  } else if (kind == 1) {
+    // FP4 entry: unit u < 32 = latent dims 16u.. (8 code bytes, scale u), u = 32 + q4 the RoPE group q4
+    const uint32_t sw[8] = {raw.s0.x, raw.s0.y, raw.s0.z, raw.s0.w, raw.s1.x, raw.s1.y, raw.s1.z, raw.s1.w};
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int u = i < 8 ? q4 + 4 * i : 32 + q4;
+      // unit q4 + 4 i has scale byte q4 of word i (a static index: no local array)
+      const uint32_t sb = i < 8 ? (sw[i] >> (8 * q4)) & 0xFFu : raw.rsc;
+      const uint32_t s2 = e4m3x2_to_h2(sb | (sb << 8));
+      uint32_t o[8];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        o[b] = hmul2u(e2m1x2_to_h2(raw.cw[i].x >> (8 * b)), s2);
+        o[4 + b] = hmul2u(e2m1x2_to_h2(raw.cw[i].y >> (8 * b)), s2);
+      }
+      put(u, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+    }
+    sig = 1.0f;
+  } else if (kind == 2 || kind == 3) {
+    const bool ring = kind == 2;
+    const int rec = a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+    const uint8_t *cb = (ring ? a.ring_codes : a.lin_codes) + src * rec;
+    if (a.swa_dtype == CSA2_SWA_MXFP8) {
+      const uint4 *sp = reinterpret_cast<const uint4 *>((ring ? a.ring_scales : a.lin_scales) +
+                                                        src * kSwaScaleStride);
+      const uint4 s0 = sp[0], s1 = sp[1];
+      const uint32_t sw[5] = {s0.x, s0.y, s0.z, s0.w, s1.x};
+      uint32_t mx = 0;
+#pragma unroll
+      for (int g = 0; g < 18; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+      // values < 448 * 2^(sc-127): keep them below 2^16 with sigma >= 0
+      const int sigma = min(15, max(0, static_cast<int>(mx) - 134));
+#pragma unroll 1
+      for (int i = 0; i < 9; ++i) {
+        const int u = q4 + 4 * i;
+        const uint4 cw = reinterpret_cast<const uint4 *>(cb)[u];
+        const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
+        const uint32_t swu = wi == 0 ? sw[0] : wi == 1 ? sw[1] : wi == 2 ? sw[2] : wi == 3 ? sw[3] : sw[4];
+        const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
+        const int kx = sc - 127 - sigma;
+        const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
+        const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
+          o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
+        }
+        put(u, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+      }
+      sig = pow2f(sigma);
+    } else {
+      const uint4 *cw = reinterpret_cast<const uint4 *>(cb);
+      float amax = 0.0f;
+#pragma unroll 1
+      for (int i = 0; i < 9; ++i) {
+        const int u = q4 + 4 * i;
+        const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[b] << 16)), fabsf(__uint_as_float(w[b] & 0xFFFF0000u))));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
+      const int sigma = amax > 0.0f ? min(15, max(0, floor_log2f(amax) - 14)) : 0;
+      const float inv = pow2f(-sigma);
+#pragma unroll 1
+      for (int i = 0; i < 9; ++i) {
+        const int u = q4 + 4 * i;
+        const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[b] << 16), inv),
+                                         __fmul_rn(__uint_as_float(w[b] & 0xFFFF0000u), inv));
+          o[b] = *reinterpret_cast<uint32_t *>(&t2);
+        }
+        put(u, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+      }
+      sig = pow2f(sigma);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int u = q4 + 4 * i;
+      put(u, make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0));
+    }
+  }
+  return sig;
+}
+
+// L2 prefetch of this producer thread's share of one entry's record (kind, src
+// as from entry_kind): the lines its dequantisation will read.
+__device__ __forceinline__ void l2_line(const void *p) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p)); }
+__device__ __forceinline__ void prefetch_entry(const AttnArgs &a, int kind, int64_t src, int q4, bool fp8) {
+  if (kind == 1) {
+    if (fp8) {
+      l2_line(a.lat_codes + src * 512 + 128 * q4);
+      if (q4 == 0) l2_line(a.lat_scales + src * 16);
+      if (q4 == 1) l2_line(a.rope_codes + src * 128);
+    } else {
+      if (q4 < 2) l2_line(a.lat_codes + src * 256 + 128 * q4);
+      if (q4 == 2) l2_line(a.lat_scales + src * 32);
+      if (q4 == 3) {
+        l2_line(a.rope_codes + src * 32);
+        l2_line(a.rope_scales + src * 4);
+      }
+    }
+  } else if (kind == 2 || kind == 3) {
+    const bool ring = kind == 2;
+    const int rec = a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
+    const uint8_t *cb = (ring ? a.ring_codes : a.lin_codes) + src * rec;
+    for (int off = 128 * q4; off < rec; off += 512) l2_line(cb + off);
+    if (q4 == 3) l2_line(cb + rec - 1);
+    if (q4 == 0 && a.swa_dtype == CSA2_SWA_MXFP8) l2_line((ring ? a.ring_scales : a.lin_scales) + src * kSwaScaleStride);
+  }
+}
+
+// load_fp4 with every load issued where it stands (volatile): the compiler may
+// not sink a prefetch for a later chunk down to its first use
+__device__ __forceinline__ uint2 ldv2(const void *p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ldv4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ldv1(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];\n" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void load_fp4_early(const AttnArgs &a, int64_t src, int q4, Fp4Raw &r) {
+  const uint8_t *lc = a.lat_codes + src * 256;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r.cw[i] = ldv2(lc + 8 * (q4 + 4 * i));
+  r.cw[8] = ldv2(a.rope_codes + src * 32 + 8 * q4);
+  r.s0 = ldv4(a.lat_scales + src * 32);
+  r.s1 = ldv4(a.lat_scales + src * 32 + 16);
+  r.rsc = ldv1(a.rope_scales + src * 4 + q4);
+}
+
 // Partial results of one (row, head block, segment) in the workspace: O
 // [HP][512] then (m, l) [HP][2], fp32.
 template <int HP>
@@ -344,154 +560,10 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
       if (c >= 2 && !dead) dead = !wait_warp(&sm.empty[st], ((c - 2) >> 1) & 1, a.err);
       if (!dead) {
         uint4 *dst = reinterpret_cast<uint4 *>(&sm.kv[st][e][0]);  // 16-dim unit u at dst[2u], dst[2u+1]
-        float sig = 0.0f;
-        if (kind == 1 && fp8) {
-          // V4 entry: 512 E4M3 codes with an E8M0 per 32, then 64 bf16 RoPE dims;
-          // scaled by a power of two 2^-sigma only if they would not fit fp16
-          const uint8_t *lc = a.lat_codes + src * 512;
-          const uint4 sv = *reinterpret_cast<const uint4 *>(a.lat_scales + src * 16);
-          const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-          uint32_t mx = 0;
-#pragma unroll
-          for (int g = 0; g < 16; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
-          const uint4 *rc = reinterpret_cast<const uint4 *>(a.rope_codes + src * 128 + 32 * q4);
-          const uint4 r0 = rc[0], r1 = rc[1];
-          const uint32_t rw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-          float ramax = 0.0f;
-#pragma unroll
-          for (int b = 0; b < 8; ++b)
-            ramax = fmaxf(ramax, fmaxf(fabsf(__uint_as_float(rw[b] << 16)), fabsf(__uint_as_float(rw[b] & 0xFFFF0000u))));
-          ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 1));
-          ramax = fmaxf(ramax, __shfl_xor_sync(qmask, ramax, 2));
-          // latent values < 448 * 2^(mx-127), RoPE values <= ramax: both below 2^16 after 2^-sigma
-          const int s_lat = static_cast<int>(mx) - 134;
-          const int s_rope = ramax > 0.0f ? floor_log2f(ramax) - 14 : 0;
-          const int sigma = min(15, max(0, max(s_lat, s_rope)));
-#pragma unroll 1
-          for (int i = 0; i < 8; ++i) {
-            const int u = q4 + 4 * i;  // 16 latent dims, half of scale block u / 2
-            const uint4 cw = reinterpret_cast<const uint4 *>(lc)[u];
-            const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
-            const uint32_t swu = wi == 0 ? sv.x : wi == 1 ? sv.y : wi == 2 ? sv.z : sv.w;
-            const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
-            const int kx = sc - 127 - sigma;
-            const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
-            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
-              o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
-            }
-            dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          {  // RoPE unit 32 + q4: 16 bf16 dims
-            const float inv = pow2f(-sigma);
-            uint32_t o[8];
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-              __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(rw[b] << 16), inv),
-                                             __fmul_rn(__uint_as_float(rw[b] & 0xFFFF0000u), inv));
-              o[b] = *reinterpret_cast<uint32_t *>(&t2);
-            }
-            dst[2 * (32 + q4)] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[2 * (32 + q4) + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          sig = pow2f(sigma);
-        } else if (kind == 1) {
-          // FP4 entry: unit u < 32 = latent dims 16u.. (8 code bytes, scale u), u = 32 + q4 the RoPE group q4
-          const uint32_t sw[8] = {raw.s0.x, raw.s0.y, raw.s0.z, raw.s0.w, raw.s1.x, raw.s1.y, raw.s1.z, raw.s1.w};
-#pragma unroll
-          for (int i = 0; i < 9; ++i) {
-            const int u = i < 8 ? q4 + 4 * i : 32 + q4;
-            const uint32_t sb = i < 8 ? (sw[u >> 2] >> (8 * (u & 3))) & 0xFFu : raw.rsc;
-            const uint32_t s2 = e4m3x2_to_h2(sb | (sb << 8));
-            uint32_t o[8];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-              o[b] = hmul2u(e2m1x2_to_h2(raw.cw[i].x >> (8 * b)), s2);
-              o[4 + b] = hmul2u(e2m1x2_to_h2(raw.cw[i].y >> (8 * b)), s2);
-            }
-            dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-          }
-          sig = 1.0f;
-        } else if (kind == 2 || kind == 3) {
-          const bool ring = kind == 2;
-          const int rec = a.swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
-          const uint8_t *cb = (ring ? a.ring_codes : a.lin_codes) + src * rec;
-          if (a.swa_dtype == CSA2_SWA_MXFP8) {
-            const uint4 *sp = reinterpret_cast<const uint4 *>((ring ? a.ring_scales : a.lin_scales) +
-                                                              src * kSwaScaleStride);
-            const uint4 s0 = sp[0], s1 = sp[1];
-            const uint32_t sw[5] = {s0.x, s0.y, s0.z, s0.w, s1.x};
-            uint32_t mx = 0;
-#pragma unroll
-            for (int g = 0; g < 18; ++g) mx = max(mx, (sw[g >> 2] >> (8 * (g & 3))) & 0xFFu);
-            // values < 448 * 2^(sc-127): keep them below 2^16 with sigma >= 0
-            const int sigma = min(15, max(0, static_cast<int>(mx) - 134));
-#pragma unroll 1
-            for (int i = 0; i < 9; ++i) {
-              const int u = q4 + 4 * i;
-              const uint4 cw = reinterpret_cast<const uint4 *>(cb)[u];
-              const int wi = u >> 3;  // scale word of unit u (a select chain: no local array)
-              const uint32_t swu = wi == 0 ? sw[0] : wi == 1 ? sw[1] : wi == 2 ? sw[2] : wi == 3 ? sw[3] : sw[4];
-              const int sc = static_cast<int>((swu >> (8 * ((u >> 1) & 3))) & 0xFFu);
-              const int kx = sc - 127 - sigma;
-              const uint32_t m2 = h2_splat(kx < -24 ? 0.0f : pow2f(kx));
-              const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-              uint32_t o[8];
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                o[2 * b] = hmul2u(e4m3x2_to_h2(w[b] & 0xFFFFu), m2);
-                o[2 * b + 1] = hmul2u(e4m3x2_to_h2(w[b] >> 16), m2);
-              }
-              dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
-              dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-            sig = pow2f(sigma);
-          } else {
-            const uint4 *cw = reinterpret_cast<const uint4 *>(cb);
-            float amax = 0.0f;
-#pragma unroll 1
-            for (int i = 0; i < 9; ++i) {
-              const int u = q4 + 4 * i;
-              const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
-              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-              for (int b = 0; b < 8; ++b)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[b] << 16)), fabsf(__uint_as_float(w[b] & 0xFFFF0000u))));
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(qmask, amax, 2));
-            const int sigma = amax > 0.0f ? min(15, max(0, floor_log2f(amax) - 14)) : 0;
-            const float inv = pow2f(-sigma);
-#pragma unroll 1
-            for (int i = 0; i < 9; ++i) {
-              const int u = q4 + 4 * i;
-              const uint4 v0 = cw[2 * u], v1 = cw[2 * u + 1];
-              const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-              uint32_t o[8];
-#pragma unroll
-              for (int b = 0; b < 8; ++b) {
-                __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[b] << 16), inv),
-                                               __fmul_rn(__uint_as_float(w[b] & 0xFFFF0000u), inv));
-                o[b] = *reinterpret_cast<uint32_t *>(&t2);
-              }
-              dst[2 * u] = make_uint4(o[0], o[1], o[2], o[3]);
-              dst[2 * u + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-            sig = pow2f(sigma);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 9; ++i) {
-            const int u = q4 + 4 * i;
-            dst[2 * u] = make_uint4(0, 0, 0, 0);
-            dst[2 * u + 1] = make_uint4(0, 0, 0, 0);
-          }
-        }
+        const float sig = dequant_entry(a, kind, src, raw, q4, qmask, fp8, [&](int u, uint4 lo, uint4 hi) {
+          dst[2 * u] = lo;
+          dst[2 * u + 1] = hi;
+        });
         if (q4 == 0) sm.sig[st][e] = sig;
       }
       tc::mbar_arrive(&sm.full[st]);
@@ -750,6 +822,538 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
     }
 }
 
+// ============================================================================ tensor-core kernel
+// The same schedule (segments of a row, one cluster per row and 64 heads, the
+// ordered merge; the library launches it on one-segment rows) with both
+// contractions on the 5th-generation tensor cores:
+// tcgen05.mma kind::f16, fp16 operands in shared memory, fp32 accumulators in
+// tensor memory (TMEM).
+//   S = Q K^T        M = 64 heads, N = 32 entries, K = 576 (36 MMAs); head h's
+//                    row of S sits in TMEM lane 32 (h / 16) + h % 16
+//   O^T += V^T P^T   four blocks of M = 128 latent dims x N = 64 heads, K = the
+//                    chunk's 32 entries (the fp16 tile read MN-major); O^T of
+//                    block b in TMEM columns 64 + 64 b, dim 128 b + lane
+// Roles (384 threads):
+//   warps 0-3  query to fp16 (once); per chunk the softmax (lanes 0-15 of warp
+//              w: heads 16w .. 16w + 15) and, at a segment's end, the O^T
+//              read-out (every thread one TMEM lane); P (fp16, times the
+//              entry's 2^sigma) goes to shared memory as the B operand.  A
+//              head's reference max moves only when some 2^sigma-weighted logit
+//              of the chunk would exceed it by more than 2^kSlack; O^T's column
+//              of that head is then rescaled in TMEM before the chunk's PV
+//   warps 4-7  producers, as in k_attn, into a three-stage tile in the operand
+//              layout (core matrices of 8 entries x 8 dims)
+//   warp 8     one thread issues every MMA: PV of chunk c, then S of chunk
+//              c + 2 (its tile and its S buffer are free by then), so the
+//              tensor core computes S ahead of the softmax
+//   warps 8-11 with warps 0-3, the query to fp16 (eight heads per warp)
+// Every wait is bounded (CSA2_DEVERR_TIMEOUT if one runs out).
+constexpr int kTcHeads = 64;
+constexpr int kTcStages = 3;
+constexpr int kTcMmaWarp = 8;
+constexpr int kTcThreads = 32 * 12;
+constexpr int kQBytes = kTcHeads * kDqk * 2;   // 73,728
+constexpr int kTileBytes = kE * kDqk * 2;      // 36,864
+constexpr int kPBytes = kTcHeads * kE * 2;     // 4,096
+constexpr float kSlack = 15.0f;                // P * 2^sigma stays below 2^16 (fp16)
+constexpr uint32_t kTcCols = 512;              // S[2]: columns 0..63; O^T block b: 64 + 64 b
+
+// Operand layouts (no swizzle; core matrices of 8 rows x 16 bytes).
+//   Q (head h, dim d): A of S, K-major                     LBO 1024, SBO 128
+__device__ __forceinline__ uint32_t q_off(int h, int d) {
+  return static_cast<uint32_t>((d >> 3) * 1024 + (h >> 3) * 128 + (h & 7) * 16 + (d & 7) * 2);
+}
+//   tile (entry e, dim d): B of S, K-major (N = e)         LBO 512, SBO 128
+//                          A of O^T, MN-major (M = d)       LBO 128, SBO 512
+__device__ __forceinline__ uint32_t t_off(int e, int d) {
+  return static_cast<uint32_t>((d >> 3) * 512 + (e >> 3) * 128 + (e & 7) * 16 + (d & 7) * 2);
+}
+//   P (head h, entry e): B of O^T, K-major (N = h)          LBO 1024, SBO 128
+__device__ __forceinline__ uint32_t p_off(int h, int e) {
+  return static_cast<uint32_t>((e >> 3) * 1024 + (h >> 3) * 128 + (h & 7) * 16 + (e & 7) * 2);
+}
+// kind::f16 instruction descriptor: fp16 x fp16 -> fp32; a_mn marks an MN-major A
+__host__ __device__ __forceinline__ uint32_t idesc_f16(int m, int n, int a_mn) {
+  uint32_t d = 1u << 4;  // D format fp32; A and B fp16
+  d |= static_cast<uint32_t>(a_mn & 1) << 15;
+  d |= static_cast<uint32_t>((n >> 3) & 0x3F) << 17;
+  d |= static_cast<uint32_t>((m >> 4) & 0x1F) << 24;
+  return d;
+}
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+// named barrier over the softmax warps returning the OR of v
+__device__ __forceinline__ int bar_sm_or(int v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 2, 128, p;\n selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ int bar_sm_and(int v) {
+  int r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, 2, 128, p;\n selp.s32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ void bar_sm() { asm volatile("bar.sync 2, 128;\n" ::: "memory"); }
+
+// Read-out of O^T blocks [b0, b1) of one TMEM lane quarter into O rows:
+// dst[h * 512 + 128 b + d] = O^T[d][h] * fin[h] for the heads h < nh; the warp
+// reads lanes lane_base .. + 31 (dims 128 b + d_lane), four 16-column loads in
+// flight, then stores each head's 32 dims as one coalesced 128-byte row piece.
+__device__ __forceinline__ void read_out(uint32_t tmem, uint32_t lane_base, int d_lane, int b0, int b1, float *dst,
+                                         const float *fin, int nh) {
+#pragma unroll 1
+  for (int b = b0; b < b1; ++b) {
+    uint32_t r[4][16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tc::tmem_ld_32x32b_x16(tmem + lane_base + 64 + 64 * b + 16 * q, r[q]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tc::tmem_ld_wait_x16(r[q]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (16 * q + i < nh) dst[(16 * q + i) * kLat + 128 * b + d_lane] = __uint_as_float(r[q][i]) * fin[16 * q + i];
+  }
+}
+__device__ __forceinline__ void bar_ro() { asm volatile("bar.sync 3, 256;\n" ::: "memory"); }
+
+struct __align__(1024) TcAttnSmem {
+  uint8_t q[kQBytes];
+  uint8_t tile[kTcStages][kTileBytes];
+  uint8_t p[2][kPBytes];
+  __align__(16) float qf[kTcHeads];    // logit factor of head h: 2^e_h * sm_scale * log2(e)
+  __align__(16) float alpha[kTcHeads]; // this chunk's rescale of head h's O^T column (1: none)
+  __align__(16) float fin[kTcHeads];   // output factor of head h (one-segment rows)
+  __align__(16) float sig[kTcStages][kE];  // 2^sigma_j of entry j of a stage (read as float4); 0 = empty entry
+  __align__(16) float sgm[kTcStages][kE];  // sigma_j (-inf for an empty entry)
+  int16_t chunk_id[kMaxChunks];
+  int8_t seg_end[kMaxChunks];    // the segment a chunk ends, or -1
+  int8_t seg_first[kMaxChunks];  // 1: a segment's first chunk
+  int32_t sel[kMaxChunks][kE];   // selected index of entry e of local chunk i (-1: none)
+  int nchunks;
+  uint32_t tmem;
+  float *ro_dst;  // the last segment's O rows (partial or output), for the producer warps' share
+  int ro_alive;
+  __align__(8) uint64_t full[kTcStages];
+  __align__(8) uint64_t empty[kTcStages];
+  __align__(8) uint64_t s_full[2];
+  __align__(8) uint64_t p_full[2];
+  __align__(8) uint64_t pv_done[2];
+  __align__(8) uint64_t q_ready;
+  __align__(8) uint64_t o_free;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta, int n_seg, float *part_ws) {
+  extern __shared__ uint8_t smem_raw[];
+  TcAttnSmem &sm = *reinterpret_cast<TcAttnSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kTcHeads;
+  const int nh = min(kTcHeads, a.heads - hbase);
+  const int seq = a.cache_seq < 0 ? row : a.cache_seq;
+  const int kpad = (a.k + kE - 1) / kE * kE;
+  const int total_chunks = (kpad + kWin) / kE;
+
+  if (warp == kTcMmaWarp) {
+    tc::tmem_alloc(&sm.tmem, kTcCols);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      tc::mbar_init(&sm.full[i], kProdThreads);
+      tc::mbar_init(&sm.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm.s_full[i], 1);
+      tc::mbar_init(&sm.p_full[i], 4);
+      tc::mbar_init(&sm.pv_done[i], 1);
+    }
+    tc::mbar_init(&sm.q_ready, 8);
+    tc::mbar_init(&sm.o_free, 4);
+    tc::fence_mbar_init();
+    int n = 0;
+    for (int sg = cta; sg < n_seg; sg += n_cta) {
+      for (int ch = sg; ch < total_chunks && n < kMaxChunks; ch += n_seg) {
+        sm.chunk_id[n] = static_cast<int16_t>(ch);
+        sm.seg_end[n] = -1;
+        sm.seg_first[n] = ch == sg ? 1 : 0;
+        ++n;
+      }
+      if (n > 0) sm.seg_end[n - 1] = static_cast<int8_t>(sg);
+    }
+    sm.nchunks = n;
+  }
+  // a programmatic dependent of the previous kernel: nothing in memory is read
+  // before that grid is complete
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const int nchunks = sm.nchunks;
+  const int64_t qpos = a.q_pos[row];
+  const int64_t T = qpos / a.ratio;
+  const int64_t ntok = a.n_tokens[seq];
+  const int64_t lin_base = a.lin_base ? *a.lin_base : INT64_MAX;
+
+  // the query to fp16 with a power-of-two scale per head (|q * 2^-e| < 2^15):
+  // warps 0-3 and 8-11 convert eight heads each (qw, qw + 8, ...), every raw
+  // value of the eight requested before any is used (one round trip)
+  if (warp < 4 || warp >= kTcMmaWarp) {
+    constexpr int kQW = kTcHeads / 8, kQP = kDqk / 2 / 32;
+    const int qw = warp < 4 ? warp : warp - 4;
+    uint32_t raw[kQW][kQP];
+#pragma unroll
+    for (int j = 0; j < kQW; ++j) {
+      const int h = qw + 8 * j;
+      const uint32_t *gq =
+          reinterpret_cast<const uint32_t *>(a.q + (static_cast<size_t>(row) * a.heads + hbase + h) * kDqk);
+#pragma unroll
+      for (int i = 0; i < kQP; ++i) raw[j][i] = h < nh ? __ldg(gq + lane + 32 * i) : 0u;
+    }
+    float amax[kQW];
+#pragma unroll
+    for (int j = 0; j < kQW; ++j) {
+      amax[j] = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kQP; ++i)
+        amax[j] = fmaxf(amax[j], fmaxf(fabsf(__uint_as_float(raw[j][i] << 16)),
+                                       fabsf(__uint_as_float(raw[j][i] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+      for (int j = 0; j < kQW; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+#pragma unroll
+    for (int j = 0; j < kQW; ++j) {
+      const int h = qw + 8 * j;
+      int ex = amax[j] > 0.0f ? floor_log2f(amax[j]) - 14 : 0;
+      ex = max(ex, -110);
+      const float inv = pow2f(-ex);
+#pragma unroll
+      for (int i = 0; i < kQP; ++i) {
+        __half2 t2 = __floats2half2_rn(__fmul_rn(__uint_as_float(raw[j][i] << 16), inv),
+                                       __fmul_rn(__uint_as_float(raw[j][i] & 0xFFFF0000u), inv));
+        *reinterpret_cast<__half2 *>(sm.q + q_off(h, 2 * (lane + 32 * i))) = t2;
+      }
+      if (lane == 0) sm.qf[h] = h < nh ? pow2f(ex) * a.sm_scale * kLog2e : 0.0f;
+    }
+    tc::fence_proxy_async_smem();  // Q is read by the tensor cores
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&sm.q_ready);
+  }
+
+  if (warp >= 4 && warp < 8) {
+    // ================================================================ producers
+    const int pt = tid - 128;
+    const int e = pt >> 2, q4 = pt & 3;
+    const uint32_t qmask = 0xFu << (lane & ~3);
+    const int32_t *idx_row = a.idx + static_cast<size_t>(row) * a.k;
+    // the selected indices of every chunk of this CTA, loaded once (one round
+    // trip) into shared memory: a chunk's record address is then known at once
+    for (int i = pt; i < nchunks * kE; i += kProdThreads) {
+      const int j = sm.chunk_id[i / kE] * kE + i % kE;
+      sm.sel[i / kE][i % kE] = j < a.k ? idx_row[j] : -1;
+    }
+    asm volatile("bar.sync 4, %0;\n" ::"r"(kProdThreads) : "memory");
+    auto sel_of = [&](int i) -> int32_t { return sm.sel[i][e]; };
+    // two chunks in flight: chunk c is dequantised from one record buffer while
+    // chunk c + 1's loads land in the other; chunk c + 2's are then issued into
+    // the first (no register copies, so no wait on a load before its use)
+    const bool fp8 = a.entry_format == CSA2_ENTRY_FP8;
+    struct Rec {
+      int kind;
+      int64_t src;
+      Fp4Raw raw;
+    };
+    auto fetch = [&](int c, Rec &r) {  // chunk c's record: FP4 into registers, other kinds into L2
+      r.kind = entry_kind(a, seq, sm.chunk_id[c] * kE + e, kpad, sel_of(c), qpos, T, ntok, lin_base, r.src);
+      if (r.kind == 1 && !fp8) load_fp4_early(a, r.src, q4, r.raw);
+      else prefetch_entry(a, r.kind, r.src, q4, fp8);
+    };
+    bool dead = false;
+    auto produce = [&](int c, Rec &r) {
+      const int ts = c % kTcStages;
+      if (c >= kTcStages && !dead) dead = !wait_warp(&sm.empty[ts], ((c / kTcStages) - 1) & 1, a.err);
+      if (!dead) {
+        uint8_t *tile = sm.tile[ts];
+        const float sig = dequant_entry(a, r.kind, r.src, r.raw, q4, qmask, fp8, [&](int u, uint4 lo, uint4 hi) {
+          *reinterpret_cast<uint4 *>(tile + t_off(e, 16 * u)) = lo;
+          *reinterpret_cast<uint4 *>(tile + t_off(e, 16 * u + 8)) = hi;
+        });
+        if (q4 == 0) {
+          sm.sig[ts][e] = sig;
+          sm.sgm[ts][e] = sig > 0.0f ? static_cast<float>(floor_log2f(sig)) : -INFINITY;
+        }
+      }
+      tc::fence_proxy_async_smem();  // the tile is read by the tensor cores
+      tc::mbar_arrive(&sm.full[ts]);
+      if (c + 2 < nchunks) fetch(c + 2, r);
+    };
+    Rec ra, rb;
+    if (nchunks > 0) fetch(0, ra);
+    if (nchunks > 1) fetch(1, rb);
+    for (int c = 0; c < nchunks; c += 2) {
+      produce(c, ra);
+      if (c + 1 < nchunks) produce(c + 1, rb);
+    }
+    if (nchunks > 0) {
+      // blocks 2, 3 of the last segment's O^T (warp 4 + w reads TMEM lanes 32 w ..)
+      bar_ro();
+      tc::tc_fence_after();
+      if (sm.ro_alive)
+        read_out(tmem, static_cast<uint32_t>(32 * (warp - 4)) << 16, 32 * (warp - 4) + lane, 2, 4, sm.ro_dst, sm.fin, nh);
+      tc::tc_fence_before();
+    }
+  } else if (warp == kTcMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_f16(64, kE, 0), idO = idesc_f16(128, kTcHeads, 1);
+      const uint32_t qa = tc::smem_addr(sm.q);
+      bool dead = !tc::mbar_wait_bounded(&sm.q_ready, 0, kWaitIters);
+      auto issue_qk = [&](int c) {
+        const int ts = c % kTcStages, sb = c & 1;
+        if (dead || !tc::mbar_wait_bounded(&sm.full[ts], (c / kTcStages) & 1, kWaitIters)) {
+          dead = true;
+          return;
+        }
+        tc::tc_fence_after();
+        const uint32_t ta = tc::smem_addr(sm.tile[ts]);
+#pragma unroll 4
+        for (int kk = 0; kk < kDqk / 16; ++kk)
+          mma_f16_ss(tmem + 32 * sb, tc::smem_desc_noswizzle(qa + kk * 2048, 1024, 128),
+                     tc::smem_desc_noswizzle(ta + kk * 1024, 512, 128), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(&sm.s_full[sb]);
+      };
+      if (nchunks > 0) issue_qk(0);
+      if (nchunks > 1) issue_qk(1);
+      int seg_ends = 0;
+      for (int c = 0; c < nchunks && !dead; ++c) {
+        const int ts = c % kTcStages, sb = c & 1;
+        if (!tc::mbar_wait_bounded(&sm.p_full[sb], (c >> 1) & 1, kWaitIters)) {
+          dead = true;
+          break;
+        }
+        const bool first = sm.seg_first[c] != 0;
+        if (first && c > 0 && !tc::mbar_wait_bounded(&sm.o_free, (seg_ends++) & 1, kWaitIters)) {
+          dead = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t ta = tc::smem_addr(sm.tile[ts]), pa = tc::smem_addr(sm.p[sb]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            mma_f16_ss(tmem + 64 + 64 * b, tc::smem_desc_noswizzle(ta + 8192 * b + 256 * ks, 128, 512),
+                       tc::smem_desc_noswizzle(pa + 2048 * ks, 1024, 128), idO, (first && ks == 0) ? 0u : 1u);
+        tc::mma_commit(&sm.empty[ts]);
+        tc::mma_commit(&sm.pv_done[sb]);
+        if (c + 2 < nchunks) issue_qk(c + 2);
+      }
+      if (dead) raise_err(a.err, CSA2_DEVERR_TIMEOUT);
+    }
+  } else if (warp < 4) {
+    // ================================================================ softmax / O^T (warps 0-3)
+    const bool head_thread = lane < 16;
+    const int h = 16 * warp + lane;  // this thread's head (head_thread)
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    float m_ref = -INFINITY, l_run = 0.0f;
+    bool dead = !wait_warp(&sm.q_ready, 0, a.err);  // qf of every head written
+    const float qf = head_thread ? sm.qf[h] : 0.0f;
+    for (int c = 0; c < nchunks; ++c) {
+      const int ts = c % kTcStages, sb = c & 1;
+      // P buffer sb is free once PV of chunk c - 2 is complete
+      if (c >= 2 && !dead) dead = !wait_warp(&sm.pv_done[sb], ((c - 2) >> 1) & 1, a.err);
+      if (!dead) dead = !wait_warp(&sm.s_full[sb], (c >> 1) & 1, a.err);
+      tc::tc_fence_after();
+      uint32_t sv[32];
+      tc::tmem_ld_32x32b_x16(tmem + lane_base + 32 * sb, sv);
+      tc::tmem_ld_32x32b_x16(tmem + lane_base + 32 * sb + 16, sv + 16);
+      tc::tmem_ld_wait_x16(sv);
+      tc::tmem_ld_wait_x16(sv + 16);
+      int moved = 0;
+      if (head_thread && !dead) {
+        // logits z_j = s_j qf 2^sigma_j (in place of s_j), and the largest
+        // weighted logit z_j + sigma_j, which bounds P_j 2^sigma_j
+        float my = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kE; j += 4) {
+          const float4 g4 = *reinterpret_cast<const float4 *>(&sm.sig[ts][j]);
+          const float4 s4 = *reinterpret_cast<const float4 *>(&sm.sgm[ts][j]);
+          const float g[4] = {g4.x, g4.y, g4.z, g4.w}, sg[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float zz = g[i] > 0.0f ? __uint_as_float(sv[j + i]) * qf * g[i] : -INFINITY;
+            sv[j + i] = __float_as_uint(zz);
+            my = fmaxf(my, zz + sg[i]);
+          }
+        }
+        float m_new = m_ref, alpha = 1.0f;
+        if (my != -INFINITY) {
+          if (m_ref == -INFINITY) {
+            m_new = my;  // this head's first entries: O^T's column is still zero
+          } else if (my > m_ref + kSlack) {
+            m_new = my;
+            alpha = exp2f(m_ref - m_new);
+            moved = 1;
+          }
+        }
+        float sum = 0.0f;
+        uint8_t *pb = sm.p[sb];
+        const float mz = m_new == -INFINITY ? 0.0f : m_new;  // exp2(-inf - mz) = 0 for every empty entry
+#pragma unroll
+        for (int j = 0; j < kE; j += 8) {
+          const float4 ga = *reinterpret_cast<const float4 *>(&sm.sig[ts][j]);
+          const float4 gb = *reinterpret_cast<const float4 *>(&sm.sig[ts][j + 4]);
+          const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float p0 = exp2f(__uint_as_float(sv[j + i]) - mz);
+            const float p1 = exp2f(__uint_as_float(sv[j + i + 1]) - mz);
+            sum += p0 + p1;
+            __half2 h2 = __floats2half2_rn(p0 * g[i], p1 * g[i + 1]);
+            w[i / 2] = *reinterpret_cast<uint32_t *>(&h2);
+          }
+          *reinterpret_cast<uint4 *>(pb + p_off(h, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l_run = l_run * alpha + sum;
+        m_ref = m_new;
+        sm.alpha[h] = alpha;
+      }
+      // some head moved its reference: its O^T column is rescaled once PV of
+      // chunk c - 1 is complete (a segment's first chunk restarts O^T instead)
+      if (bar_sm_or(moved) && !sm.seg_first[c]) {
+        if (!dead) dead = !wait_warp(&sm.pv_done[sb ^ 1], ((c - 1) >> 1) & 1, a.err);
+        tc::tc_fence_after();
+#pragma unroll 1
+        for (int b = 0; b < 4; ++b)
+#pragma unroll 1
+          for (int h0 = 0; h0 < kTcHeads; h0 += 16) {
+            uint32_t r[16];
+            const uint32_t ta = tmem + lane_base + 64 + 64 * b + h0;
+            tc::tmem_ld_32x32b_x16(ta, r);
+            tc::tmem_ld_wait_x16(r);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * sm.alpha[h0 + i]);
+            tmem_st_32x32b_x16(ta, r);
+          }
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+      }
+      tc::fence_proxy_async_smem();  // P is read by the tensor cores
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.p_full[sb]);
+      const int seg = sm.seg_end[c];
+      if (seg >= 0) {
+        // ---- the segment ends: its O^T is complete once PV of chunk c is
+        if (!dead) dead = !wait_warp(&sm.pv_done[sb], (c >> 1) & 1, a.err);
+        tc::tc_fence_after();
+        const int alive = bar_sm_and(dead ? 0 : 1);
+        float *dst = nullptr;  // O[h][d] rows of this segment (or of the output)
+        if (n_seg > 1) {
+          float *mine = part_ws + (static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg + seg) * part_floats<kTcHeads>();
+          if (head_thread)
+            *reinterpret_cast<float2 *>(mine + kTcHeads * kLat + 2 * h) =
+                alive ? make_float2(m_ref, l_run) : make_float2(-INFINITY, 0.0f);
+          dst = mine;
+          if (tid < kTcHeads) sm.fin[tid] = 1.0f;
+        } else {
+          if (head_thread) {
+            float m = m_ref, l = l_run, f = 1.0f;
+            if (h < nh && a.sink) {
+              const float s2 = a.sink[hbase + h] * kLog2e;
+              const float mf = fmaxf(m, s2);
+              f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
+              l = l * f + exp2f(s2 - mf);
+              m = mf;
+            }
+            sm.fin[h] = l > 0.0f ? f / l : 0.0f;
+            if (h < nh && alive)
+              a.lse[static_cast<size_t>(row) * a.heads + hbase + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+          }
+          dst = a.out + static_cast<size_t>(row) * a.heads * kLat + static_cast<size_t>(hbase) * kLat;
+        }
+        if (c == nchunks - 1) {
+          // the CTA's last segment: the producer warps (done) read out blocks 2, 3
+          if (tid == 0) {
+            sm.ro_dst = dst;
+            sm.ro_alive = alive;
+          }
+          bar_ro();  // fin, ro_dst and ro_alive written; the producers join here
+          if (alive) read_out(tmem, lane_base, 32 * warp + lane, 0, 2, dst, sm.fin, nh);
+        } else {
+          bar_sm();  // fin of every head written
+          if (alive) read_out(tmem, lane_base, 32 * warp + lane, 0, 4, dst, sm.fin, nh);
+        }
+        tc::tc_fence_before();
+        bar_sm();  // every read of O^T and of fin done
+        if (lane == 0) tc::mbar_arrive(&sm.o_free);
+        m_ref = -INFINITY;
+        l_run = 0.0f;
+      }
+    }
+  }
+
+  // ---- teardown of the tensor memory, then the merge of the row's segments
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMmaWarp) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTcCols);
+  }
+  if (n_seg > 1) {
+    cluster_sync();
+    const float *part_row = part_ws + static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg * part_floats<kTcHeads>();
+    if (n_seg <= 4)
+      merge_heads<4, 2, kTcHeads>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kTcThreads / 32, lane);
+    else
+      merge_heads<kMaxSeg, 1, kTcHeads>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kTcThreads / 32, lane);
+  }
+}
+
+cudaError_t launch_tc(const AttnArgs &a, int n_cta, int n_seg, float *part, cudaStream_t st) {
+  const int smem = static_cast<int>(sizeof(TcAttnSmem)) + 1024;
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_attn_tc), smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_cta, a.rows, (a.heads + kTcHeads - 1) / kTcHeads);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = n_cta;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_attn_tc, a, n_cta, n_seg, part);
+}
+
 int head_blocks(int heads, int hp) { return (heads + hp - 1) / hp; }
 
 // Launch shape: G CTAs per (row, head block), one cluster, and hp heads per CTA.
@@ -821,6 +1425,11 @@ cudaError_t launch_attn(const AttnArgs &a0, int n_seg, void *ws, size_t ws_bytes
                     reinterpret_cast<uintptr_t>(ws) % 16 != 0))
     return cudaErrorInvalidValue;
   float *part = static_cast<float *>(ws);
+  // one-segment rows (the chunked prefill: a query's whole entry list in one
+  // CTA) on the tensor-core kernel; decode rows on the mma.sync kernel, whose
+  // O stays in registers (the segments' read-out and merge cost more from TMEM
+  // than the faster contractions save on a 5-chunk segment)
+  if (n_seg == 1) return launch_tc(a0, 1, 1, part, st);
   if (sh.hp == 16) return launch_hp<16>(a0, sh.n_cta, n_seg, part, st);
   if (sh.hp == 32) return launch_hp<32>(a0, sh.n_cta, n_seg, part, st);
   return launch_hp<64>(a0, sh.n_cta, n_seg, part, st);
