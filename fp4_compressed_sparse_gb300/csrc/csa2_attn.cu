@@ -823,9 +823,9 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
 }
 
 // ============================================================================ tensor-core kernel
-// The same schedule (segments of a row, one cluster per row and 64 heads, the
-// ordered merge; the library launches it on one-segment rows) with both
-// contractions on the 5th-generation tensor cores:
+// One-segment rows (the chunked prefill): one CTA = one query row and 64 heads,
+// the row's chunks in order, with both contractions on the 5th-generation tensor
+// cores:
 // tcgen05.mma kind::f16, fp16 operands in shared memory, fp32 accumulators in
 // tensor memory (TMEM).
 //   S = Q K^T        M = 64 heads, N = 32 entries, K = 576 (36 MMAs); head h's
@@ -835,8 +835,9 @@ __global__ void __launch_bounds__(HP * 4 + kProdThreads, 1) k_attn(AttnArgs a, i
 //                    block b in TMEM columns 64 + 64 b, dim 128 b + lane
 // Roles (384 threads):
 //   warps 0-3  query to fp16 (once); per chunk the softmax (lanes 0-15 of warp
-//              w: heads 16w .. 16w + 15) and, at a segment's end, the O^T
-//              read-out (every thread one TMEM lane); P (fp16, times the
+//              w: heads 16w .. 16w + 15) and, after the last chunk, the
+//              normalised O read-out of blocks 0, 1 (every thread one TMEM
+//              lane; the producer warps read blocks 2, 3); P (fp16, times the
 //              entry's 2^sigma) goes to shared memory as the B operand.  A
 //              head's reference max moves only when some 2^sigma-weighted logit
 //              of the chunk would exceed it by more than 2^kSlack; O^T's column
@@ -914,7 +915,6 @@ __device__ __forceinline__ int bar_sm_and(int v) {
       : "memory");
   return r;
 }
-__device__ __forceinline__ void bar_sm() { asm volatile("bar.sync 2, 128;\n" ::: "memory"); }
 
 // Read-out of O^T blocks [b0, b1) of one TMEM lane quarter into O rows:
 // dst[h * 512 + 128 b + d] = O^T[d][h] * fin[h] for the heads h < nh; the warp
@@ -947,29 +947,25 @@ struct __align__(1024) TcAttnSmem {
   __align__(16) float fin[kTcHeads];   // output factor of head h (one-segment rows)
   __align__(16) float sig[kTcStages][kE];  // 2^sigma_j of entry j of a stage (read as float4); 0 = empty entry
   __align__(16) float sgm[kTcStages][kE];  // sigma_j (-inf for an empty entry)
-  int16_t chunk_id[kMaxChunks];
-  int8_t seg_end[kMaxChunks];    // the segment a chunk ends, or -1
-  int8_t seg_first[kMaxChunks];  // 1: a segment's first chunk
-  int32_t sel[kMaxChunks][kE];   // selected index of entry e of local chunk i (-1: none)
-  int nchunks;
+  int32_t sel[kMaxChunks][kE];  // selected index of entry e of chunk i (-1: none)
   uint32_t tmem;
-  float *ro_dst;  // the last segment's O rows (partial or output), for the producer warps' share
-  int ro_alive;
+  int ro_alive;  // the row's result is valid (no wait ran out)
   __align__(8) uint64_t full[kTcStages];
   __align__(8) uint64_t empty[kTcStages];
   __align__(8) uint64_t s_full[2];
   __align__(8) uint64_t p_full[2];
   __align__(8) uint64_t pv_done[2];
   __align__(8) uint64_t q_ready;
-  __align__(8) uint64_t o_free;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta, int n_seg, float *part_ws) {
+// grid (rows, head blocks of 64)
+__global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   TcAttnSmem &sm = *reinterpret_cast<TcAttnSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cta = blockIdx.x, row = blockIdx.y, hbase = blockIdx.z * kTcHeads;
+  const int row = blockIdx.x, hbase = blockIdx.y * kTcHeads;
   const int nh = min(kTcHeads, a.heads - hbase);
+  float *out_rows = a.out + (static_cast<size_t>(row) * a.heads + hbase) * kLat;  // O[h][d] of this CTA's heads
   const int seq = a.cache_seq < 0 ? row : a.cache_seq;
   const int kpad = (a.k + kE - 1) / kE * kE;
   const int total_chunks = (kpad + kWin) / kE;
@@ -989,19 +985,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
       tc::mbar_init(&sm.pv_done[i], 1);
     }
     tc::mbar_init(&sm.q_ready, 8);
-    tc::mbar_init(&sm.o_free, 4);
     tc::fence_mbar_init();
-    int n = 0;
-    for (int sg = cta; sg < n_seg; sg += n_cta) {
-      for (int ch = sg; ch < total_chunks && n < kMaxChunks; ch += n_seg) {
-        sm.chunk_id[n] = static_cast<int16_t>(ch);
-        sm.seg_end[n] = -1;
-        sm.seg_first[n] = ch == sg ? 1 : 0;
-        ++n;
-      }
-      if (n > 0) sm.seg_end[n - 1] = static_cast<int8_t>(sg);
-    }
-    sm.nchunks = n;
   }
   // a programmatic dependent of the previous kernel: nothing in memory is read
   // before that grid is complete
@@ -1010,7 +994,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem;
-  const int nchunks = sm.nchunks;
+  const int nchunks = total_chunks;  // the row's chunks, in order
   const int64_t qpos = a.q_pos[row];
   const int64_t T = qpos / a.ratio;
   const int64_t ntok = a.n_tokens[seq];
@@ -1072,7 +1056,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
     // the selected indices of every chunk of this CTA, loaded once (one round
     // trip) into shared memory: a chunk's record address is then known at once
     for (int i = pt; i < nchunks * kE; i += kProdThreads) {
-      const int j = sm.chunk_id[i / kE] * kE + i % kE;
+      const int j = i;  // entry j of the row's list: chunk j / 32
       sm.sel[i / kE][i % kE] = j < a.k ? idx_row[j] : -1;
     }
     asm volatile("bar.sync 4, %0;\n" ::"r"(kProdThreads) : "memory");
@@ -1087,7 +1071,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
       Fp4Raw raw;
     };
     auto fetch = [&](int c, Rec &r) {  // chunk c's record: FP4 into registers, other kinds into L2
-      r.kind = entry_kind(a, seq, sm.chunk_id[c] * kE + e, kpad, sel_of(c), qpos, T, ntok, lin_base, r.src);
+      r.kind = entry_kind(a, seq, c * kE + e, kpad, sel_of(c), qpos, T, ntok, lin_base, r.src);
       if (r.kind == 1 && !fp8) load_fp4_early(a, r.src, q4, r.raw);
       else prefetch_entry(a, r.kind, r.src, q4, fp8);
     };
@@ -1122,7 +1106,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
       bar_ro();
       tc::tc_fence_after();
       if (sm.ro_alive)
-        read_out(tmem, static_cast<uint32_t>(32 * (warp - 4)) << 16, 32 * (warp - 4) + lane, 2, 4, sm.ro_dst, sm.fin, nh);
+        read_out(tmem, static_cast<uint32_t>(32 * (warp - 4)) << 16, 32 * (warp - 4) + lane, 2, 4, out_rows, sm.fin, nh);
       tc::tc_fence_before();
     }
   } else if (warp == kTcMmaWarp) {
@@ -1147,18 +1131,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
       };
       if (nchunks > 0) issue_qk(0);
       if (nchunks > 1) issue_qk(1);
-      int seg_ends = 0;
       for (int c = 0; c < nchunks && !dead; ++c) {
         const int ts = c % kTcStages, sb = c & 1;
         if (!tc::mbar_wait_bounded(&sm.p_full[sb], (c >> 1) & 1, kWaitIters)) {
           dead = true;
           break;
         }
-        const bool first = sm.seg_first[c] != 0;
-        if (first && c > 0 && !tc::mbar_wait_bounded(&sm.o_free, (seg_ends++) & 1, kWaitIters)) {
-          dead = true;
-          break;
-        }
+        const bool first = c == 0;
         tc::tc_fence_after();
         const uint32_t ta = tc::smem_addr(sm.tile[ts]), pa = tc::smem_addr(sm.p[sb]);
 #pragma unroll
@@ -1243,8 +1222,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
         sm.alpha[h] = alpha;
       }
       // some head moved its reference: its O^T column is rescaled once PV of
-      // chunk c - 1 is complete (a segment's first chunk restarts O^T instead)
-      if (bar_sm_or(moved) && !sm.seg_first[c]) {
+      // chunk c - 1 is complete (the first chunk starts O^T instead)
+      if (bar_sm_or(moved) && c > 0) {
         if (!dead) dead = !wait_warp(&sm.pv_done[sb ^ 1], ((c - 1) >> 1) & 1, a.err);
         tc::tc_fence_after();
 #pragma unroll 1
@@ -1265,93 +1244,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_attn_tc(AttnArgs a, int n_cta
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.p_full[sb]);
-      const int seg = sm.seg_end[c];
-      if (seg >= 0) {
-        // ---- the segment ends: its O^T is complete once PV of chunk c is
+      if (c == nchunks - 1) {
+        // ---- the last chunk: O^T is complete once its PV is; normalise (with
+        // the sink) and write the row's output, blocks 0, 1 here and 2, 3 by the
+        // producer warps
         if (!dead) dead = !wait_warp(&sm.pv_done[sb], (c >> 1) & 1, a.err);
         tc::tc_fence_after();
         const int alive = bar_sm_and(dead ? 0 : 1);
-        float *dst = nullptr;  // O[h][d] rows of this segment (or of the output)
-        if (n_seg > 1) {
-          float *mine = part_ws + (static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg + seg) * part_floats<kTcHeads>();
-          if (head_thread)
-            *reinterpret_cast<float2 *>(mine + kTcHeads * kLat + 2 * h) =
-                alive ? make_float2(m_ref, l_run) : make_float2(-INFINITY, 0.0f);
-          dst = mine;
-          if (tid < kTcHeads) sm.fin[tid] = 1.0f;
-        } else {
-          if (head_thread) {
-            float m = m_ref, l = l_run, f = 1.0f;
-            if (h < nh && a.sink) {
-              const float s2 = a.sink[hbase + h] * kLog2e;
-              const float mf = fmaxf(m, s2);
-              f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
-              l = l * f + exp2f(s2 - mf);
-              m = mf;
-            }
-            sm.fin[h] = l > 0.0f ? f / l : 0.0f;
-            if (h < nh && alive)
-              a.lse[static_cast<size_t>(row) * a.heads + hbase + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        if (head_thread) {
+          float m = m_ref, l = l_run, f = 1.0f;
+          if (h < nh && a.sink) {
+            const float s2 = a.sink[hbase + h] * kLog2e;
+            const float mf = fmaxf(m, s2);
+            f = (m == -INFINITY) ? 0.0f : exp2f(m - mf);
+            l = l * f + exp2f(s2 - mf);
+            m = mf;
           }
-          dst = a.out + static_cast<size_t>(row) * a.heads * kLat + static_cast<size_t>(hbase) * kLat;
+          sm.fin[h] = l > 0.0f ? f / l : 0.0f;
+          if (h < nh && alive)
+            a.lse[static_cast<size_t>(row) * a.heads + hbase + h] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
         }
-        if (c == nchunks - 1) {
-          // the CTA's last segment: the producer warps (done) read out blocks 2, 3
-          if (tid == 0) {
-            sm.ro_dst = dst;
-            sm.ro_alive = alive;
-          }
-          bar_ro();  // fin, ro_dst and ro_alive written; the producers join here
-          if (alive) read_out(tmem, lane_base, 32 * warp + lane, 0, 2, dst, sm.fin, nh);
-        } else {
-          bar_sm();  // fin of every head written
-          if (alive) read_out(tmem, lane_base, 32 * warp + lane, 0, 4, dst, sm.fin, nh);
-        }
+        if (tid == 0) sm.ro_alive = alive;
+        bar_ro();  // fin and ro_alive written; the producer warps join here
+        if (alive) read_out(tmem, lane_base, 32 * warp + lane, 0, 2, out_rows, sm.fin, nh);
         tc::tc_fence_before();
-        bar_sm();  // every read of O^T and of fin done
-        if (lane == 0) tc::mbar_arrive(&sm.o_free);
-        m_ref = -INFINITY;
-        l_run = 0.0f;
       }
     }
   }
 
-  // ---- teardown of the tensor memory, then the merge of the row's segments
+  // ---- teardown of the tensor memory
   tc::tc_fence_before();
   __syncthreads();
   if (warp == kTcMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTcCols);
   }
-  if (n_seg > 1) {
-    cluster_sync();
-    const float *part_row = part_ws + static_cast<size_t>(row * gridDim.z + blockIdx.z) * n_seg * part_floats<kTcHeads>();
-    if (n_seg <= 4)
-      merge_heads<4, 2, kTcHeads>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kTcThreads / 32, lane);
-    else
-      merge_heads<kMaxSeg, 1, kTcHeads>(a, part_row, row, hbase, nh, cta, n_cta, n_seg, warp, kTcThreads / 32, lane);
-  }
 }
 
-cudaError_t launch_tc(const AttnArgs &a, int n_cta, int n_seg, float *part, cudaStream_t st) {
+cudaError_t launch_tc(const AttnArgs &a, cudaStream_t st) {
   const int smem = static_cast<int>(sizeof(TcAttnSmem)) + 1024;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void *>(k_attn_tc), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_cta, a.rows, (a.heads + kTcHeads - 1) / kTcHeads);
+  cfg.gridDim = dim3(a.rows, (a.heads + kTcHeads - 1) / kTcHeads);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = n_cta;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_attn_tc, a, n_cta, n_seg, part);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_attn_tc, a);
 }
 
 int head_blocks(int heads, int hp) { return (heads + hp - 1) / hp; }
@@ -1429,7 +1373,7 @@ cudaError_t launch_attn(const AttnArgs &a0, int n_seg, void *ws, size_t ws_bytes
   // CTA) on the tensor-core kernel; decode rows on the mma.sync kernel, whose
   // O stays in registers (the segments' read-out and merge cost more from TMEM
   // than the faster contractions save on a 5-chunk segment)
-  if (n_seg == 1) return launch_tc(a0, 1, 1, part, st);
+  if (n_seg == 1) return launch_tc(a0, st);
   if (sh.hp == 16) return launch_hp<16>(a0, sh.n_cta, n_seg, part, st);
   if (sh.hp == 32) return launch_hp<32>(a0, sh.n_cta, n_seg, part, st);
   return launch_hp<64>(a0, sh.n_cta, n_seg, part, st);
