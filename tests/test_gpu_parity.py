@@ -492,13 +492,14 @@ def test_encoder_group_decode_steps(orc):
 
 
 # ------------------------------------------------------------------ prefill (small)
-@pytest.mark.parametrize("prior,Q,H_I", [
-    (300, 70, 4),
-    (300, 71, 64),   # 64 indexer heads (the workloads' count), an odd chunk
-    (301, 40, 64),   # odd prior: a token waits in the compression buffer
+@pytest.mark.parametrize("prior,Q,H_I,H,use_sink", [
+    (300, 70, 4, 16, False),
+    (300, 71, 64, 16, False),   # 64 indexer heads (the workloads' count), an odd chunk
+    (301, 40, 64, 16, False),   # odd prior: a token waits in the compression buffer
+    (301, 33, 16, 96, True),    # two head blocks of the attention (64 + 32 padded), with a sink
 ])
-def test_prefill_chunk_small(orc, prior, Q, H_I):
-    H, k = 16, 32
+def test_prefill_chunk_small(orc, prior, Q, H_I, H, use_sink):
+    k = 32
     c, oc, rope, err, (ba, bb), _, _ = build_r2(orc, 2, prior, csa2.SWA_MXFP8, seed=61,
                                                chunks=[prior], cap=(prior + Q) // 2 + 8)
     seq = 1
@@ -507,13 +508,15 @@ def test_prefill_chunk_small(orc, prior, Q, H_I):
     q_idx = torch.randn((Q, H_I, 128), generator=g).to(torch.bfloat16)
     w = torch.rand((Q, H_I), generator=g)
     q = torch.randn((Q, H, 576), generator=g).to(torch.bfloat16)
+    sink = (torch.randn((H,), generator=g) * 2).float() if use_sink else None
     idx = torch.empty((Q, k), dtype=torch.int32, device="cuda")
     out = torch.empty((Q, H, 512), device="cuda")
     lse = torch.empty((Q, H), device="cuda")
     ws = csa2.prefill_workspace(Q, c.capacity, H_I, H, k)
     scale = 1 / math.sqrt(576)
     csa2.prefill_chunk(c, seq, [r.cuda() for r in rows] + [ba.cuda(), bb.cuda()], rope, q_idx.cuda(),
-                       w.cuda(), q.cuda(), k, scale, idx, out, lse, ws, err=err)
+                       w.cuda(), q.cuda(), k, scale, idx, out, lse, ws,
+                       sink=sink.cuda() if sink is not None else None, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     o = oc[seq]
@@ -540,5 +543,6 @@ def test_prefill_chunk_small(orc, prior, Q, H_I):
         toks = list(range(max(0, t - 127), t + 1))
         wc = np.array([(chunk_win[x] if x >= prior else prior_ring[x])[0] for x in toks])
         wsc = np.array([(chunk_win[x] if x >= prior else prior_ring[x])[1] for x in toks])
-        ro, rl = orc.sparse_attn(o, u16(q[i]), r_idx, t, scale, swa_codes=wc, swa_scales=wsc)
+        ro, rl = orc.sparse_attn(o, u16(q[i]), r_idx, t, scale, sink=sink.numpy() if sink is not None else None,
+                                 swa_codes=wc, swa_scales=wsc)
         attn_close(out[i].cpu().numpy(), lse[i].cpu().numpy(), ro, rl)
