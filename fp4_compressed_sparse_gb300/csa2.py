@@ -27,7 +27,7 @@ EXPORTS = [
     "csa2_score_aux_size", "csa2_index_score",
     "csa2_topk_workspace_size", "csa2_topk", "csa2_topk_noalloc", "csa2_attn_workspace_size", "csa2_sparse_attn_decode",
     "csa2_prefill_workspace_size", "csa2_prefill_chunk", "csa2_mask_to_pool", "csa2_mxf4_peak_launch",
-    "csa2_set_phase_events",
+    "csa2_bounded_wait_check", "csa2_set_phase_events",
     "csa2_phase_events_recorded", "csa2_status_string", "csa2_last_error_detail", "csa2_version",
 ]
 
@@ -94,6 +94,7 @@ def load() -> ctypes.CDLL:
                                      vp, vp, vp, vp, sz, vp, vp]),
         "csa2_mask_to_pool": (i32, [vp, i64, i32, i32, vp, vp, i32, i32, vp]),
         "csa2_mxf4_peak_launch": (i32, [i32, i32, vp, vp, vp]),
+        "csa2_bounded_wait_check": (i32, [i32, i32, vp, vp]),
         "csa2_set_phase_events": (i32, [vp, i32]),
         "csa2_phase_events_recorded": (i32, []),
         "csa2_status_string": (ctypes.c_char_p, [i32]),
@@ -347,6 +348,14 @@ def mxf4_peak_launch(n_ctas, iters, sink=None, err=None, stream=None):
     the caller times it: n_ctas * iters * 2 * 128 * 128 * 64 FLOP."""
     _check("csa2_mxf4_peak_launch", load().csa2_mxf4_peak_launch(n_ctas, iters, _ptr(sink), _ptr(err),
                                                                   _stream(stream)))
+
+
+def bounded_wait_check(iters, complete, err, stream=None):
+    """One warp holding tensor memory across the library's bounded mbarrier wait:
+    complete=True -> the wait succeeds; False -> it gives up after `iters` polls
+    (<= ~1 ms each) and ORs DEVERR_TIMEOUT into `err` (int32 device tensor)."""
+    _check("csa2_bounded_wait_check", load().csa2_bounded_wait_check(iters, 1 if complete else 0, _ptr(err),
+                                                                      _stream(stream)))
 
 
 _phase_keep = None

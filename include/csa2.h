@@ -386,6 +386,21 @@ csa2_status csa2_mxf4_peak_launch(int32_t n_ctas, int32_t iters, uint32_t *sink,
                                   csa2_stream_t stream);
 
 /*
+ * csa2_bounded_wait_check: self-check of the failure path (not a step of the
+ * method).  Every wait inside the library's kernels is bounded: a wait that
+ * runs out sets CSA2_DEVERR_TIMEOUT in the call's error word, the kernel frees
+ * its tensor memory and returns, and the context stays usable.  This launches
+ * one warp that holds 32 TMEM columns across the same bounded wait on an
+ * mbarrier that one arrival completes (complete = 1: the wait succeeds, no bit
+ * is set) or that nothing completes (complete = 0: the wait gives up after
+ * `iters` polls of at most ~1 ms each and sets the TIMEOUT bit), so that a host
+ * can see the bit arrive and keep using the device.  iters 1..64; err_word:
+ * device int32, 4-byte aligned, required (OR-ed into, never cleared).
+ * Asynchronous on `stream` like every other call.
+ */
+csa2_status csa2_bounded_wait_check(int32_t iters, int32_t complete, int32_t *err_word, csa2_stream_t stream);
+
+/*
  * csa2_set_phase_events: measurement helper.  events: n_events cudaEvent_t
  * (created by the caller, owned by it) that this thread's next
  * csa2_prefill_chunk calls record on their stream, in order, at the phase

@@ -130,6 +130,13 @@ def test_measurement_helpers_validate(lib):
     assert lib.csa2_mxf4_peak_launch(152, 1, None, None, None) == 2
     assert b"iters" in lib.csa2_last_error_detail()
     assert lib.csa2_set_phase_events(None, 3) == 1
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.csa2_bounded_wait_check(0, 0, fake, None) == 2
+    assert lib.csa2_bounded_wait_check(65, 0, fake, None) == 2
+    assert lib.csa2_bounded_wait_check(4, 2, fake, None) == 4
+    assert lib.csa2_bounded_wait_check(4, 0, None, None) == 1
+    assert lib.csa2_bounded_wait_check(4, 0, ctypes.c_void_p((1 << 20) + 2), None) == 3
+    assert b"4-byte" in lib.csa2_last_error_detail()
     assert lib.csa2_set_phase_events(None, 0) == 0 and lib.csa2_phase_events_recorded() == 0
 
 

@@ -1,6 +1,8 @@
-"""GPU checks of the measurement helpers: the FP4 tensor-core throughput kernel
-finishes without a device error, and the prefill records its phase events in
-order (start, append done, then scored / selected / attended per block)."""
+"""GPU checks of the measurement and self-check helpers: the FP4 tensor-core
+throughput kernel finishes without a device error; a bounded device wait that
+nothing completes returns with the TIMEOUT bit and leaves the context usable;
+the prefill records its phase events in order (start, append done, then
+scored / selected / attended per block)."""
 import math
 
 import pytest
@@ -30,6 +32,30 @@ def test_mxf4_peak_kernel_runs():
     assert int(err.item()) == 0
     tflops = sms * 4096 * 2.0 * 128 * 128 * 64 / (a.elapsed_time(b) / 1e3) / 1e12
     assert 100.0 < tflops < 40000.0
+
+
+def test_bounded_wait_timeout_reports_and_returns():
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.bounded_wait_check(4, True, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0  # completed barrier: the wait succeeds
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    csa2.bounded_wait_check(8, False, err)  # nothing arrives: gives up after 8 polls
+    b.record()
+    torch.cuda.synchronize()
+    assert int(err.item()) == csa2.DEVERR_TIMEOUT
+    assert a.elapsed_time(b) < 2000.0
+    # the context is intact and the timed-out warp gave its tensor memory back:
+    # a tensor-core kernel on every SM allocates all 512 columns and finishes
+    err.zero_()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    csa2.mxf4_peak_launch(sms, 64, None, err)
+    csa2.bounded_wait_check(1, True, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    x = torch.arange(1024, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 1023 * 1024 / 2
 
 
 def test_prefill_phase_events(orc):
