@@ -519,6 +519,10 @@ PrefillLayout prefill_layout(int Q, int capacity, int n_heads, int k, int swa_dt
   const int cb = swa_dtype == CSA2_SWA_MXFP8 ? 576 : 1152;
   // bound the score block to ~256 MB
   int qb = static_cast<int>((size_t(256) << 20) / (static_cast<size_t>(capacity) * 4));
+  // whole waves: the attention runs one CTA per query and SM, the selection two
+  // per SM, so a block of a multiple of 2 x SMs queries leaves no partial wave
+  const int wave = 2 * csa2::device_sm_count();
+  if (qb > wave) qb = qb / wave * wave;
   if (qb < 1) qb = 1;
   if (qb > Q) qb = Q;
   if (qb > 4096) qb = 4096;

@@ -355,7 +355,11 @@ csa2_status csa2_sparse_attn_decode(const csa2_cache *cache, const uint16_t *q, 
  *   cmp: rows [Q][704] for this sequence; q_idx bf16 [Q][n_heads_idx][128];
  *   w fp32 [Q][n_heads_idx]; q bf16 [Q][n_heads][576];
  *   idx_out int32 [Q][k]; out fp32 [Q][n_heads][512]; lse fp32 [Q][n_heads].
- * ws: device workspace of csa2_prefill_workspace_size() bytes.
+ * ws: device workspace of csa2_prefill_workspace_size() bytes (queries are
+ *   scored, selected and attended in blocks: the block holds ~256 MB of fp32
+ *   score rows, rounded down to a multiple of twice the current device's SM
+ *   count, so the size depends on the device the call runs on; query it with
+ *   that device current).
  * Each query's attention is one pass over its entries (one segment), so its
  * bits do not depend on the chunk's size either; they may differ in the last
  * bits from a decode step at the same position (csa2_sparse_attn_decode merges

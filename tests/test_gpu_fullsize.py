@@ -225,10 +225,14 @@ def test_prefill_q8192_prior131072(orc):
     for name, g in (("lat_codes", c.lat_codes), ("lat_scales", c.lat_scales), ("rope_codes", c.rope_codes),
                     ("rope_scales", c.rope_scales), ("idx_codes", ic), ("idx_scales", isc)):
         assert np.array_equal(g[0, :n_entries].cpu().numpy(), getattr(o, name)), f"prefill cache {name}"
-    # the chunk is scored in blocks of queries whose fp32 score rows fill 256 MB:
-    # the first and last query of every such block, of every 512-query span, and
-    # the middle of the chunk
-    qb = max(1, min(Q, 4096, (256 << 20) // (cap * 4)))
+    # the chunk is scored in blocks of queries whose fp32 score rows fill 256 MB,
+    # rounded down to a multiple of twice the SM count: the first and last query
+    # of every such block, of every 512-query span, and the middle of the chunk
+    qb = (256 << 20) // (cap * 4)
+    wave = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    if qb > wave:
+        qb = qb // wave * wave
+    qb = max(1, min(Q, 4096, qb))
     qs = {1, Q // 2 - 1, Q // 2}
     for span in (qb, 512):
         for q0 in range(0, Q, span):
