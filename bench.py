@@ -664,7 +664,8 @@ class GroupDecode:
 
     def step(self, s, marks=None):
         """One step; with `marks` (a list of events) the parts run in order on one stream
-        with an event before each layer's indexer part, each attention and the end."""
+        with an event before each layer's score, its top-k, its attention and at the end
+        (a Reuse layer records the first two back to back)."""
         c, W = self.csa2, self.W
         main = torch.cuda.current_stream()
         mark = (lambda: marks.pop(0).record()) if marks is not None else (lambda: None)
@@ -690,12 +691,14 @@ class GroupDecode:
             if role == "full":
                 c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.scores, err=self.err,
                               ws=self.ws_score, aux=self.aux)
+                mark()
                 c.topk(self.scores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_topk,
                        pool_out=self.pool if self.build_pool else None,
                        pool_count=self.pool_cnt if self.build_pool else None, err=self.err, aux=self.aux)
             elif role == "reindex":
                 c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.pscores,
                               pool=self.pool, err=self.err, ws=self.ws_score, aux=self.paux)
+                mark()
                 c.topk(self.pscores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_ptopk, pool=self.pool,
                        err=self.err, aux=self.paux)
             elif role == "reindex_masked":
@@ -703,8 +706,11 @@ class GroupDecode:
                 # mask the positions outside the pool, top-k of the whole row
                 c.index_score(self.cache, self.q_idx[s][l], self.w[s][l], self.q_pos[s], self.scores, err=self.err,
                               ws=self.ws_score)
+                mark()
                 c.mask_to_pool(self.scores, W.ratio, self.q_pos[s], self.pool, W.pool_block_size)
                 c.topk(self.scores, W.ratio, self.q_pos[s], W.topk, self.idx, self.ws_topk, err=self.err)
+            else:
+                mark()  # Reuse: no indexer
             if not joined:
                 main.wait_event(join)  # the attention reads the new token's window slot
                 joined = True
@@ -935,14 +941,15 @@ def _time_group(bench, W, steps, warmup, dev, first=0):
     ms = statistics.mean(step_ms)
     del graphs
     # per-layer breakdown: one more step, parts in order with events between
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(W.layers) + 1)]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(3 * len(W.layers) + 1)]
     flush()
     bench.step(first + warmup + steps, marks=list(marks))
     torch.cuda.synchronize()
     parts = []
     for l, role in enumerate(W.layers):
-        a, b, c2 = marks[2 * l], marks[2 * l + 1], marks[2 * l + 2]
+        a, m, b, c2 = marks[3 * l], marks[3 * l + 1], marks[3 * l + 2], marks[3 * l + 3]
         parts.append({"layer": l, "role": role, "indexer_ms": round(a.elapsed_time(b), 4),
+                      "score_ms": round(a.elapsed_time(m), 4), "topk_ms": round(m.elapsed_time(b), 4),
                       "attention_ms": round(b.elapsed_time(c2), 4)})
     hbm, hbm_kind = peaks()
     T = (W.context + first + warmup + steps // 2) // W.ratio  # visible entries at the middle step

@@ -48,6 +48,19 @@ __device__ __forceinline__ uint32_t key_of(float f) { return isnan(f) ? 0u : ord
 __device__ __forceinline__ float float_of_key(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
+// The lowest non-NaN value of histogram bin b > 0.  Keys below that of -inf
+// (0x007FFFFF) belong to negative NaN payloads, which rank as key 0: the bin
+// holding -inf starts at -inf, not at the NaN its first key decodes to.
+__device__ __forceinline__ float bin_low(uint32_t b) {
+  const uint32_t k = b << kSelBinShift;
+  return float_of_key(k > 0x007FFFFFu ? k : 0x007FFFFFu);
+}
+// The highest non-NaN value of bin b: keys above that of +inf (0xFF800000)
+// belong to positive NaN payloads.
+__device__ __forceinline__ float bin_high(uint32_t b) {
+  const uint32_t k = ((b + 1) << kSelBinShift) - 1;
+  return float_of_key(k < 0xFF800000u ? k : 0xFF800000u);
+}
 
 __device__ __forceinline__ int prob_k(const TopkArgs &a, int p) { return p == 0 ? a.k : a.out_pool_blocks; }
 
@@ -367,8 +380,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
     // order keys are monotone in the float value: "above the bin" is f > hi and
     // "in the bin" is lo <= f <= hi (exact, -0 == +0; NaN is neither, like its
     // key 0 when the threshold bin is above 0); slots outside the row read as NaN
-    const float lo = float_of_key(thr << kSelBinShift);
-    const float hi = float_of_key(((thr + 1) << kSelBinShift) - 1);
+    const float lo = bin_low(thr);
+    const float hi = bin_high(thr);
     for (int64_t w0 = w_lo + static_cast<int64_t>(warp) * kFB; w0 < w_hi; w0 += static_cast<int64_t>(kSelWarps) * kFB) {
       if (w0 != w_lo + static_cast<int64_t>(warp) * kFB) {
 #pragma unroll
@@ -664,8 +677,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const
   if (plain && thr > 0) {
     // "above the bin" is f > hi and "in the bin" lo <= f <= hi (order keys are
     // monotone in the float value; -0 == +0; NaN is neither)
-    const float lo = float_of_key(thr << kSelBinShift);
-    const float hi = float_of_key(((thr + 1) << kSelBinShift) - 1);
+    const float lo = bin_low(thr);
+    const float hi = bin_high(thr);
     for (int w0 = warp * kFB; w0 < nw; w0 += kRowWarps * kFB) {
       if (w0 != warp * kFB) {
 #pragma unroll

@@ -332,6 +332,42 @@ def test_topk_nan_score_is_reported(orc):
     assert 123 not in idx[0].tolist()
 
 
+@pytest.mark.parametrize("reps,k", [
+    (1, 512),   # 4 rows: 4-CTA clusters
+    (25, 512),  # 100 rows: one CTA per row
+    (1, 4),     # small k: the threshold bin sits among the finite or the +inf scores
+    (1, 5),
+])
+def test_topk_infinite_scores(orc, reps, k):
+    """Rows whose k-th score is -inf (fewer finite scores than k: the threshold
+    bin is the one that holds -inf), rows whose top is +inf (more +inf scores
+    than k: the bin that holds +inf), and infinities scattered in a normal row,
+    for the top-k and a 64-block pool, against the oracle."""
+    T, nblk = 6000, 64
+    rng = np.random.default_rng(77)
+    sc = rng.standard_normal((4, T)).astype(np.float32)
+    sc[0, 300:] = -np.inf
+    sc[1, rng.choice(T, 10, replace=False)] = np.inf
+    sc[1, rng.choice(T, 5, replace=False)] = -np.inf
+    sc[2, :] = -np.inf
+    sc[3, rng.choice(T, 600, replace=False)] = np.inf
+    sc = np.ascontiguousarray(np.tile(sc, (reps, 1)))
+    B = sc.shape[0]
+    q_pos = torch.full((B,), T, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    pool = torch.empty((B, nblk), dtype=torch.int32, device="cuda")
+    pcnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    csa2.topk(torch.from_numpy(sc).cuda(), 1, q_pos, k, idx, csa2.topk_workspace(B, T, k, nblk),
+              pool_out=pool, pool_count=pcnt, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for b in range(B):
+        assert idx[b].tolist() == orc.topk(sc[b], k).tolist(), f"row {b}: top-k"
+        pids, cnt = orc.pool(sc[b], T, 8, nblk)
+        assert int(pcnt[b].item()) == cnt and pool[b].tolist() == pids.tolist(), f"row {b}: pool"
+
+
 # ------------------------------------------------------------------ attention
 @pytest.mark.parametrize("B,T,H,k,swa_dtype,use_sink", [
     (3, 700, 64, 64, csa2.SWA_MXFP8, False),   # 4 segments, one per CTA; 16-head blocks
