@@ -285,7 +285,8 @@ csa2_status csa2_topk(const float *scores, int64_t score_stride, const void *sco
  * large batch x score_stride) return CSA2_ERR_WORKSPACE with the sizes in
  * csa2_last_error_detail().  The first call on each device looks up the
  * array's device address (a runtime query), so make that first call before any
- * stream capture.  Every call shares the array and leaves its contents behind
+ * stream capture; the address is kept for the process, so a cudaDeviceReset
+ * after that first call is not supported.  Every call shares the array and leaves its contents behind
  * (each call clears and rewrites what it reads): calls whose kernels may
  * overlap on the GPU -- different streams without ordering -- race.
  */
