@@ -382,6 +382,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
     // key 0 when the threshold bin is above 0); slots outside the row read as NaN
     const float lo = bin_low(thr);
     const float hi = bin_high(thr);
+    bool nan_seen = false;  // a NaN score in this lane's slots (reported once, after the pass)
     for (int64_t w0 = w_lo + static_cast<int64_t>(warp) * kFB; w0 < w_hi; w0 += static_cast<int64_t>(kSelWarps) * kFB) {
       if (w0 != w_lo + static_cast<int64_t>(warp) * kFB) {
 #pragma unroll
@@ -397,16 +398,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
         if (w >= w_hi) break;  // warp-uniform
         const float f = fb[b];
         const uint32_t slot = static_cast<uint32_t>(w * 32 + lane);
-        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && slot < nsu)) {
-          if (isnan(f) && slot < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
-        }
+        nan_seen |= isnan(f) && slot < nsu;
         const uint32_t word = __ballot_sync(0xffffffffu, f > hi);
         if (lane == 0) bm_local[w - w_lo] = word;
         const bool want = f >= lo && f <= hi;
-        add_cands(__ballot_sync(0xffffffffu, want), want,
-                  (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
+        const uint32_t mask = __ballot_sync(0xffffffffu, want);
+        if (mask)  // the candidate keys only where a word has any
+          add_cands(mask, want, (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
       }
     }
+    if (p == 0 && nan_seen) raise_err(a.err, CSA2_DEVERR_NAN);
   } else {
     for (int64_t w = w_lo + warp; w < w_hi; w += kSelWarps) {
       bool ok;
@@ -679,6 +680,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const
     // monotone in the float value; -0 == +0; NaN is neither)
     const float lo = bin_low(thr);
     const float hi = bin_high(thr);
+    bool nan_seen = false;  // a NaN score in this lane's slots (reported once, after the pass)
     for (int w0 = warp * kFB; w0 < nw; w0 += kRowWarps * kFB) {
       if (w0 != warp * kFB) {
 #pragma unroll
@@ -694,16 +696,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const
         if (w >= nw) break;  // warp-uniform
         const float f = fb[b];
         const uint32_t slot = static_cast<uint32_t>(w) * 32 + lane;
-        if (p == 0 && __any_sync(0xffffffffu, isnan(f) && slot < nsu)) {
-          if (isnan(f) && slot < nsu) raise_err(a.err, CSA2_DEVERR_NAN);
-        }
+        nan_seen |= isnan(f) && slot < nsu;
         const uint32_t word = __ballot_sync(0xffffffffu, f > hi);
         if (lane == 0) sm.bitmap[w] = word;
         const bool want = f >= lo && f <= hi;
-        add_cands(__ballot_sync(0xffffffffu, want), want,
-                  (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
+        const uint32_t mask = __ballot_sync(0xffffffffu, want);
+        if (mask)  // the candidate keys only where a word has any
+          add_cands(mask, want, (static_cast<uint64_t>(orderable(f)) << 32) | (0xFFFFFFFFu - slot));
       }
     }
+    if (p == 0 && nan_seen) raise_err(a.err, CSA2_DEVERR_NAN);
   } else {
     for (int w = warp; w < nw; w += kRowWarps) {
       bool ok;
