@@ -284,6 +284,33 @@ def test_topk_bruteforce_with_ties(orc, T, k):
     assert list(got) == want
 
 
+def test_topk_and_pool_with_infinities(orc):
+    """-inf is an ordinary lowest score and +inf an ordinary highest one: rows with
+    fewer finite scores than k, with more +inf scores than k, and mixed, against
+    Python's sort on (score desc, position asc) and the block maxima it implies."""
+    rng = np.random.default_rng(21)
+    T, k, nb_keep = 600, 64, 16
+    rows = []
+    a = rng.standard_normal(T).astype(np.float32)
+    a[30:] = -np.inf
+    rows.append(a)
+    b = rng.standard_normal(T).astype(np.float32)
+    b[rng.choice(T, 100, replace=False)] = np.inf
+    rows.append(b)
+    c = rng.standard_normal(T).astype(np.float32)
+    c[rng.choice(T, 7, replace=False)] = np.inf
+    c[rng.choice(T, 200, replace=False)] = -np.inf
+    rows.append(c)
+    rows.append(np.full(T, -np.inf, np.float32))
+    for s in rows:
+        ref = sorted(sorted(range(T), key=lambda i: (-float(s[i]), i))[:k])
+        assert list(orc.topk(s, k)) == ref
+        nb = (T + 7) // 8
+        bm = [max(float(x) for x in s[j * 8:min(T, j * 8 + 8)]) for j in range(nb)]
+        ids, cnt = orc.pool(s, T, 8, nb_keep)
+        assert cnt == nb_keep and list(ids) == sorted(sorted(range(nb), key=lambda j: (-bm[j], j))[:nb_keep])
+
+
 def test_topk_positions_and_nan(orc):
     s = np.array([1.0, 3.0, 3.0, 2.0], np.float32)
     pos = np.array([40, 7, 9, 100])
