@@ -31,6 +31,9 @@
 //      counts and writes the chosen positions in ascending order, -1 padded.
 // Slots run in ascending position order in every mode, so the bitmap order is
 // the output order and no sort is needed.
+// Launches with more (row, problem) pairs than one wave of such clusters holds
+// (the chunked prefill's query blocks) run k_select_row instead: the same steps
+// inside one 1024-thread CTA per (row, problem).
 #include "csa2_internal.cuh"
 
 namespace csa2 {
