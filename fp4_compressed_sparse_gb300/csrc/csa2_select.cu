@@ -430,17 +430,39 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
 
   // ---- 3. the leader gathers the candidates and selects the ones still needed
   if (rank == 0) {
-    uint32_t cnt[kSelClusterMax], off[kSelClusterMax], n = 0, ovf = 0;
-    for (uint32_t r = 0; r < static_cast<uint32_t>(ncl); ++r) {
-      cnt[r] = r == 0 ? sm.ncand : ld_dsmem_u32(&sm.ncand, r);
-      ovf |= r == 0 ? sm.overflow : ld_dsmem_u32(&sm.overflow, r);
+    // every peer's count and overflow flag, then every peer's candidates, are
+    // requested before any of them is used: two round trips in all
+    uint32_t cnt[kSelClusterMax], off[kSelClusterMax], ovr[kSelClusterMax], n = 0, ovf = sm.overflow, maxc = 0;
+    cnt[0] = sm.ncand;
+#pragma unroll
+    for (int r = 1; r < kSelClusterMax; ++r) {
+      cnt[r] = 0;
+      ovr[r] = 0;
+      if (r < ncl) {
+        cnt[r] = ld_dsmem_u32(&sm.ncand, r);
+        ovr[r] = ld_dsmem_u32(&sm.overflow, r);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kSelClusterMax; ++r) {
+      if (r > 0) {
+        ovf |= ovr[r];
+        maxc = max(maxc, cnt[r]);
+      }
       off[r] = n;
       n += cnt[r];
     }
     const bool from_row = ovf != 0 || n > static_cast<uint32_t>(kSelCap);
     if (!from_row) {
-      for (uint32_t r = 1; r < static_cast<uint32_t>(ncl); ++r)
-        for (uint32_t i = tid; i < cnt[r]; i += kSelThreads) sm.cand[off[r] + i] = ld_dsmem_u64(&sm.cand[i], r);
+      for (uint32_t i = tid; i < maxc; i += kSelThreads) {
+        uint64_t v[kSelClusterMax];
+#pragma unroll
+        for (int r = 1; r < kSelClusterMax; ++r)
+          if (i < cnt[r]) v[r] = ld_dsmem_u64(&sm.cand[i], r);
+#pragma unroll
+        for (int r = 1; r < kSelClusterMax; ++r)
+          if (i < cnt[r]) sm.cand[off[r] + i] = v[r];
+      }
     }
     __syncthreads();
     if (tid == 0) sm.rem = need;
