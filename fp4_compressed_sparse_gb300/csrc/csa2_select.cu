@@ -230,7 +230,6 @@ __device__ __forceinline__ void pick_digit(const uint32_t *hist, int sh, uint32_
 }
 
 struct SelSmem {
-  uint32_t hist[kSelBins];
   uint64_t cand[kSelCap];  // this CTA's keys of the threshold bin; the leader then gathers everyone's
   uint32_t warp_tot[kSelWarps + 1];
   uint32_t dhist[256];
@@ -321,8 +320,21 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
 
   // ---- 1. threshold bin from the histogram (every CTA of the cluster, identically)
   {
-    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
-    for (int i = tid; i < kSelBins / 4; i += kSelThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
+    // thread t owns the bins kSelBins-1-per*t-i (thread 0 the top ones): per
+    // contiguous, 16-byte aligned counts, read straight into registers
+    constexpr int per = kSelBins / kSelThreads;
+    const int top = kSelBins - 1 - tid * per;
+    const uint32_t base = static_cast<uint32_t>(top - per + 1);  // hb[j] = count of bin base + j
+    uint32_t hb[per];
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p)) + base / 4;
+#pragma unroll
+    for (int q = 0; q < per / 4; ++q) {
+      const uint4 v = h4[q];
+      hb[4 * q] = v.x;
+      hb[4 * q + 1] = v.y;
+      hb[4 * q + 2] = v.z;
+      hb[4 * q + 3] = v.w;
+    }
     if (tid == 0) {
       sm.ncand = 0;
       sm.cnt_below = 0;
@@ -331,32 +343,30 @@ __global__ void __launch_bounds__(kSelThreads, 2) k_select(TopkArgs a, const uin
       sm.done = 0;
       sm.prefix = 0;
     }
-    __syncthreads();
-    // thread t owns the bins kSelBins-1-per*t-i (thread 0 the top ones)
-    constexpr int per = kSelBins / kSelThreads;
-    const int top = kSelBins - 1 - tid * per;
     uint32_t local = 0;
 #pragma unroll
-    for (int i = 0; i < per; ++i) local += sm.hist[top - ((i + tid) & (per - 1))];
+    for (int j = 0; j < per; ++j) local += hb[j];
     uint32_t total;
-    const uint32_t above = block_excl_scan(local, sm.warp_tot, &total);
+    const uint32_t above = block_excl_scan(local, sm.warp_tot, &total);  // also orders the writes above
     if (total <= k) {
-      if (tid == 0) {  // every valid slot is chosen: bin 0 is the threshold bin
+      if (base == 0) {  // the owner of bin 0: every valid slot is chosen, bin 0 is the threshold bin
         sm.thr = 0;
-        sm.above = total - sm.hist[0];
+        sm.above = total - hb[0];
         sm.total = total;
       }
     } else if (above < k && k <= above + local) {
       uint32_t acc = above;
+      bool found = false;
+#pragma unroll
       for (int i = 0; i < per; ++i) {
-        const uint32_t bin = top - i;
-        if (acc + sm.hist[bin] >= k) {
-          sm.thr = bin;
+        const uint32_t c = hb[per - 1 - i];  // bin top - i
+        if (!found && acc + c >= k) {
+          sm.thr = static_cast<uint32_t>(top - i);
           sm.above = acc;
           sm.total = total;
-          break;
+          found = true;
         }
-        acc += sm.hist[bin];
+        acc += c;
       }
     }
     __syncthreads();
@@ -576,7 +586,6 @@ constexpr int64_t kRowMaxSlots = 131072;
 constexpr int kRowMaxWords = static_cast<int>(kRowMaxSlots / 32);
 
 struct RowSmem {
-  uint32_t hist[kSelBins];
   uint64_t cand[kSelCap];
   uint32_t bitmap[kRowMaxWords];
   uint32_t warp_tot[kRowWarps + 1];
@@ -643,8 +652,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const
 
   // ---- 1. threshold bin from the histogram
   {
-    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p));
-    for (int i = tid; i < kSelBins / 4; i += kRowThreads) reinterpret_cast<uint4 *>(sm.hist)[i] = h4[i];
+    constexpr int per = kSelBins / kRowThreads;  // 8 contiguous bins per thread, thread 0 the top ones
+    const int top = kSelBins - 1 - tid * per;
+    const uint32_t base = static_cast<uint32_t>(top - per + 1);  // hb[j] = count of bin base + j
+    uint32_t hb[per];
+    const uint4 *h4 = reinterpret_cast<const uint4 *>(aux_hist(aux, aux_row, row, p)) + base / 4;
+#pragma unroll
+    for (int q = 0; q < per / 4; ++q) {
+      const uint4 v = h4[q];
+      hb[4 * q] = v.x;
+      hb[4 * q + 1] = v.y;
+      hb[4 * q + 2] = v.z;
+      hb[4 * q + 3] = v.w;
+    }
     for (int i = tid; i < nw; i += kRowThreads) sm.bitmap[i] = 0;
     if (tid == 0) {
       sm.ncand = 0;
@@ -653,31 +673,30 @@ __global__ void __launch_bounds__(kRowThreads, 1) k_select_row(TopkArgs a, const
       sm.done = 0;
       sm.prefix = 0;
     }
-    __syncthreads();
-    constexpr int per = kSelBins / kRowThreads;  // 8 bins per thread, thread 0 the top ones
-    const int top = kSelBins - 1 - tid * per;
     uint32_t local = 0;
 #pragma unroll
-    for (int i = 0; i < per; ++i) local += sm.hist[top - ((i + tid) & (per - 1))];
+    for (int j = 0; j < per; ++j) local += hb[j];
     uint32_t total;
-    const uint32_t above = row_excl_scan(local, sm.warp_tot, &total);
+    const uint32_t above = row_excl_scan(local, sm.warp_tot, &total);  // also orders the writes above
     if (total <= k) {
-      if (tid == 0) {  // every valid slot is chosen: bin 0 is the threshold bin
+      if (base == 0) {  // the owner of bin 0: every valid slot is chosen, bin 0 is the threshold bin
         sm.thr = 0;
-        sm.above = total - sm.hist[0];
+        sm.above = total - hb[0];
         sm.total = total;
       }
     } else if (above < k && k <= above + local) {
       uint32_t acc = above;
+      bool found = false;
+#pragma unroll
       for (int i = 0; i < per; ++i) {
-        const uint32_t bin = top - i;
-        if (acc + sm.hist[bin] >= k) {
-          sm.thr = bin;
+        const uint32_t c = hb[per - 1 - i];  // bin top - i
+        if (!found && acc + c >= k) {
+          sm.thr = static_cast<uint32_t>(top - i);
           sm.above = acc;
           sm.total = total;
-          break;
+          found = true;
         }
-        acc += sm.hist[bin];
+        acc += c;
       }
     }
     __syncthreads();
